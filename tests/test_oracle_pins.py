@@ -1,0 +1,415 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself (a library routine, autograd, finite differences, a closed form,
+invariants of softmax attention, brute force), chosen so that a plausible
+mistake (dropped term, wrong sign or index, transposed operand, wrong head
+group, wrong block index) fails at least one of them. ``test_planted_mistakes``
+plants such mistakes in the oracle and checks that the pins catch them."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import bsa_oracle as O
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rand(shape, seed, std=1.0):
+    return np.random.Generator(np.random.PCG64(seed)).standard_normal(shape) * std
+
+
+def _case(B=1, N1=2, N2=1, S=40, Skv=None, D=8, bx=8, by=8, p=0.5, seed=0, diag=True):
+    Skv = S if Skv is None else Skv
+    q = _rand((B, N1, S, D), seed)
+    k = _rand((B, N2, Skv, D), seed + 1)
+    v = _rand((B, N2, Skv, D), seed + 2)
+    do = _rand((B, N1, S, D), seed + 3)
+    Mq, Mk = -(-S // bx), -(-Skv // by)
+    rng = np.random.Generator(np.random.PCG64(seed + 4))
+    m = (rng.random((B, N1, Mq, Mk)) < p).astype(np.uint8)
+    if diag:
+        for i in range(min(Mq, Mk)):
+            m[:, :, i, i] = 1
+        m[:, :, :, 0] = np.maximum(m[:, :, :, 0], 1)   # every query row has a key
+    return q, k, v, do, m
+
+
+def _sdpa_fwd_bwd(q, k, v, do, m, bx, by, scale, G):
+    """torch SDPA (float64, CPU) with the block mask expanded to tokens."""
+    B, N1, S, D = q.shape
+    Skv = k.shape[2]
+    if m is None:
+        tm = np.ones((B, N1, S, Skv), dtype=bool)
+    else:   # expanded here with np.repeat, independently of the oracle
+        tm = np.repeat(np.repeat(np.asarray(m) != 0, bx, axis=2), by, axis=3)[:, :, :S, :Skv]
+    Q = torch.tensor(q, requires_grad=True)
+    K = torch.tensor(k, requires_grad=True)
+    V = torch.tensor(v, requires_grad=True)
+    Kr = K.repeat_interleave(G, dim=1)
+    Vr = V.repeat_interleave(G, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        Q, Kr, Vr, attn_mask=torch.tensor(tm), scale=scale)
+    out.backward(torch.tensor(do))
+    return out.detach().numpy(), Q.grad.numpy(), K.grad.numpy(), V.grad.numpy()
+
+
+# ---------------------------------------------------------------- forward pins
+@pytest.mark.parametrize("N1,N2,S,Skv,bx,by", [(2, 2, 40, 40, 8, 8), (4, 2, 33, 50, 8, 16),
+                                               (3, 1, 64, 24, 16, 8)])
+def test_forward_matches_sdpa(N1, N2, S, Skv, bx, by):
+    q, k, v, do, m = _case(N1=N1, N2=N2, S=S, Skv=Skv, bx=bx, by=by, seed=11)
+    out, lse = O.forward(q, k, v, m, (bx, by), num_kv_heads=N2, scale=0.37)
+    ref, *_ = _sdpa_fwd_bwd(q, k, v, do, m, bx, by, 0.37, N1 // N2)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    # lse against its definition, spelled out per row with the math library
+    b, h, s = 0, N1 - 1, S - 1
+    keys = [t for t in range(Skv) if m[b, h, s // bx, t // by]]
+    g = h // (N1 // N2)
+    xs = [0.37 * float(np.dot(q[b, h, s], k[b, g, t])) for t in keys]
+    mx = max(xs)
+    assert abs(lse[b, h, s, 0] - (mx + math.log(sum(math.exp(x - mx) for x in xs)))) < 1e-12
+
+
+def test_forward_dense_matches_sdpa_no_mask():
+    q, k, v, do, _ = _case(N1=2, N2=1, S=48, D=16)
+    out, _ = O.forward(q, k, v, None, (16, 16), num_kv_heads=1, scale=0.25)
+    ref, *_ = _sdpa_fwd_bwd(q, k, v, do, None, 16, 16, 0.25, 2)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_blockrows_matches_forward():
+    q, k, v, do, m = _case(N1=4, N2=2, S=70, Skv=90, bx=16, by=32, seed=5, diag=False)
+    m[0, 1, 2, :] = 0                                   # an empty query block row
+    a = O.forward(q, k, v, m, (16, 32), num_kv_heads=2, scale=0.5)
+    b = O.forward_blockrows(q, k, v, m, (16, 32), num_kv_heads=2, scale=0.5)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(np.isinf(a[1]), np.isinf(b[1]))
+    fin = np.isfinite(a[1])
+    np.testing.assert_allclose(a[1][fin], b[1][fin], rtol=1e-12, atol=1e-12)
+    # reading R6: an empty row has out 0 and lse -inf
+    assert np.all(a[0][0, 1, 32:48] == 0) and np.all(np.isneginf(a[1][0, 1, 32:48]))
+
+
+# --------------------------------------------------------------- backward pins
+@pytest.mark.parametrize("N1,N2,S,Skv,D,bx,by,seed", [(2, 2, 40, 40, 8, 8, 8, 1),
+                                                      (4, 2, 37, 52, 16, 8, 16, 2),
+                                                      (4, 1, 64, 64, 8, 16, 16, 3),
+                                                      (2, 1, 24, 70, 4, 8, 32, 4)])
+def test_backward_matches_sdpa_autograd(N1, N2, S, Skv, D, bx, by, seed):
+    q, k, v, do, m = _case(N1=N1, N2=N2, S=S, Skv=Skv, D=D, bx=bx, by=by, seed=seed)
+    scale = D ** -0.5
+    out, lse = O.forward(q, k, v, m, (bx, by), num_kv_heads=N2, scale=scale)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, m, (bx, by), num_kv_heads=N2, scale=scale)
+    _, gq, gk, gv = _sdpa_fwd_bwd(q, k, v, do, m, bx, by, scale, N1 // N2)
+    for a, b in ((dq, gq), (dk, gk), (dv, gv)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+
+
+def test_backward_finite_differences():
+    """Central differences of L = <dOut, Out(Q, K, V)> on a tiny case."""
+    q, k, v, do, m = _case(B=1, N1=2, N2=1, S=12, Skv=10, D=4, bx=4, by=4, seed=21)
+    scale, bs = 0.6, (4, 4)
+
+    def loss(q_, k_, v_):
+        o, _ = O.forward(q_, k_, v_, m, bs, num_kv_heads=1, scale=scale)
+        return float((o * do).sum())
+
+    out, lse = O.forward(q, k, v, m, bs, num_kv_heads=1, scale=scale)
+    grads = O.backward(do, q, k, v, out, lse, m, bs, num_kv_heads=1, scale=scale)
+    h = 1e-6
+    for which, (x, g) in enumerate(zip((q, k, v), grads)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which], args_m[which] = xp, xm
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(fd - g).max() / max(1e-3, np.abs(g).max())
+        assert err < 1e-6, (which, err)
+
+
+def test_softmax_shift_invariants():
+    """Shifting every key by c leaves the softmax unchanged, so sum_t dK_t = 0
+    (equivalently sum_t dS_st = 0 per row); shifting every value by c shifts Out
+    by c, so sum_t dV_t = sum over rows with keys of dOut_s. Both need a
+    consistent fp64 Out and lse."""
+    q, k, v, do, m = _case(N1=4, N2=2, S=50, Skv=45, D=8, bx=8, by=8, seed=31, diag=False)
+    m[0, 0, 3, :] = 0                              # rows 24..31 of head 0: no keys
+    out, lse = O.forward(q, k, v, m, (8, 8), num_kv_heads=2, scale=0.4)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, m, (8, 8), num_kv_heads=2, scale=0.4)
+    assert np.abs(dk.sum(axis=2)).max() < 1e-12 * max(1.0, np.abs(dk).max()) * 100
+    has = np.isfinite(lse[..., 0])
+    rhs = np.where(has[..., None], do, 0.0).reshape(1, 2, 2, 50, 8).sum(axis=(2, 3))
+    np.testing.assert_allclose(dv.sum(axis=2), rhs, rtol=1e-10, atol=1e-10)
+    assert np.all(dq[0, 0, 24:32] == 0)
+
+
+def test_null_mask_equals_all_ones():
+    q, k, v, do, _ = _case(N1=2, N2=1, S=40, Skv=40, D=8)
+    ones = np.ones((1, 2, 5, 5), np.uint8)
+    out, lse = O.forward(q, k, v, None, (8, 8), num_kv_heads=1, scale=0.3)
+    a = O.backward(do, q, k, v, out, lse, None, (8, 8), num_kv_heads=1, scale=0.3)
+    b = O.backward(do, q, k, v, out, lse, ones, (8, 8), num_kv_heads=1, scale=0.3)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_unselected_blocks_contribute_nothing():
+    q, k, v, do, m = _case(N1=2, N2=1, S=32, Skv=48, D=8, bx=8, by=8, seed=41, diag=False)
+    m[:, :, :, 0] = 1
+    m[:, :, :, 3] = 0                                   # key block 3 (rows 24..31): unused
+    out, lse = O.forward(q, k, v, m, (8, 8), num_kv_heads=1, scale=0.5)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, m, (8, 8), num_kv_heads=1, scale=0.5)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, 24:32] += 100.0
+    v2[:, :, 24:32] -= 100.0
+    dq2, dk2, dv2 = O.backward(do, q, k2, v2, out, lse, m, (8, 8), num_kv_heads=1, scale=0.5)
+    np.testing.assert_array_equal(dq, dq2)
+    assert np.all(dk[:, :, 24:32] == 0) and np.all(dv[:, :, 24:32] == 0)
+    assert np.all(dk2[:, :, 24:32] == 0) and np.all(dv2[:, :, 24:32] == 0)
+
+
+def test_bits_outside_valid_range_are_ignored():
+    q, k, v, do, m = _case(N1=2, N2=1, S=64, Skv=64, D=8, bx=16, by=16, seed=51)
+    sq, skv = [37], [45]                                # BNSD with actual lengths
+    out, lse = O.forward(q, k, v, m, (16, 16), sq, skv, num_kv_heads=1, scale=0.5)
+    a = O.backward(do, q, k, v, out, lse, m, (16, 16), sq, skv, num_kv_heads=1, scale=0.5)
+    m2 = m.copy()
+    m2[:, :, 3, :] = 1                                  # block row 3 starts at 48 >= 37
+    m2[:, :, :, 3] = 1                                  # block col 3 starts at 48 >= 45
+    b = O.backward(do, q, k, v, out, lse, m2, (16, 16), sq, skv, num_kv_heads=1, scale=0.5)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    assert np.all(a[0][:, :, 37:] == 0) and np.all(a[1][:, :, 45:] == 0)
+    # padding contents do not matter
+    q3, k3 = q.copy(), k.copy()
+    q3[:, :, 37:] = 1e6
+    k3[:, :, 45:] = -1e6
+    c = O.backward(do, q3, k3, v, out, lse, m, (16, 16), sq, skv, num_kv_heads=1, scale=0.5)
+    for x, y in zip(a, c):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_page_call_example_closed_form():
+    """The page's call example: q = k = v = out = 0.1, dout = 0.01 (fp16), lse = 5,
+    S = 128, D = 128, 64x64 blocks, all-ones mask, scale = 1/sqrt(128)."""
+    with open(os.path.join(HERE, "golden", "p1_call_example.json")) as f:
+        g = json.load(f)
+    S, D = g["q_seqlen"], g["head_dim"]
+    x = float(np.float16(g["q_k_v_out_value"]))
+    assert x == g["q_k_v_out_f16"]
+    d = float(np.float16(g["dout_value"]))
+    assert d == g["dout_f16"]
+    q = np.full((1, 1, S, D), x)
+    dout = np.full((1, 1, S, D), d)
+    lse = np.full((1, 1, S), g["lse_value"])
+    mask = np.ones((1, 1, 2, 2), np.uint8)
+    scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = O.backward(dout, q, q, q, q, lse, mask, tuple(g["block_shape"]),
+                            num_kv_heads=1, scale=scale)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    expect = S * math.exp(scale * D * x * x - g["lse_value"]) * d
+    assert abs(expect - g["closed_form"]["dv_value"]) < 1e-15
+    np.testing.assert_allclose(dv, expect, rtol=1e-12)
+
+
+def test_gqa_equals_mha_with_repeated_heads():
+    q, k, v, do, m = _case(N1=6, N2=2, S=30, Skv=40, D=8, bx=8, by=8, seed=61)
+    out, lse = O.forward(q, k, v, m, (8, 8), num_kv_heads=2, scale=0.4)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, m, (8, 8), num_kv_heads=2, scale=0.4)
+    kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+    dq2, dk2, dv2 = O.backward(do, q, kr, vr, out, lse, m, (8, 8), num_kv_heads=6, scale=0.4)
+    np.testing.assert_allclose(dq, dq2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dk, dk2.reshape(1, 2, 3, 40, 8).sum(2), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv, dv2.reshape(1, 2, 3, 40, 8).sum(2), rtol=1e-12, atol=1e-13)
+
+
+def test_tnd_equals_bnsd_per_sequence():
+    lens_q, lens_k = [13, 30, 7], [21, 9, 30]
+    N1, N2, D, bx, by = 4, 2, 8, 8, 8
+    Mq, Mk = 4, 4
+    rng = np.random.Generator(np.random.PCG64(71))
+    m = (rng.random((3, N1, Mq, Mk)) < 0.6).astype(np.uint8)
+    m[:, :, :, 0] = 1
+    qt = _rand((sum(lens_q), N1, D), 72)
+    kt = _rand((sum(lens_k), N2, D), 73)
+    vt = _rand((sum(lens_k), N2, D), 74)
+    dot = _rand((sum(lens_q), N1, D), 75)
+    out, lse = O.forward(qt, kt, vt, m, (bx, by), lens_q, lens_k, "TND", N2, 0.3)
+    dq, dk, dv = O.backward(dot, qt, kt, vt, out, lse, m, (bx, by), lens_q, lens_k, "TND", N2, 0.3)
+    oq, ok = O.seq_offsets(lens_q), O.seq_offsets(lens_k)
+    for b in range(3):
+        sl_q, sl_k = slice(oq[b], oq[b + 1]), slice(ok[b], ok[b + 1])
+        to_bnsd = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2))[None]
+        o1, l1 = O.forward(to_bnsd(qt[sl_q]), to_bnsd(kt[sl_k]), to_bnsd(vt[sl_k]),
+                           m[b:b + 1], (bx, by), num_kv_heads=N2, scale=0.3)
+        np.testing.assert_allclose(o1[0].transpose(1, 0, 2), out[sl_q], rtol=1e-13, atol=1e-14)
+        g1 = O.backward(to_bnsd(dot[sl_q]), to_bnsd(qt[sl_q]), to_bnsd(kt[sl_k]), to_bnsd(vt[sl_k]),
+                        o1, l1, m[b:b + 1], (bx, by), num_kv_heads=N2, scale=0.3)
+        for x, y, sl in zip(g1, (dq, dk, dv), (sl_q, sl_k, sl_k)):
+            np.testing.assert_allclose(x[0].transpose(1, 0, 2), y[sl], rtol=1e-12, atol=1e-13)
+
+
+def test_bruteforce_every_tiny_mask():
+    """B = N = 1, S = 8, 4x4 blocks: all 16 masks against SDPA + autograd."""
+    q, k, v, do, _ = _case(B=1, N1=1, N2=1, S=8, D=4, bx=4, by=4, seed=81)
+    for bits in range(16):
+        m = np.array([(bits >> i) & 1 for i in range(4)], np.uint8).reshape(1, 1, 2, 2)
+        out, lse = O.forward(q, k, v, m, (4, 4), num_kv_heads=1, scale=0.7)
+        dq, dk, dv = O.backward(do, q, k, v, out, lse, m, (4, 4), num_kv_heads=1, scale=0.7)
+        rows_with_keys = [i for i in range(2) if m[0, 0, i].any()]
+        if len(rows_with_keys) < 2:
+            # SDPA gives NaN for rows without keys; check them by reading R6
+            for i in range(2):
+                if i not in rows_with_keys:
+                    assert np.all(out[0, 0, 4 * i:4 * i + 4] == 0)
+                    assert np.all(dq[0, 0, 4 * i:4 * i + 4] == 0)
+            if not rows_with_keys:
+                assert np.all(dk == 0) and np.all(dv == 0)
+                continue
+            r = slice(4 * rows_with_keys[0], 4 * rows_with_keys[0] + 4)
+            ref, gq, gk, gv = _sdpa_fwd_bwd(q[:, :, r], k, v, do[:, :, r],
+                                            m[:, :, rows_with_keys[0]:rows_with_keys[0] + 1],
+                                            4, 4, 0.7, 1)
+            np.testing.assert_allclose(out[:, :, r], ref, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(dq[:, :, r], gq, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dk, gk, rtol=1e-10, atol=1e-12)
+            np.testing.assert_allclose(dv, gv, rtol=1e-10, atol=1e-12)
+            continue
+        ref, gq, gk, gv = _sdpa_fwd_bwd(q, k, v, do, m, 4, 4, 0.7, 1)
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+        for a, b in ((dq, gq), (dk, gk), (dv, gv)):
+            np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-12)
+
+
+def test_sampled_rows_match_full_backward():
+    q, k, v, do, m = _case(N1=4, N2=2, S=60, Skv=50, D=8, bx=16, by=8, seed=91)
+    out, lse = O.forward(q, k, v, m, (16, 8), num_kv_heads=2, scale=0.3)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, m, (16, 8), num_kv_heads=2, scale=0.3)
+    rows = np.array([0, 17, 59])
+    np.testing.assert_allclose(
+        O.backward_dq_rows(do, q, k, v, out, lse, 0, 3, rows, m, (16, 8), num_kv_heads=2, scale=0.3),
+        dq[0, 3, rows], rtol=1e-13, atol=1e-14)
+    a, b = O.backward_dkdv_rows(do, q, k, v, out, lse, 0, 1, np.array([1, 25, 49]), m, (16, 8),
+                                num_kv_heads=2, scale=0.3)
+    np.testing.assert_allclose(a, dk[0, 1, [1, 25, 49]], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b, dv[0, 1, [1, 25, 49]], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------ compaction pins
+def test_compaction_brute_force():
+    rng = np.random.Generator(np.random.PCG64(101))
+    B, N, Mq, Mk, bx, by = 2, 3, 7, 5, 16, 32
+    m = (rng.random((B, N, Mq, Mk)) < 0.4).astype(np.uint8) * rng.integers(1, 255, (B, N, Mq, Mk)).astype(np.uint8)
+    sq, skv = [100, 112], [150, 70]                     # clips rows/cols per batch
+    rp, ci, cp, ri = O.compact_mask(m, bx, by, sq, skv)
+    assert rp.dtype == np.int32 and len(rp) == B * N * (Mq + 1) and len(cp) == B * N * (Mk + 1)
+    dense_r = np.zeros_like(m, dtype=bool)
+    dense_c = np.zeros_like(m, dtype=bool)
+    for b in range(B):
+        for h in range(N):
+            sl = b * N + h
+            for i in range(Mq):
+                cols = ci[rp[sl * (Mq + 1) + i]:rp[sl * (Mq + 1) + i + 1]]
+                assert np.all(np.diff(cols) > 0)
+                dense_r[b, h, i, cols] = True
+            for j in range(Mk):
+                rws = ri[cp[sl * (Mk + 1) + j]:cp[sl * (Mk + 1) + j + 1]]
+                assert np.all(np.diff(rws) > 0)
+                dense_c[b, h, rws, j] = True
+    valid = np.zeros_like(dense_r)
+    for b in range(B):
+        valid[b, :, :-(-sq[b] // bx), :-(-skv[b] // by)] = True
+    expect = (m != 0) & valid
+    np.testing.assert_array_equal(dense_r, expect)
+    np.testing.assert_array_equal(dense_c, expect)
+    assert len(ci) == len(ri) == int(expect.sum())
+
+
+# -------------------------------------------------------- planted mistakes
+def _planted(kind):
+    def head_backward(Qm, Km, Vm, dOm, Om, lse, M, scale):
+        Dv = (dOm * Om).sum(axis=1)
+        if kind == "drop_D":
+            Dv = 0 * Dv
+        S = scale * (Qm @ Km.T)
+        if kind == "lse_sign":
+            S = S + 2 * lse[:, None]
+        P = np.where(M, np.exp(np.where(M, S - lse[:, None], 0.0)), 0.0)
+        if kind == "mask_ignored":
+            P = np.exp(np.minimum(S - lse[:, None], 50.0))
+        dP = dOm @ Vm.T
+        dS = P * (dP - Dv[:, None])
+        if kind == "dS_sign":
+            dS = P * (Dv[:, None] - dP)
+        dV = P.T @ dOm
+        if kind == "dV_uses_dS":
+            dV = dS.T @ dOm
+        dQ = scale * (dS @ Km)
+        if kind == "dq_no_scale":
+            dQ = dS @ Km
+        dK = scale * (dS.T @ Qm)
+        if kind == "dk_uses_P":
+            dK = scale * (P.T @ Qm)
+        return dQ, dK, dV
+    return head_backward
+
+
+PINS = [
+    lambda: test_backward_matches_sdpa_autograd(4, 2, 37, 52, 16, 8, 16, 2),
+    test_softmax_shift_invariants,
+    test_page_call_example_closed_form,
+    test_unselected_blocks_contribute_nothing,
+]
+
+
+@pytest.mark.parametrize("kind", ["drop_D", "lse_sign", "mask_ignored", "dS_sign",
+                                  "dV_uses_dS", "dq_no_scale", "dk_uses_P"])
+def test_planted_mistakes_are_caught(kind, monkeypatch):
+    monkeypatch.setattr(O, "_head_backward", _planted(kind))
+    caught = 0
+    for pin in PINS:
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
+    assert caught >= 1, kind
+
+
+def test_planted_block_index_mistake_is_caught(monkeypatch):
+    """mask[b, h, j, i] read instead of mask[b, h, i, j]."""
+    real = O.token_mask
+    monkeypatch.setattr(O, "token_mask", lambda bm, bx, by, Lq, Lk:
+                        real(None if bm is None else np.asarray(bm).T, bx, by, Lq, Lk))
+    with pytest.raises(AssertionError):
+        test_backward_matches_sdpa_autograd(2, 2, 40, 40, 8, 8, 8, 1)
+
+
+def test_planted_gqa_mapping_mistake_is_caught(monkeypatch):
+    """Query head h paired with key head h % N2 instead of h // (N1/N2)."""
+    def wrong(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=None,
+              seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0):
+        B, N1, S, D = q.shape
+        N2, Skv = k.shape[1], k.shape[2]
+        dq = np.zeros(q.shape)
+        dk = np.zeros(k.shape)
+        dv = np.zeros(v.shape)
+        for b in range(B):
+            for h in range(N1):
+                g = h % N2
+                M = O.token_mask(mask[b, h], block_shape[0], block_shape[1], S, Skv)
+                a, c, e = O._head_backward(q[b, h], k[b, g], v[b, g], dout[b, h], out[b, h],
+                                           lse[b, h, :, 0], M, scale)
+                dq[b, h] = a
+                dk[b, g] += c
+                dv[b, g] += e
+        return dq, dk, dv
+    monkeypatch.setattr(O, "backward", wrong)
+    with pytest.raises(AssertionError):
+        test_backward_matches_sdpa_autograd(4, 2, 37, 52, 16, 8, 16, 2)
