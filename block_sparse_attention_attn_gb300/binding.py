@@ -1,0 +1,261 @@
+"""ctypes binding of libbsa (include/bsa.h): argument marshalling only.
+
+Every function named like a C entry point takes torch tensors (device memory
+owned by the caller), builds the ``bsa_tensor`` descriptors and calls the
+library; all computation happens in the library's CUDA kernels. If the library
+has not been built, every call raises :class:`BsaError` (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libbsa.so")
+_lib = None
+
+BSA_OK = 0
+BSA_ERR_PARAM_NULLPTR = 161001
+BSA_ERR_PARAM_INVALID = 161002
+BSA_ERR_RUNTIME = 361001
+BSA_ERR_INNER = 561002
+
+_DTYPES = {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3, torch.uint8: 4, torch.bool: 4}
+
+
+class BsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"libbsa status {status}: {message}")
+        self.status = status
+
+
+class BsaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads libbsa.so (once). Raises BsaError when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise BsaError(BSA_ERR_RUNTIME, f"{_LIB_PATH} not built; run "
+                       "`python -m block_sparse_attention_attn_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.POINTER
+    T = P(BsaTensor)
+    i64, u64, vp = ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
+    lib.bsa_grad_workspace_size.argtypes = [
+        T, T, T, T, T, T, T, T, P(i64), i64, P(i64), i64, P(i64), i64, ctypes.c_char_p,
+        ctypes.c_char_p, i64, i64, ctypes.c_double, i64, i64, T, T, T, P(u64), P(vp)]
+    lib.bsa_grad.argtypes = [vp, u64, vp, vp]
+    lib.bsa_fwd_workspace_size.argtypes = [
+        T, T, T, T, P(i64), i64, P(i64), i64, P(i64), i64, ctypes.c_char_p, ctypes.c_char_p,
+        i64, ctypes.c_double, T, T, P(u64), P(vp)]
+    lib.bsa_fwd.argtypes = [vp, u64, vp, vp]
+    lib.bsa_executor_destroy.argtypes = [vp]
+    lib.bsa_mask_compact_workspace_size.argtypes = [T, i64, i64, P(u64)]
+    lib.bsa_mask_compact.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp, vp, vp,
+                                     u64, vp]
+    lib.bsa_check_status.argtypes = [vp, vp]
+    lib.bsa_last_error.restype = ctypes.c_char_p
+    lib.bsa_version.restype = ctypes.c_int32
+    for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
+                 "bsa_executor_destroy", "bsa_mask_compact_workspace_size", "bsa_mask_compact",
+                 "bsa_check_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != BSA_OK:
+        raise BsaError(status, load_library().bsa_last_error().decode())
+
+
+def _desc(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    d = BsaTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return ctypes.byref(d), d
+
+
+def _ptr(x):
+    return None if x is None else x[0]
+
+
+def _i64_array(v: Optional[Sequence[int]]):
+    if v is None:
+        return None, 0
+    arr = (ctypes.c_int64 * len(v))(*[int(a) for a in v])
+    return arr, len(v)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class Executor:
+    """Owns a C executor until a run call consumes it."""
+
+    def __init__(self, handle: int, keep):
+        self.handle = handle
+        self._keep = keep   # the descriptors' tensors must outlive the run
+
+    def take(self) -> int:
+        h, self.handle = self.handle, None
+        if h is None:
+            raise BsaError(BSA_ERR_PARAM_NULLPTR, "executor already consumed")
+        return h
+
+    def __del__(self):
+        if getattr(self, "handle", None) is not None and _lib is not None:
+            _lib.bsa_executor_destroy(self.handle)
+
+
+def bsa_grad_workspace_size(dout, query, key, value, attention_out, softmax_lse,
+                            block_sparse_mask=None, atten_mask=None, block_shape=None,
+                            actual_seq_lengths=None, actual_seq_lengths_kv=None,
+                            q_layout="BNSD", kv_layout=None, num_key_value_heads=None,
+                            mask_type=0, scale_value=1.0, pre_tokens=2147483647,
+                            next_tokens=2147483647, dq=None, dk=None, dv=None):
+    """First stage of the backward. Returns (workspace_size, Executor)."""
+    lib = load_library()
+    kv_layout = q_layout if kv_layout is None else kv_layout
+    if num_key_value_heads is None:
+        num_key_value_heads = key.shape[1]
+    ds = [_desc(t) for t in (dout, query, key, value, attention_out, softmax_lse,
+                             block_sparse_mask, atten_mask, dq, dk, dv)]
+    bs, nbs = _i64_array(block_shape)
+    sq, nsq = _i64_array(actual_seq_lengths)
+    sk, nsk = _i64_array(actual_seq_lengths_kv)
+    ws = ctypes.c_uint64(0)
+    ex = ctypes.c_void_p(None)
+    _check(lib.bsa_grad_workspace_size(
+        *[_ptr(d) for d in ds[:8]], bs, nbs, sq, nsq, sk, nsk, q_layout.encode(),
+        kv_layout.encode(), int(num_key_value_heads), int(mask_type), float(scale_value),
+        int(pre_tokens), int(next_tokens), *[_ptr(d) for d in ds[8:]], ctypes.byref(ws),
+        ctypes.byref(ex)))
+    return ws.value, Executor(ex.value, ds)
+
+
+def bsa_grad(workspace: torch.Tensor, workspace_size: int, executor: Executor, stream=None):
+    """Second stage of the backward; asynchronous on `stream` (default: current)."""
+    lib = load_library()
+    _check(lib.bsa_grad(workspace.data_ptr(), int(workspace_size), executor.take(),
+                        _stream(stream)))
+
+
+def bsa_fwd_workspace_size(query, key, value, block_sparse_mask=None, block_shape=None,
+                           actual_seq_lengths=None, actual_seq_lengths_kv=None,
+                           q_layout="BNSD", kv_layout=None, num_key_value_heads=None,
+                           scale_value=1.0, attention_out=None, softmax_lse=None):
+    lib = load_library()
+    kv_layout = q_layout if kv_layout is None else kv_layout
+    if num_key_value_heads is None:
+        num_key_value_heads = key.shape[1]
+    ds = [_desc(t) for t in (query, key, value, block_sparse_mask, attention_out, softmax_lse)]
+    bs, nbs = _i64_array(block_shape)
+    sq, nsq = _i64_array(actual_seq_lengths)
+    sk, nsk = _i64_array(actual_seq_lengths_kv)
+    ws = ctypes.c_uint64(0)
+    ex = ctypes.c_void_p(None)
+    _check(lib.bsa_fwd_workspace_size(
+        _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ds[3]), bs, nbs, sq, nsq, sk, nsk,
+        q_layout.encode(), kv_layout.encode(), int(num_key_value_heads), float(scale_value),
+        _ptr(ds[4]), _ptr(ds[5]), ctypes.byref(ws), ctypes.byref(ex)))
+    return ws.value, Executor(ex.value, ds)
+
+
+def bsa_fwd(workspace: torch.Tensor, workspace_size: int, executor: Executor, stream=None):
+    lib = load_library()
+    _check(lib.bsa_fwd(workspace.data_ptr(), int(workspace_size), executor.take(), _stream(stream)))
+
+
+def bsa_check_status(workspace: torch.Tensor, stream=None):
+    lib = load_library()
+    _check(lib.bsa_check_status(workspace.data_ptr(), _stream(stream)))
+
+
+def bsa_mask_compact(mask: torch.Tensor, bx: int, by: int, actual_seq_lengths=None,
+                     actual_seq_lengths_kv=None, stream=None):
+    """Block-level CSR/CSC of a block mask: (row_ptr, col_idx, col_ptr, row_idx),
+    int32 device tensors; col_idx/row_idx trimmed to nnz."""
+    lib = load_library()
+    B, N, Mq, Mk = mask.shape
+    d = _desc(mask)
+    need = ctypes.c_uint64(0)
+    _check(lib.bsa_mask_compact_workspace_size(d[0], int(bx), int(by), ctypes.byref(need)))
+    dev = mask.device
+    ws = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+    row_ptr = torch.empty(B * N * (Mq + 1), dtype=torch.int32, device=dev)
+    col_ptr = torch.empty(B * N * (Mk + 1), dtype=torch.int32, device=dev)
+    col_idx = torch.empty(max(B * N * Mq * Mk, 1), dtype=torch.int32, device=dev)
+    row_idx = torch.empty(max(B * N * Mq * Mk, 1), dtype=torch.int32, device=dev)
+    sq, nsq = _i64_array(actual_seq_lengths)
+    sk, nsk = _i64_array(actual_seq_lengths_kv)
+    _check(lib.bsa_mask_compact(d[0], int(bx), int(by), sq, nsq, sk, nsk, row_ptr.data_ptr(),
+                                col_idx.data_ptr(), col_ptr.data_ptr(), row_idx.data_ptr(),
+                                ws.data_ptr(), int(need.value), _stream(stream)))
+    torch.cuda.synchronize(dev)
+    nnz = int(row_ptr[-1].item())
+    return row_ptr, col_idx[:nnz], col_ptr, row_idx[:nnz]
+
+
+def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_lse,
+                                block_sparse_mask=None, block_shape=None,
+                                actual_seq_lengths=None, actual_seq_lengths_kv=None,
+                                layout="BNSD", num_key_value_heads=None, scale_value=None,
+                                dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Both stages; allocates outputs/workspace with torch when not given.
+    Returns (dq, dk, dv, workspace)."""
+    if scale_value is None:
+        scale_value = query.shape[-1] ** -0.5
+    dq = torch.empty_like(query) if dq is None else dq
+    dk = torch.empty_like(key) if dk is None else dk
+    dv = torch.empty_like(value) if dv is None else dv
+    size, ex = bsa_grad_workspace_size(
+        dout, query, key, value, attention_out, softmax_lse, block_sparse_mask, None,
+        block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
+        num_key_value_heads, 0, scale_value, dq=dq, dk=dk, dv=dv)
+    if workspace is None or workspace.numel() < size:
+        workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=query.device)
+    bsa_grad(workspace, size, ex, stream)
+    return dq, dk, dv, workspace
+
+
+def block_sparse_attention_fwd(query, key, value, block_sparse_mask=None, block_shape=None,
+                               actual_seq_lengths=None, actual_seq_lengths_kv=None,
+                               layout="BNSD", num_key_value_heads=None, scale_value=None,
+                               out=None, lse=None, workspace=None, stream=None):
+    """Companion forward; returns (out, lse [..., 1] fp32, workspace)."""
+    if scale_value is None:
+        scale_value = query.shape[-1] ** -0.5
+    out = torch.empty_like(query) if out is None else out
+    if lse is None:
+        lse = torch.empty((*query.shape[:-1], 1), dtype=torch.float32, device=query.device)
+    size, ex = bsa_fwd_workspace_size(query, key, value, block_sparse_mask, block_shape,
+                                      actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
+                                      num_key_value_heads, scale_value, out, lse)
+    if workspace is None or workspace.numel() < size:
+        workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=query.device)
+    bsa_fwd(workspace, size, ex, stream)
+    return out, lse, workspace

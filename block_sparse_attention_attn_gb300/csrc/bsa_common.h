@@ -1,0 +1,115 @@
+// bsa_common.h - plan structures shared by the host planner and the kernels.
+//
+// Terminology (aclnnBlockSparseAttentionGrad page, parameter table):
+//   B batch, N1 query heads, N2 = numKeyValueHeads, G = N1/N2, D head dim,
+//   bx/by = blockShape (query / key direction), Mq/Mk = mask block counts.
+// The kernels work on 128x128 token tiles: a tile holds rb = 128/bx query
+// blocks and cb = 128/by key blocks (1 or 2 each); a tile takes part when any
+// of its blocks is selected, and the blocks it holds but that are not selected
+// are masked out element by element ("sub-block mask", 4 bits).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bsa {
+
+constexpr int kTile = 128;            // tile rows (query and key direction)
+constexpr int kLayoutBNSD = 0;
+constexpr int kLayoutTND = 1;
+constexpr int kDtF16 = 1;
+constexpr int kDtBF16 = 2;
+
+// header words at the start of every workspace
+enum HeaderWord {
+  kHdrError = 0,       // nonzero: a kernel gave up (bounded wait / bad state)
+  kHdrWorkCounter = 1, // persistent-kernel work queue head
+  kHdrNumItems = 2,    // number of backward work items
+  kHdrTotalTiles = 3,  // active tiles
+  kHdrSlotsUsed = 4,   // split columns that got an fp32 partial slot
+  kHdrChunkLen = 5,    // split threshold used
+  kHdrErrorWhere = 6,  // code of the wait that gave up
+  kHdrWords = 64
+};
+
+// Error codes written to kHdrErrorWhere (first failure wins).
+enum ErrWhere {
+  kErrNone = 0,
+  kErrSmemAlign = 1,
+  kErrWaitItem = 2,
+  kErrWaitKV = 3,
+  kErrWaitQ = 4,
+  kErrWaitS = 5,
+  kErrWaitDP = 6,
+  kErrWaitP = 7,
+  kErrWaitDS = 8,
+  kErrWaitDQ = 9,
+  kErrWaitAcc = 10,
+  kErrWaitMisc = 11,
+};
+
+// Entry of a backward work list: query tile `it` of local head `hl`, with the
+// sub-block mask in bits 28..31 (bit (ri*2 + cj) = query block ri, key block cj
+// of the tile).
+__host__ __device__ inline int32_t pack_entry(int it, int hl, int sub) {
+  return (it & 0xFFFFF) | ((hl & 0xFF) << 20) | ((sub & 0xF) << 28);
+}
+__host__ __device__ inline int entry_it(int32_t e) { return e & 0xFFFFF; }
+__host__ __device__ inline int entry_hl(int32_t e) { return (e >> 20) & 0xFF; }
+__host__ __device__ inline int entry_sub(int32_t e) { return (int)(((uint32_t)e) >> 28); }
+
+// Everything the kernels need, passed by value.
+struct Plan {
+  // problem
+  int B, N1, N2, G, D;
+  int bx, by, rb, cb;      // block shape, blocks per tile
+  int Mq, Mk;              // mask dims (blocks); 0 when the mask is null
+  int Mq_t, Mk_t;          // max tiles per sequence (query / key)
+  int layout, dtype;
+  int has_mask;
+  int Sq, Skv;             // BNSD padded lengths (TND: longest sequence)
+  int Tq, Tkv;             // TND token totals (BNSD: 0)
+  float scale, scale_log2; // scale, scale*log2(e)
+  // tensors (device)
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const void* out;
+  const float* lse;
+  const uint8_t* mask;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t mask_sb, mask_sh, mask_si;    // mask strides (b, h, i); j stride 1
+  int64_t dq_st[4], dk_st[4], dv_st[4]; // output strides (elements), layout order
+  int dq_vec, dkv_vec;                  // outputs allow 16-byte row stores
+  // per-batch info in the workspace (int32 [B] each)
+  const int* lq;
+  const int* lk;
+  const int* cu_q;       // TND token offsets (BNSD: 0)
+  const int* cu_k;
+  const int* qrow;       // padded query-row offset of batch b (multiple of 128)
+  const int* krow;       // padded key-tile offset of batch b (in tiles)
+  const int* qtile_b;    // batch of padded query tile r/128
+  int Rq;                // padded query rows per head (sum of 128*ceil(lq/128))
+  int n_qtiles;          // Rq / 128
+  // workspace arrays
+  int* header;
+  float* lse2;           // [N1][Rq] lse*log2(e) (0 on padding rows)
+  float* dvec;           // [N1][Rq] rowsum(dout*out) (0 on padding rows)
+  float* dqacc;          // [N1][Rq][D] fp32 dQ accumulator
+  int* colcnt;           // [NC] active tiles of grouped column (b,g,jt,hl)
+  int* colptr;           // [NC+1]
+  int32_t* entries;      // [max_entries]
+  int4* items;           // [max_items] {gcol, e_begin, e_end, slot}
+  int* colinfo;          // [NGC] -1 empty, -2 single item, >=0 slot
+  float* slots;          // [max_slots][2][128][D] fp32 dK, dV partials
+  int NC;                // B*N2*Mk_t*G grouped columns
+  int NGC;               // B*N2*Mk_t key tiles
+  int max_items, max_slots, max_entries;
+  int num_sms;
+  int min_chunk;         // smallest split chunk
+};
+
+}  // namespace bsa

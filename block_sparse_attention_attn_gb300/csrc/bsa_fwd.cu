@@ -1,0 +1,538 @@
+// bsa_fwd.cu - companion block-sparse attention forward on the sm_103a tensor
+// cores: Out = softmax(scale * Q K^T over the selected blocks) V and
+// softmaxLse = natural-log logsumexp of the selected scaled scores
+// (aclnnBlockSparseAttentionGrad page, section 计算公式, forward part), with
+// the online rescaling of the FlashAttentionScore page (section 实现原理): the
+// running row max m and sum l are updated per key tile and the partial PV
+// product is rescaled by exp(m_old - m_new) when the max grows.
+//
+// One persistent CTA per SM, 192 threads:
+//   warp 4      producer: scans the mask row(s) of its query tile for selected
+//               key tiles and streams K/V tiles through a 2-stage TMA ring;
+//   warp 5      MMA issuer (S = Q K^T into one of two TMEM buffers, O += P V
+//               with P read from TMEM) and TMEM owner;
+//   warps 0-3   softmax: TMEM lane s = query row s.
+// The rescale is lazy: O is only rescaled when a row max grows by more than
+// 8 (log2 units), so P stays below 2^8 and most tiles skip the TMEM round trip.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bsa_common.h"
+#include "bsa_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace bsa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kProdWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kPanel = 128 * 128;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kRescaleThreshold = 8.f;
+
+enum Bar {
+  kQFull = 0, kQEmpty,
+  kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kKvAux0, kKvAux1,
+  kSFull0, kSFull1, kPReady0, kPReady1, kPvDone0, kPvDone1,
+  kOFull, kOEmpty,
+  kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
+  kDrain,
+  kNumBars
+};
+
+template <int D>
+struct Smem {
+  static constexpr int kTileBytes = (D / 64) * kPanel;
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kTileBytes;       // [2]
+  static constexpr int oV = oK + 2 * kTileBytes;   // [2]
+  static constexpr int oBar = oV + 2 * kTileBytes;
+  static constexpr int oMisc = oBar + kNumBars * 8;
+  static constexpr int kBytes = oMisc + 128;
+};
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<kDtBF16> {
+  using T = __nv_bfloat16;
+  static constexpr int kAB = 1;
+  __device__ static uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+template <>
+struct Elem<kDtF16> {
+  using T = __half;
+  static constexpr int kAB = 0;
+  __device__ static uint32_t pack(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+
+__device__ __forceinline__ void record_error(int* header, int where) {
+  atomicCAS(&header[kHdrErrorWhere], 0, where);
+  atomicExch(&header[kHdrError], 1);
+}
+
+__device__ __forceinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
+  const int n16 = (128 - r0) * 8;
+  for (int pnl = 0; pnl < panels; ++pnl) {
+    uint4* base = reinterpret_cast<uint4*>(tile + pnl * kPanel + r0 * 128);
+    for (int i = lane; i < n16; i += 32) base[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+struct FItem {
+  int b, h, it;
+};
+
+__device__ __forceinline__ FItem decode(const Plan& p, int idx) {
+  FItem r;
+  r.it = idx % p.Mq_t;
+  const int bh = idx / p.Mq_t;
+  r.h = bh % p.N1;
+  r.b = bh / p.N1;
+  return r;
+}
+
+// Sub-block bits of key tile jt for query tile `it` of (b, h).
+__device__ __forceinline__ int fwd_tile_bits(const Plan& p, int b, int h, int it, int jt, int Lq,
+                                             int Lk) {
+  int bits = 0;
+  for (int ri = 0; ri < p.rb; ++ri) {
+    const int i = it * p.rb + ri;
+    if (i * p.bx >= Lq) break;
+    for (int cj = 0; cj < p.cb; ++cj) {
+      const int j = jt * p.cb + cj;
+      if (j * p.by >= Lk) break;
+      bool on = true;
+      if (p.has_mask)
+        on = (i < p.Mq && j < p.Mk) &&
+             p.mask[(int64_t)b * p.mask_sb + (int64_t)h * p.mask_sh + (int64_t)i * p.mask_si + j] != 0;
+      if (on) bits |= 1 << (ri * 2 + cj);
+    }
+  }
+  return bits;
+}
+
+template <int D, int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_fwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+          const __grid_constant__ CUtensorMap tm_v, const FwdPlan f) {
+  using S = Smem<D>;
+  using E = Elem<DT>;
+  using T = typename E::T;
+  const Plan& p = f.p;
+  constexpr int kPanels = D / 64;
+  constexpr uint32_t kIdS = idesc_f16(128, 128, E::kAB, 0, 0);  // S = Q K^T
+  constexpr uint32_t kIdO = idesc_f16(128, D, E::kAB, 0, 1);     // O += P V (A in TMEM)
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  int* misc = reinterpret_cast<int*>(smem + S::oMisc);
+  volatile int* abort_flag = misc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 1);
+  int* item_slot = misc + 2;   // [2]
+  int* meta = misc + 4;        // [2] per stage: jt | bits << 24, -1 = end of item
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(p.header, kErrSmemAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(&bars[kQFull], 1);
+    mbar_init(&bars[kQEmpty], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kKvFull0 + i], 1);
+      mbar_init(&bars[kKvEmpty0 + i], 5);  // MMA + 4 softmax warps
+      mbar_init(&bars[kKvAux0 + i], 1);
+      mbar_init(&bars[kSFull0 + i], 1);
+      mbar_init(&bars[kPReady0 + i], 4);
+      mbar_init(&bars[kPvDone0 + i], 1);
+      mbar_init(&bars[kItemFull0 + i], 1);
+      mbar_init(&bars[kItemEmpty0 + i], 5);
+    }
+    mbar_init(&bars[kOFull], 1);
+    mbar_init(&bars[kOEmpty], 4);
+    mbar_init(&bars[kDrain], 1);
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint8_t* sQ = smem + S::oQ;
+  uint8_t* sK0 = smem + S::oK;
+  uint8_t* sV0 = smem + S::oV;
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t n = 0, itc = 0, aux[2] = {0u, 0u};
+    bool ok = true;
+    int pend_q = 0, pend_kv[2] = {0, 0}, pend_aux[2] = {0, 0};
+    uint32_t par_kv[2] = {0u, 0u};
+    while (ok) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitItem);
+        break;
+      }
+      if (lane == 0) {
+        const int idx = atomicAdd(&p.header[kHdrWorkCounter], 1);
+        item_slot[slot] = idx < f.n_rows_items ? idx : -1;
+        mbar_arrive(&bars[kItemFull0 + slot]);
+      }
+      __syncwarp();
+      const int idx = item_slot[slot];
+      if (idx < 0) break;
+      const FItem fi = decode(p, idx);
+      const int Lq = p.lq[fi.b], Lk = p.lk[fi.b];
+      const int q0 = fi.it * 128;
+      const bool has_rows = q0 < Lq;
+      if (!mbar_wait(&bars[kQEmpty], (itc & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitQ);
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[kQFull], S::kTileBytes);
+        const int c1 = p.layout == kLayoutBNSD ? q0 : fi.h;
+        const int c2 = p.layout == kLayoutBNSD ? fi.b * p.N1 + fi.h : p.cu_q[fi.b] + q0;
+        for (int pn = 0; pn < kPanels; ++pn) tma_load_3d(sQ + pn * kPanel, &tm_q, &bars[kQFull], pn * 64, c1, c2);
+      }
+      pend_q = 1;
+      const int ncolt = has_rows ? (Lk + 127) / 128 : 0;
+      for (int jt0 = 0; jt0 < ncolt && ok; jt0 += 32) {
+        const int jt = jt0 + lane;
+        const int bits = jt < ncolt ? fwd_tile_bits(p, fi.b, fi.h, fi.it, jt, Lq, Lk) : 0;
+        unsigned ball = __ballot_sync(0xffffffffu, bits != 0);
+        while (ball && ok) {
+          const int src = __ffs(ball) - 1;
+          ball &= ball - 1;
+          const int jsel = jt0 + src;
+          const int bsel = __shfl_sync(0xffffffffu, bits, src);
+          const int st = n & 1;
+          if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+            record_error(p.header, kErrWaitKV);
+            ok = false;
+            break;
+          }
+          const bool tail = (Lk - jsel * 128) < 128;
+          uint8_t* sK = sK0 + st * S::kTileBytes;
+          uint8_t* sV = sV0 + st * S::kTileBytes;
+          if (lane == 0) {
+            meta[st] = jsel | (bsel << 24);
+            uint64_t* tb = tail ? &bars[kKvAux0 + st] : &bars[kKvFull0 + st];
+            mbar_arrive_expect_tx(tb, 2 * S::kTileBytes);
+            const int c1 = p.layout == kLayoutBNSD ? jsel * 128 : fi.h / p.G;
+            const int c2 = p.layout == kLayoutBNSD ? fi.b * p.N2 + fi.h / p.G : p.cu_k[fi.b] + jsel * 128;
+            for (int pn = 0; pn < kPanels; ++pn) {
+              tma_load_3d(sK + pn * kPanel, &tm_k, tb, pn * 64, c1, c2);
+              tma_load_3d(sV + pn * kPanel, &tm_v, tb, pn * 64, c1, c2);
+            }
+          }
+          pend_kv[st] = tail ? 0 : 1;
+          par_kv[st] = (n >> 1) & 1;
+          if (tail) {
+            pend_aux[st] = 1;
+            if (!mbar_wait(&bars[kKvAux0 + st], aux[st] & 1, abort_flag)) {
+              record_error(p.header, kErrWaitKV);
+              ok = false;
+              break;
+            }
+            aux[st]++;
+            pend_aux[st] = 0;
+            zero_rows(sV, kPanels, Lk - jsel * 128, lane);  // 0 * NaN padding would poison O
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kKvFull0 + st]);
+          }
+          ++n;
+        }
+      }
+      if (!ok) break;
+      // end-of-item marker
+      const int st = n & 1;
+      if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitKV);
+        break;
+      }
+      if (lane == 0) {
+        meta[st] = -1;
+        mbar_arrive(&bars[kKvFull0 + st]);
+      }
+      __syncwarp();
+      ++n;
+      ++itc;
+    }
+    if (*abort_flag) {
+      if (pend_q) mbar_wait_drain(&bars[kQFull], (itc & 1));
+      for (int st = 0; st < 2; ++st) {
+        if (pend_kv[st]) mbar_wait_drain(&bars[kKvFull0 + st], par_kv[st]);
+        if (pend_aux[st]) mbar_wait_drain(&bars[kKvAux0 + st], aux[st] & 1);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    uint32_t n = 0, itc = 0;
+    int where = 0;
+    const uint32_t aQ = smem_u32(sQ);
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int idx = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      if (idx < 0) break;
+      if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
+      tc_fence_after();
+      int j = 0;
+      while (true) {
+        const int st = n & 1;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int m = meta[st];
+        if (m < 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+          ++n;
+          break;
+        }
+        const uint32_t sb = st;
+        if (!mbar_wait(&bars[kPvDone0 + sb], ((n >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
+        tc_fence_after();
+        const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
+        const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
+        const uint32_t colS = sb ? kColS1 : kColS0;
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
+            mma_ss(tmem + colS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS, k > 0);
+          }
+          tc_commit(&bars[kSFull0 + sb]);
+        }
+        __syncwarp();
+        if (!mbar_wait(&bars[kPReady0 + sb], (n >> 1) & 1, abort_flag)) { where = kErrWaitP; break; }
+        if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        tc_fence_after();
+        if (lane == 0) {  // O += P V: A = P (TMEM, packed in the S buffer), B = V (MN-major)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColO, tmem + colS + 8 * k, sdesc_sw128(aV + k * 2048, kPanel, 1024), kIdO,
+                   (j == 0 && k == 0) ? 0u : 1u);
+          tc_commit(&bars[kPvDone0 + sb]);
+          tc_commit(&bars[kKvEmpty0 + st]);
+        }
+        __syncwarp();
+        ++j;
+        ++n;
+      }
+      if (where) break;
+      if (lane == 0) {
+        tc_commit(&bars[kOFull]);
+        tc_commit(&bars[kQEmpty]);
+      }
+      __syncwarp();
+      ++itc;
+    }
+    if (where) record_error(p.header, where);
+    if (*abort_flag) {
+      if (lane == 0) tc_commit(&bars[kDrain]);
+      __syncwarp();
+      mbar_wait_drain(&bars[kDrain], 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int s = warp * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t n = 0, itc = 0;
+    int where = 0;
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int idx = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      if (idx < 0) break;
+      const FItem fi = decode(p, idx);
+      const int Lq = p.lq[fi.b], Lk = p.lk[fi.b];
+      const bool s_ok = fi.it * 128 + s < Lq;
+      float m = -INFINITY, l = 0.f;  // running max (log2 units) and sum
+      int j = 0;
+      while (true) {
+        const int st = n & 1;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int mt = meta[st];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+        if (mt < 0) { ++n; break; }
+        const int jt = mt & 0xFFFFFF, bits = mt >> 24;
+        const uint32_t sb = st;
+        const uint32_t colS = sb ? kColS1 : kColS0;
+        if (!mbar_wait(&bars[kSFull0 + sb], (n >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
+        tc_fence_after();
+        const int t_lim = Lk - jt * 128;
+        const int s_sub = p.rb == 2 ? (s >> 6) : 0;
+        // column c is live when t < t_lim and its key sub-block bit is set
+        auto col_on = [&](int t) -> bool {
+          const int t_sub = p.cb == 2 ? (t >> 6) : 0;
+          return s_ok && t < t_lim && ((bits >> (s_sub * 2 + t_sub)) & 1);
+        };
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lane_off + colS + 32 * c, x);
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (col_on(32 * c + k)) mx = fmaxf(mx, __uint_as_float(x[k]) * p.scale_log2);
+        }
+        float m_use = m;
+        const bool grow = mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY);
+        if (__any_sync(0xffffffffu, grow) && j > 0) {
+          // rescale O rows whose max grew, after the previous PV has landed
+          const uint32_t pb = (n - 1) & 1;
+          if (!mbar_wait(&bars[kPvDone0 + pb], ((n - 1) >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+          tc_fence_after();
+          const float alpha = grow ? ex2_approx(m - mx) : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+            if (grow) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            }
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) { lo[k] = o[k]; hi[k] = o[16 + k]; }
+            tmem_st16(tmem + lane_off + kColO + 32 * c, lo);
+            tmem_st16(tmem + lane_off + kColO + 32 * c + 16, hi);
+          }
+        }
+        if (grow) {
+          l = (m == -INFINITY) ? 0.f : l * ex2_approx(m - mx);
+          m_use = mx;
+          m = mx;
+        }
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lane_off + colS + 32 * c, x);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float p0 = 0.f, p1 = 0.f;
+            if (col_on(32 * c + 2 * k)) p0 = ex2_approx(__uint_as_float(x[2 * k]) * p.scale_log2 - m_use);
+            if (col_on(32 * c + 2 * k + 1)) p1 = ex2_approx(__uint_as_float(x[2 * k + 1]) * p.scale_log2 - m_use);
+            rs += p0 + p1;
+            pk[k] = E::pack(p0, p1);
+          }
+          tmem_st16(tmem + lane_off + colS + 16 * c, pk);
+        }
+        l += rs;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kPReady0 + sb]);
+        ++j;
+        ++n;
+      }
+      if (where) break;
+      // epilogue: Out = O / l, lse = (m + log2 l) * ln 2
+      if (!mbar_wait(&bars[kOFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
+      tc_fence_after();
+      const int srow = fi.it * 128 + s;
+      const bool write_row = p.layout == kLayoutBNSD ? (srow < p.Sq) : (srow < Lq);
+      const bool live = s_ok && l > 0.f;
+      const float inv = live ? 1.f / l : 0.f;
+      int64_t ooff;
+      int64_t sd;
+      if (p.layout == kLayoutBNSD) {
+        ooff = fi.b * f.out_st[0] + fi.h * f.out_st[1] + (int64_t)srow * f.out_st[2];
+        sd = f.out_st[3];
+      } else {
+        ooff = ((int64_t)p.cu_q[fi.b] + srow) * f.out_st[0] + fi.h * f.out_st[1];
+        sd = f.out_st[2];
+      }
+      T* out = static_cast<T*>(f.out) + ooff;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (j > 0) tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+        if (write_row) {
+          if (f.out_vec) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 u;
+              const float* of = reinterpret_cast<const float*>(o);
+              u.x = E::pack(live ? of[8 * q] * inv : 0.f, live ? of[8 * q + 1] * inv : 0.f);
+              u.y = E::pack(live ? of[8 * q + 2] * inv : 0.f, live ? of[8 * q + 3] * inv : 0.f);
+              u.z = E::pack(live ? of[8 * q + 4] * inv : 0.f, live ? of[8 * q + 5] * inv : 0.f);
+              u.w = E::pack(live ? of[8 * q + 6] * inv : 0.f, live ? of[8 * q + 7] * inv : 0.f);
+              *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = u;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const uint32_t pk = E::pack(live ? __uint_as_float(o[k]) * inv : 0.f, 0.f);
+              out[(32 * c + k) * sd] = *reinterpret_cast<const T*>(&pk);
+            }
+          }
+        }
+      }
+      if (write_row) {
+        int64_t li;
+        if (p.layout == kLayoutBNSD)
+          li = ((int64_t)fi.b * p.N1 + fi.h) * p.Sq + srow;
+        else
+          li = ((int64_t)p.cu_q[fi.b] + srow) * p.N1 + fi.h;
+        f.lse_out[li] = live ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kOEmpty]);
+      ++itc;
+    }
+    if (where) record_error(p.header, where);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DT>
+cudaError_t launch_t(const FwdPlan& f, const FwdMaps& m, cudaStream_t st) {
+  const size_t smem = Smem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(k_fwd<D, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = f.p.num_sms;
+  if (f.n_rows_items < grid) grid = f.n_rows_items;
+  if (grid < 1) grid = 1;
+  k_fwd<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, f);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes(int D) { return D == 128 ? Smem<128>::kBytes : Smem<64>::kBytes; }
+
+cudaError_t launch_fwd(const FwdPlan& f, const FwdMaps& m, cudaStream_t st) {
+  if (f.p.dtype == kDtBF16)
+    return f.p.D == 128 ? launch_t<128, kDtBF16>(f, m, st) : launch_t<64, kDtBF16>(f, m, st);
+  return f.p.D == 128 ? launch_t<128, kDtF16>(f, m, st) : launch_t<64, kDtF16>(f, m, st);
+}
+
+}  // namespace bsa

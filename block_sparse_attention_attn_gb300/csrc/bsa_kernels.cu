@@ -1,0 +1,518 @@
+// bsa_kernels.cu - the bandwidth-bound steps around the tensor-core kernels:
+//   * mask compaction (BlockSparseMask -> per-column / per-row active lists),
+//     page "aclnnBlockSparseAttentionGrad", parameter table, row
+//     blockSparseMaskOptional (1 = the block takes part);
+//   * the backward work planner (column lists -> balanced work items);
+//   * the preprocess D = rowsum(dOut * attentionOut) (formulas, softmax_grad)
+//     and lse*log2(e), plus zeroing of the fp32 dQ accumulator;
+//   * the finalize kernels: fp32 dQ (and split-column dK/dV) -> output dtype,
+//     zeros for padding rows and for key tiles no query selects.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bsa_common.h"
+#include "bsa_launch.h"
+
+namespace bsa {
+
+// --------------------------------------------------------------------------
+// compaction
+// --------------------------------------------------------------------------
+// Sub-block bits of tile (it, jt) for (b, h): bit (ri*2+cj) set when block
+// (it*rb+ri, jt*cb+cj) lies inside the valid range and is selected.
+__device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int it, int jt,
+                                         int Lq, int Lk) {
+  int bits = 0;
+  for (int ri = 0; ri < a.rb; ++ri) {
+    const int i = it * a.rb + ri;
+    if ((int64_t)i * a.bx >= Lq) break;
+    for (int cj = 0; cj < a.cb; ++cj) {
+      const int j = jt * a.cb + cj;
+      if ((int64_t)j * a.by >= Lk) break;
+      bool on = true;
+      if (a.has_mask) {
+        on = (i < a.Mq && j < a.Mk) &&
+             a.mask[(int64_t)b * a.sb + (int64_t)h * a.sh + (int64_t)i * a.si + j] != 0;
+      }
+      if (on) bits |= 1 << (ri * 2 + cj);
+    }
+  }
+  return bits;
+}
+
+// One warp per column (b, g, jt, hl) with index ((b*N2+g)*col_slots + jt)*G + hl.
+// fill == 0: counts[col] = active tiles; fill == 1: writes the entries.
+__global__ void k_columns(CompactArgs a, int fill) {
+  const int warps = blockDim.x >> 5;
+  const int col = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int ncols = a.B * a.N2 * a.col_slots * a.G;
+  if (col >= ncols) return;
+  const int hl = col % a.G;
+  const int r = col / a.G;
+  const int jt = r % a.col_slots;
+  const int bg = r / a.col_slots;
+  const int g = bg % a.N2;
+  const int b = bg / a.N2;
+  const int h = g * a.G + hl;
+  const int Lq = a.lq[b], Lk = a.lk[b];
+  const int nrows = (Lq + a.tq - 1) / a.tq;
+  const int ncolt = (Lk + a.tk - 1) / a.tk;
+  int count = 0;
+  int base = fill ? a.ptr[col] : 0;
+  if (jt < ncolt) {
+    for (int it0 = 0; it0 < nrows; it0 += 32) {
+      const int it = it0 + lane;
+      const int bits = it < nrows ? tile_bits(a, b, h, it, jt, Lq, Lk) : 0;
+      const unsigned ball = __ballot_sync(0xffffffffu, bits != 0);
+      if (fill && bits) {
+        const int pos = base + count + __popc(ball & ((1u << lane) - 1u));
+        a.out[pos] = a.plain ? it : pack_entry(it, hl, bits);
+      }
+      count += __popc(ball);
+    }
+  }
+  if (!fill && lane == 0) a.counts[col] = count;
+}
+
+// One warp per row (b, h, it) with index (b*N1+h)*row_slots + it.
+__global__ void k_rows(CompactArgs a, int fill) {
+  const int warps = blockDim.x >> 5;
+  const int row = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int nrows_all = a.B * a.N1 * a.row_slots;
+  if (row >= nrows_all) return;
+  const int it = row % a.row_slots;
+  const int bh = row / a.row_slots;
+  const int h = bh % a.N1;
+  const int b = bh / a.N1;
+  const int Lq = a.lq[b], Lk = a.lk[b];
+  const int nrows = (Lq + a.tq - 1) / a.tq;
+  const int ncolt = (Lk + a.tk - 1) / a.tk;
+  int count = 0;
+  int base = fill ? a.ptr[row] : 0;
+  if (it < nrows) {
+    for (int jt0 = 0; jt0 < ncolt; jt0 += 32) {
+      const int jt = jt0 + lane;
+      const int bits = jt < ncolt ? tile_bits(a, b, h, it, jt, Lq, Lk) : 0;
+      const unsigned ball = __ballot_sync(0xffffffffu, bits != 0);
+      if (fill && bits) {
+        const int pos = base + count + __popc(ball & ((1u << lane) - 1u));
+        a.out[pos] = a.plain ? jt : pack_entry(jt, 0, bits);
+      }
+      count += __popc(ball);
+    }
+  }
+  if (!fill && lane == 0) a.counts[row] = count;
+}
+
+// Block-wide exclusive scan of one value per thread (1024 threads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    int s = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nw) warp_sums[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int warp_prefix = w ? warp_sums[w - 1] : 0;
+  const int res = warp_prefix + x - v;
+  const int tot = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  *total = tot;
+  return res;
+}
+
+// out[i] = sum_{k<i} in[k] for i in [0, n]; single block of 1024 threads.
+__global__ void k_scan(const int* in, int* out, int n) {
+  __shared__ int ws[32];
+  int carry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int v = i < n ? in[i] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, ws, &tot);
+    if (i < n) out[i] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) out[n] = carry;
+}
+
+// Backward planner (single block of 1024 threads):
+//  1. colptr = exclusive scan of the grouped column counts;
+//  2. per key tile gc (all G heads of the group): n = its active tiles; a
+//     column longer than the chunk length L (and while partial slots remain)
+//     is split into ceil(n/L) equal chunks that add into an fp32 slot;
+//  3. items: split chunks first (the longest work), then one item per
+//     non-empty column in (b, g, jt) order.
+__global__ void k_plan(Plan p) {
+  __shared__ int ws[32];
+  __shared__ int s_L;
+  int carry = 0;
+  for (int base = 0; base < p.NC; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const int v = i < p.NC ? p.colcnt[i] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, ws, &tot);
+    if (i < p.NC) p.colptr[i] = carry + ex;
+    carry += tot;
+  }
+  const int T = carry;
+  if (threadIdx.x == 0) {
+    p.colptr[p.NC] = T;
+    int L = (T + 2 * p.num_sms - 1) / (2 * p.num_sms);
+    if (L < p.min_chunk) L = p.min_chunk;
+    s_L = L;
+  }
+  __syncthreads();
+  const int L = s_L;
+  // pass 0: slots; pass 1: split items; pass 2: single items
+  int slot_carry = 0, split_carry = 0;
+  for (int base = 0; base < p.NGC; base += blockDim.x) {
+    const int gc = base + threadIdx.x;
+    int n = 0;
+    if (gc < p.NGC) n = p.colptr[(gc + 1) * p.G] - p.colptr[gc * p.G];
+    const int want = (n > L) ? 1 : 0;
+    int tot;
+    const int sidx = block_exclusive_scan(want, ws, &tot) + slot_carry;
+    slot_carry += tot;
+    const int split = want && (sidx < p.max_slots);
+    const int chunks = split ? (n + L - 1) / L : 0;
+    const int cidx = block_exclusive_scan(chunks, ws, &tot) + split_carry;
+    split_carry += tot;
+    if (gc < p.NGC) {
+      p.colinfo[gc] = (n == 0) ? -1 : (split ? sidx : -2);
+      if (split) {
+        const int e0 = p.colptr[gc * p.G];
+        for (int c = 0; c < chunks; ++c) {  // balanced: every chunk is non-empty
+          const int b0 = e0 + (int)(((int64_t)c * n) / chunks);
+          const int b1 = e0 + (int)(((int64_t)(c + 1) * n) / chunks);
+          p.items[cidx + c] = make_int4(gc, b0, b1, sidx);
+        }
+      }
+    }
+  }
+  const int n_split_items = split_carry;
+  int single_carry = 0;
+  for (int base = 0; base < p.NGC; base += blockDim.x) {
+    const int gc = base + threadIdx.x;
+    int single = 0, n = 0, e0 = 0;
+    if (gc < p.NGC) {
+      e0 = p.colptr[gc * p.G];
+      n = p.colptr[(gc + 1) * p.G] - e0;
+      single = (p.colinfo[gc] == -2) ? 1 : 0;
+    }
+    int tot;
+    const int idx = block_exclusive_scan(single, ws, &tot) + single_carry + n_split_items;
+    single_carry += tot;
+    if (single) p.items[idx] = make_int4(gc, e0, e0 + n, -1);
+  }
+  if (threadIdx.x == 0) {
+    p.header[kHdrNumItems] = n_split_items + single_carry;
+    p.header[kHdrTotalTiles] = T;
+    p.header[kHdrSlotsUsed] = min(slot_carry, p.max_slots);
+    p.header[kHdrChunkLen] = L;
+    p.header[kHdrWorkCounter] = 0;
+    p.header[kHdrError] = 0;
+    p.header[kHdrErrorWhere] = 0;
+  }
+}
+
+// Zero the fp32 partial slots of split columns (one block per slot).
+__global__ void k_zero_slots(Plan p) {
+  const int slot = blockIdx.x;
+  if (slot >= p.header[kHdrSlotsUsed]) return;
+  float4* s = reinterpret_cast<float4*>(p.slots + (int64_t)slot * 2 * kTile * p.D);
+  const int n4 = 2 * kTile * p.D / 4;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// --------------------------------------------------------------------------
+// preprocess: D_s = sum_d dout_sd * out_sd, lse2_s = lse_s * log2(e); zero dQacc
+// --------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float2 to_f2(uint32_t u);
+template <>
+__device__ __forceinline__ float2 to_f2<__nv_bfloat16>(uint32_t u) {
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(h);
+}
+template <>
+__device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(h);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_preprocess(Plan p) {
+  constexpr int TPR = D / 8;  // threads per row, 8 elements (16 B) each
+  constexpr int RPB = 256 / TPR;
+  const int sub = threadIdx.x % TPR;
+  const int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR;  // over N1 * Rq
+  if (row >= (int64_t)p.N1 * p.Rq) return;
+  const int h = (int)(row / p.Rq);
+  const int r = (int)(row % p.Rq);
+  const int b = p.qtile_b[r / kTile];
+  const int s = r - p.qrow[b];
+  const bool valid = s < p.lq[b];
+  float acc = 0.f;
+  if (valid) {
+    int64_t off;
+    if (p.layout == kLayoutBNSD)
+      off = (((int64_t)b * p.N1 + h) * p.Sq + s) * D;
+    else
+      off = (((int64_t)p.cu_q[b] + s) * p.N1 + h) * D;
+    const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + off)[sub];
+    const uint4 c = reinterpret_cast<const uint4*>(static_cast<const T*>(p.out) + off)[sub];
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = to_f2<T>(av[k]), y = to_f2<T>(cv[k]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
+  if (sub == 0) {
+    float l2 = 0.f;
+    if (valid) {
+      int64_t li;
+      if (p.layout == kLayoutBNSD)
+        li = ((int64_t)b * p.N1 + h) * p.Sq + s;
+      else
+        li = ((int64_t)p.cu_q[b] + s) * p.N1 + h;
+      l2 = p.lse[li] * 1.4426950408889634f;
+    }
+    p.dvec[row] = valid ? acc : 0.f;
+    p.lse2[row] = l2;
+  }
+  float4* dst = reinterpret_cast<float4*>(p.dqacc + row * D) + sub * 2;
+  dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// --------------------------------------------------------------------------
+// finalize
+// --------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <typename T>
+__device__ __forceinline__ T cvt1(float a);
+template <>
+__device__ __forceinline__ __nv_bfloat16 cvt1<__nv_bfloat16>(float a) {
+  return __float2bfloat16_rn(a);
+}
+template <>
+__device__ __forceinline__ __half cvt1<__half>(float a) {
+  return __float2half_rn(a);
+}
+
+// Writes 8 consecutive (in d) output values at element offset `off` with
+// element stride `sd`: one 16-byte store when `vec`, else scalar stores.
+template <typename T>
+__device__ __forceinline__ void store8(void* base, int64_t off, int64_t sd, bool vec,
+                                       const float (&x)[8]) {
+  T* p = static_cast<T*>(base) + off;
+  if (vec) {
+    uint4 u;
+    u.x = pack2<T>(x[0], x[1]);
+    u.y = pack2<T>(x[2], x[3]);
+    u.z = pack2<T>(x[4], x[5]);
+    u.w = pack2<T>(x[6], x[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) p[k * sd] = cvt1<T>(x[k]);
+  }
+}
+
+__device__ __forceinline__ int batch_of_token(const int* cu, int B, int tok) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= tok) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// dq[b,h,s,:] = scale * dQacc (0 on padding rows), any output strides.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_finalize_dq(Plan p) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = 256 / TPR;
+  const int sub = threadIdx.x % TPR;
+  const int64_t nrows = (p.layout == kLayoutBNSD) ? (int64_t)p.B * p.N1 * p.Sq
+                                                  : (int64_t)p.Tq * p.N1;
+  for (int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; row < nrows;
+       row += (int64_t)gridDim.x * RPB) {
+    int b, h, s;
+    int64_t off;
+    if (p.layout == kLayoutBNSD) {
+      s = (int)(row % p.Sq);
+      const int64_t bh = row / p.Sq;
+      h = (int)(bh % p.N1);
+      b = (int)(bh / p.N1);
+      off = b * p.dq_st[0] + h * p.dq_st[1] + s * p.dq_st[2];
+    } else {
+      h = (int)(row % p.N1);
+      const int tok = (int)(row / p.N1);
+      b = batch_of_token(p.cu_q, p.B, tok);
+      s = tok - p.cu_q[b];
+      off = tok * p.dq_st[0] + h * p.dq_st[1];
+    }
+    float x[8];
+    if (s < p.lq[b]) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.dqacc + ((int64_t)h * p.Rq + p.qrow[b] + s) * D + sub * 8);
+      const float4 a = src[0], c = src[1];
+      x[0] = a.x * p.scale; x[1] = a.y * p.scale; x[2] = a.z * p.scale; x[3] = a.w * p.scale;
+      x[4] = c.x * p.scale; x[5] = c.y * p.scale; x[6] = c.z * p.scale; x[7] = c.w * p.scale;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = 0.f;
+    }
+    const int64_t sd = p.dq_st[p.layout == kLayoutBNSD ? 3 : 2];
+    store8<T>(p.dq, off + sub * 8 * sd, sd, p.dq_vec != 0, x);
+  }
+}
+
+// dk/dv rows of key tiles the backward kernel did not write: zeros for tiles
+// no query selects, the fp32 slot (dK already scaled) for split tiles.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_finalize_dkdv(Plan p) {
+  constexpr int TPR = D / 8;
+  constexpr int RPB = 256 / TPR;
+  const int sub = threadIdx.x % TPR;
+  const int64_t nrows = (p.layout == kLayoutBNSD) ? (int64_t)p.B * p.N2 * p.Skv
+                                                  : (int64_t)p.Tkv * p.N2;
+  for (int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; row < nrows;
+       row += (int64_t)gridDim.x * RPB) {
+    int b, g, t;
+    int64_t ok, ov;
+    if (p.layout == kLayoutBNSD) {
+      t = (int)(row % p.Skv);
+      const int64_t bg = row / p.Skv;
+      g = (int)(bg % p.N2);
+      b = (int)(bg / p.N2);
+      ok = b * p.dk_st[0] + g * p.dk_st[1] + t * p.dk_st[2];
+      ov = b * p.dv_st[0] + g * p.dv_st[1] + t * p.dv_st[2];
+    } else {
+      g = (int)(row % p.N2);
+      const int tok = (int)(row / p.N2);
+      b = batch_of_token(p.cu_k, p.B, tok);
+      t = tok - p.cu_k[b];
+      ok = tok * p.dk_st[0] + g * p.dk_st[1];
+      ov = tok * p.dv_st[0] + g * p.dv_st[1];
+    }
+    const int jt = t / kTile;
+    const int gc = (b * p.N2 + g) * p.Mk_t + jt;
+    const int info = p.colinfo[gc];
+    if (info == -2) continue;
+    float xk[8], xv[8];
+    if (info >= 0 && t < p.lk[b]) {
+      const float* sl = p.slots + (int64_t)info * 2 * kTile * D;
+      const float4* sk = reinterpret_cast<const float4*>(sl + (t % kTile) * D + sub * 8);
+      const float4* sv = reinterpret_cast<const float4*>(sl + (kTile + t % kTile) * D + sub * 8);
+      const float4 a = sk[0], c = sk[1], e = sv[0], f = sv[1];
+      xk[0] = a.x; xk[1] = a.y; xk[2] = a.z; xk[3] = a.w;
+      xk[4] = c.x; xk[5] = c.y; xk[6] = c.z; xk[7] = c.w;
+      xv[0] = e.x; xv[1] = e.y; xv[2] = e.z; xv[3] = e.w;
+      xv[4] = f.x; xv[5] = f.y; xv[6] = f.z; xv[7] = f.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) xk[k] = xv[k] = 0.f;
+    }
+    const int li = p.layout == kLayoutBNSD ? 3 : 2;
+    store8<T>(p.dk, ok + sub * 8 * p.dk_st[li], p.dk_st[li], p.dkv_vec != 0, xk);
+    store8<T>(p.dv, ov + sub * 8 * p.dv_st[li], p.dv_st[li], p.dkv_vec != 0, xv);
+  }
+}
+
+// --------------------------------------------------------------------------
+// launchers
+// --------------------------------------------------------------------------
+cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st) {
+  const int ncols = a.B * a.N2 * a.col_slots * a.G;
+  if (ncols == 0) return cudaSuccess;
+  k_columns<<<(ncols + 7) / 8, 256, 0, st>>>(a, fill);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows(const CompactArgs& a, int fill, cudaStream_t st) {
+  const int nrows = a.B * a.N1 * a.row_slots;
+  if (nrows == 0) return cudaSuccess;
+  k_rows<<<(nrows + 7) / 8, 256, 0, st>>>(a, fill);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int* in, int* out, int n, cudaStream_t st) {
+  k_scan<<<1, 1024, 0, st>>>(in, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const Plan& p, cudaStream_t st) {
+  k_plan<<<1, 1024, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.max_slots > 0) k_zero_slots<<<p.max_slots, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+static cudaError_t launch_pre_t(const Plan& p, cudaStream_t st) {
+  constexpr int RPB = 256 / (D / 8);
+  const int64_t rows = (int64_t)p.N1 * p.Rq;
+  if (rows == 0) return cudaSuccess;
+  k_preprocess<T, D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess(const Plan& p, cudaStream_t st) {
+  if (p.dtype == kDtBF16)
+    return p.D == 128 ? launch_pre_t<__nv_bfloat16, 128>(p, st)
+                      : launch_pre_t<__nv_bfloat16, 64>(p, st);
+  return p.D == 128 ? launch_pre_t<__half, 128>(p, st) : launch_pre_t<__half, 64>(p, st);
+}
+
+template <typename T, int D>
+static cudaError_t launch_fin_t(const Plan& p, cudaStream_t st) {
+  const int grid = p.num_sms * 8;
+  k_finalize_dq<T, D><<<grid, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_finalize_dkdv<T, D><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const Plan& p, cudaStream_t st) {
+  if (p.dtype == kDtBF16)
+    return p.D == 128 ? launch_fin_t<__nv_bfloat16, 128>(p, st)
+                      : launch_fin_t<__nv_bfloat16, 64>(p, st);
+  return p.D == 128 ? launch_fin_t<__half, 128>(p, st) : launch_fin_t<__half, 64>(p, st);
+}
+
+}  // namespace bsa

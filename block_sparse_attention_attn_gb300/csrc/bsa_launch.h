@@ -1,0 +1,62 @@
+// bsa_launch.h - host-side launchers of the kernels (all asynchronous on `st`).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bsa_common.h"
+
+namespace bsa {
+
+// Arguments of the mask compaction kernels. Columns are indexed
+// ((b*N2 + g)*col_slots + jt)*G + hl, rows (b*N1 + h)*row_slots + it; slots
+// past the valid tiles of a batch get count 0 (so a slot count of Mq+1 / Mk+1
+// yields the CSR/CSC pointer layout with a closing entry per (b, h)).
+struct CompactArgs {
+  const uint8_t* mask;
+  int64_t sb, sh, si;  // mask strides (j stride 1)
+  int has_mask;
+  int B, N1, N2, G;
+  int Mq, Mk;          // mask dims in blocks
+  int bx, by, rb, cb;  // block shape and blocks per tile
+  int tq, tk;          // tile size in tokens (rb*bx, cb*by)
+  int col_slots, row_slots;
+  const int* lq;       // device, per batch
+  const int* lk;
+  int* counts;         // count pass output
+  const int* ptr;      // fill pass: exclusive scan of counts
+  int32_t* out;        // fill pass output
+  int plain;           // 1: store the tile index only; 0: packed entry
+};
+
+cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st);
+cudaError_t launch_rows(const CompactArgs& a, int fill, cudaStream_t st);
+cudaError_t launch_scan(const int* in, int* out, int n, cudaStream_t st);
+cudaError_t launch_plan(const Plan& p, cudaStream_t st);
+cudaError_t launch_preprocess(const Plan& p, cudaStream_t st);
+cudaError_t launch_finalize(const Plan& p, cudaStream_t st);
+
+// Tensor maps of the backward / forward kernels (3-D views, 64-element x 128-row
+// boxes, 128-byte swizzle): BNSD (d, s, b*N+h), TND (d, h, token).
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;
+};
+cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st);
+size_t bwd_smem_bytes(int D);
+
+struct FwdMaps {
+  CUtensorMap q, k, v;
+};
+struct FwdPlan {
+  Plan p;          // shared geometry and tensors (out -> p.dq slot unused)
+  void* out;       // attentionOut
+  float* lse_out;  // softmaxLse
+  int64_t out_st[4];
+  int64_t lse_st[3];
+  int out_vec;
+  int n_rows_items; // B * N1 * (BNSD: ceil(Sq/128), TND: Mq_t)
+};
+cudaError_t launch_fwd(const FwdPlan& f, const FwdMaps& m, cudaStream_t st);
+size_t fwd_smem_bytes(int D);
+
+}  // namespace bsa
