@@ -43,7 +43,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["token_mask", "head_rows", "forward", "forward_blockrows", "backward",
+__all__ = ["token_mask", "token_mask_at", "head_rows", "forward", "forward_blockrows", "backward",
            "backward_dq_rows", "backward_dkdv_rows", "compact_mask", "seq_offsets"]
 
 
@@ -86,6 +86,16 @@ def token_mask(block_mask, bx, by, Lq, Lk):
     rows = np.arange(Lq) // bx
     cols = np.arange(Lk) // by
     return bm[rows[:, None], cols[None, :]]
+
+
+def token_mask_at(block_mask, bx, by, rows, cols):
+    """The entries [rows x cols] of :func:`token_mask` only (same definition,
+    evaluated on the requested query rows and key columns)."""
+    rows, cols = np.asarray(rows), np.asarray(cols)
+    if block_mask is None:
+        return np.ones((len(rows), len(cols)), dtype=bool)
+    bm = np.asarray(block_mask) != 0
+    return bm[(rows // bx)[:, None], (cols // by)[None, :]]
 
 
 def _dims(q, k, layout):
@@ -276,8 +286,8 @@ def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
     L = _lse_rows(lse, layout, b, h, lq[b], oq)[r]
     Km = head_rows(k, layout, b, g, lk[b], okv)
     Vm = head_rows(v, layout, b, g, lk[b], okv)
-    Mfull = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b])
-    dQ, _, _ = _head_backward(Qh, Km, Vm, dOh, Oh, L, Mfull[r], scale)
+    M = token_mask_at(None if mask is None else mask[b, h], bx, by, r, np.arange(lk[b]))
+    dQ, _, _ = _head_backward(Qh, Km, Vm, dOh, Oh, L, M, scale)
     res[ok] = dQ
     return res
 
@@ -306,8 +316,8 @@ def backward_dkdv_rows(dout, q, k, v, out, lse, b, g, rows, mask=None,
         dOm = head_rows(dout, layout, b, h, lq[b], oq)
         Om = head_rows(out, layout, b, h, lq[b], oq)
         L = _lse_rows(lse, layout, b, h, lq[b], oq)
-        Mfull = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b])
-        _, dK, dV = _head_backward(Qm, Kt, Vt, dOm, Om, L, Mfull[:, t], scale)
+        M = token_mask_at(None if mask is None else mask[b, h], bx, by, np.arange(lq[b]), t)
+        _, dK, dV = _head_backward(Qm, Kt, Vt, dOm, Om, L, M, scale)
         dk[ok] += dK
         dv[ok] += dV
     return dk, dv

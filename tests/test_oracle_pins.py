@@ -413,3 +413,13 @@ def test_planted_gqa_mapping_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(O, "backward", wrong)
     with pytest.raises(AssertionError):
         test_backward_matches_sdpa_autograd(4, 2, 37, 52, 16, 8, 16, 2)
+
+
+def test_token_mask_at_matches_full_expansion():
+    rng = np.random.Generator(np.random.PCG64(111))
+    bm = (rng.random((5, 7)) < 0.5).astype(np.uint8)
+    full = O.token_mask(bm, 16, 8, 70, 50)
+    rows, cols = np.array([0, 15, 16, 69]), np.array([0, 7, 8, 49])
+    np.testing.assert_array_equal(O.token_mask_at(bm, 16, 8, rows, cols), full[rows][:, cols])
+    ref = np.repeat(np.repeat(bm != 0, 16, axis=0), 8, axis=1)[:70, :50]   # independent expansion
+    np.testing.assert_array_equal(full, ref)
