@@ -1,0 +1,403 @@
+"""Benchmark of the block-sparse attention backward (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload w1|w4|...]
+    python bench.py --impl reference ...      # the fp64 CPU oracle, same metric
+
+A step is one bsa_grad call (mask compaction, preprocess, tcgen05 backward,
+finalize) over the workload's inputs, already resident in HBM. The L2 is
+flushed (a 512 MB write) between timed steps; each step is timed with CUDA
+events on the launching stream. FLOPs are the algorithmic 10*bx*by*D per
+active block per query head. Under torchrun every rank runs its own replica
+of the workload on its GPU (no data-path collective); the step time is the
+max over ranks and `value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn bwd TFLOP/s (active blocks) & % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="w1")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAK, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("bsa_bwd.cu", "sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, "block_sparse_attention_attn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """DRAM bytes per launch of the backward kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "bwd_kernel_counters.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ inputs
+def torch_dtype(name):
+    import torch
+    return {"bf16": torch.bfloat16, "f16": torch.float16}[name]
+
+
+def make_inputs(w, dev):
+    import torch
+
+    import block_sparse_attention_attn_gb300 as bsa
+    dt = torch_dtype(w.dtype)
+    dout, q, k, v = (torch.from_numpy(x).to(dt).to(dev) for x in w.tensors())
+    mask = None if w.mask is None else torch.from_numpy(w.mask).to(dev)
+    seq = dict(actual_seq_lengths=w.seq_q, actual_seq_lengths_kv=w.seq_kv)
+    out, lse, _ = bsa.block_sparse_attention_fwd(q, k, v, block_sparse_mask=mask,
+                                                 block_shape=[w.bx, w.by], layout=w.layout,
+                                                 num_key_value_heads=w.N2, scale_value=w.scale,
+                                                 **seq)
+    torch.cuda.synchronize()
+    return dict(dout=dout, query=q, key=k, value=v, attention_out=out, softmax_lse=lse,
+                block_sparse_mask=mask), seq
+
+
+def grad_executor(w, t, seq, dq, dk, dv):
+    import block_sparse_attention_attn_gb300 as bsa
+    return bsa.bsa_grad_workspace_size(
+        t["dout"], t["query"], t["key"], t["value"], t["attention_out"], t["softmax_lse"],
+        t["block_sparse_mask"], None, [w.bx, w.by], seq["actual_seq_lengths"],
+        seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, 0, w.scale,
+        dq=dq, dk=dk, dv=dv)
+
+
+# --------------------------------------------------------------- our arm
+def bench_ours(args, rank, world, local):
+    import torch
+
+    import block_sparse_attention_attn_gb300 as bsa
+    from block_sparse_attention_attn_gb300.workloads import make_workload, workload_summary
+    dev = torch.device("cuda", local)
+    w = make_workload(args.workload)
+    flops = w.flops()
+    t, seq = make_inputs(w, dev)
+    dq = torch.empty_like(t["query"])
+    dk = torch.empty_like(t["key"])
+    dv = torch.empty_like(t["value"])
+    size, ex = grad_executor(w, t, seq, dq, dk, dv)
+    ws = torch.empty(size, dtype=torch.uint8, device=dev)
+    del ex
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ex, ev=None):
+        if ev is not None:
+            ex.set_timing_events(*ev)
+        bsa.bsa_grad(ws, size, ex, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(grad_executor(w, t, seq, dq, dk, dv)[1])
+    torch.cuda.synchronize()
+    bsa.bsa_check_status(ws)
+
+    n = args.steps
+    # host-side planning (first stage) happens before the timed region
+    exs = [grad_executor(w, t, seq, dq, dk, dv)[1] for _ in range(n)]
+    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in k0 + k1:
+        e.record(stream)   # materialise the event handles before handing them to C
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for i in range(n):
+        flush.zero_()
+        s_ev[i].record(stream)
+        step(exs[i], (k0[i], k1[i]))
+        e_ev[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+    bsa.bsa_check_status(ws)
+    step_ms = [a.elapsed_time(b) for a, b in zip(s_ev, e_ev)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+    ms_step = max_over_ranks(float(np.mean(step_ms)), world)
+    ms_kern = max_over_ranks(float(np.mean(kern_ms)), world)
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> H2D -> first and
+    # second stage -> D2H of dq, dk, dv, every step
+    host = {k_: x.cpu().pin_memory() for k_, x in t.items() if x is not None}
+    h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (dq, dk, dv)]
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    e2e_n = max(3, min(n, 20))
+    e2e_times = []
+    for i in range(e2e_n + 1):      # iteration 0 warms up
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k_, x in host.items():
+            t[k_].copy_(x, non_blocking=True)
+        step(grad_executor(w, t, seq, dq, dk, dv)[1])
+        for hd, dd in zip(h_out, (dq, dk, dv)):
+            hd.copy_(dd, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:
+            e2e_times.append(a.elapsed_time(b))
+    e2e_ms = max_over_ranks(float(np.mean(e2e_times)), world)
+
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
+    achieved = flops / (ms_kern * 1e-3) / 1e12
+    summ = workload_summary(w)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded PCG64 N(0,1) inputs; Out/lse from bsa_fwd)",
+        "config": {"workload": w.name, "layout": w.layout, "B": w.B, "N1": w.N1, "N2": w.N2,
+                   "Sq": w.Sq, "Skv": w.Skv, "D": w.D, "block": [w.bx, w.by],
+                   "active_blocks": summ["active_blocks"], "density": round(summ["density"], 4),
+                   "gflop_per_step": round(flops / 1e9, 2), "parallelism": f"replicas x{world}",
+                   "l2": "flushed (512 MB write) before every timed step"},
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": committed_traffic(w.name),
+                     "kernel": "k_bwd (tcgen05 backward)", "kernel_ms": round(ms_kern, 4),
+                     "peak_source": f"{src}: MEASURED_PEAKS.json bf16_tflops (burst)"
+                     if src == "measured" else "fallback 1.9 PFLOP/s bf16"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 8 * n,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if not args.no_cpu_baseline and rank == 0:
+        try:
+            line["cpu_baseline"] = cpu_baseline(w)
+        except Exception as exc:  # the GPU numbers stand on their own
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": os.cpu_count(),
+                                    "kind": "oracle", "sample": f"failed: {exc!r}"}
+    return line
+
+
+# ------------------------------------------------------- CPU oracle timings
+def _oracle_sample(w, heads, S):
+    """The workload restricted to batch 0, the first `heads` query heads (and
+    their key heads) and the first S tokens; returns (args, kwargs, flops)."""
+    import torch
+    dt = torch_dtype(w.dtype)   # same rounding as the GPU inputs
+    G = w.N1 // w.N2
+    g_heads = -(-heads // G)
+    rng = np.random.Generator(np.random.PCG64(w.seed + 99))
+    def rnd(n):
+        return torch.from_numpy(rng.standard_normal((1, n, S, w.D), dtype=np.float32) * w.std) \
+            .to(dt).to(torch.float64).numpy()
+    q, dout, out = rnd(heads), rnd(heads), rnd(heads) * 0.1
+    k, v = rnd(g_heads), rnd(g_heads)
+    mask = None if w.mask is None else w.mask[:1, :heads, :-(-S // w.bx), :-(-S // w.by)]
+    lse = np.full((1, heads, S, 1), math.log(S) + 2.0)
+    kw = dict(mask=mask, block_shape=(w.bx, w.by), num_kv_heads=g_heads, scale=w.scale)
+    if mask is None:
+        nb = heads * (-(-S // w.bx)) * (-(-S // w.by))
+    else:
+        nb = int(np.count_nonzero(mask))
+    return (dout, q, k, v, out, lse), kw, 10.0 * w.bx * w.by * w.D * nb
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The oracle (fp64 numpy, as it stands) on a bounded sample of the workload."""
+    from oracle import bsa_oracle as O
+    S = min(w.Sq, 2048)
+    heads = 1
+    args, kw, fl = _oracle_sample(w, heads, S)
+    t0 = time.perf_counter()
+    O.backward(*args, **kw)
+    dt = time.perf_counter() - t0
+    heads = max(1, min(w.N1, int(target_s / max(dt, 1e-3))))
+    args, kw, fl = _oracle_sample(w, heads, S)
+    t0 = time.perf_counter()
+    O.backward(*args, **kw)
+    dt = time.perf_counter() - t0
+    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{w.name} batch 0, {heads} query heads, first {S} tokens, same mask "
+                      f"({fl / 1e9:.1f} GFLOP algorithmic, {dt:.1f} s, numpy fp64 BLAS threads)"}
+
+
+def bench_reference(args, rank, world):
+    from block_sparse_attention_attn_gb300.workloads import make_workload
+    from oracle import bsa_oracle as O
+    w = make_workload(args.workload)
+    S = min(w.Sq, 1024)
+    a, kw, fl = _oracle_sample(w, 1, S)
+    for _ in range(args.warmup):
+        O.backward(*a, **kw)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        O.backward(*a, **kw)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * float(np.mean(times))
+    value = fl / (ms * 1e-3) / 1e12
+    sample = f"{w.name} batch 0, 1 query head, first {S} tokens, same mask ({fl / 1e9:.2f} GFLOP)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank != 0:
+            return
+        print(json.dumps(bench_reference(args, rank, world)), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    line = bench_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -62,6 +62,7 @@ def load_library():
         i64, ctypes.c_double, T, T, P(u64), P(vp)]
     lib.bsa_fwd.argtypes = [vp, u64, vp, vp]
     lib.bsa_executor_destroy.argtypes = [vp]
+    lib.bsa_executor_set_timing_events.argtypes = [vp, vp, vp]
     lib.bsa_mask_compact_workspace_size.argtypes = [T, i64, i64, P(u64)]
     lib.bsa_mask_compact.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp, vp, vp,
                                      u64, vp]
@@ -69,7 +70,8 @@ def load_library():
     lib.bsa_last_error.restype = ctypes.c_char_p
     lib.bsa_version.restype = ctypes.c_int32
     for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
-                 "bsa_executor_destroy", "bsa_mask_compact_workspace_size", "bsa_mask_compact",
+                 "bsa_executor_destroy", "bsa_executor_set_timing_events",
+                 "bsa_mask_compact_workspace_size", "bsa_mask_compact",
                  "bsa_check_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -125,6 +127,13 @@ class Executor:
         if h is None:
             raise BsaError(BSA_ERR_PARAM_NULLPTR, "executor already consumed")
         return h
+
+    def set_timing_events(self, before, after):
+        """Records torch.cuda.Event `before`/`after` around the main kernel."""
+        lib = load_library()
+        _check(lib.bsa_executor_set_timing_events(
+            self.handle, None if before is None else before.cuda_event,
+            None if after is None else after.cuda_event))
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:

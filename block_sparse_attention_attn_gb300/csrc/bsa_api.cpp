@@ -299,6 +299,7 @@ struct bsa_executor {
   uint64_t off_info = 0, off_lse2 = 0, off_dvec = 0, off_dqacc = 0, off_colcnt = 0,
            off_colptr = 0, off_entries = 0, off_items = 0, off_colinfo = 0, off_slots = 0;
   uint64_t ws_size = 0;
+  cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
 };
 
 namespace {
@@ -371,6 +372,14 @@ extern "C" {
 const char* bsa_last_error(void) { return g_last_error.c_str(); }
 
 int32_t bsa_version(void) { return 100; }
+
+bsa_status bsa_executor_set_timing_events(bsa_executor* executor, void* event_before,
+                                          void* event_after) {
+  if (executor == nullptr) return fail(BSA_ERR_PARAM_NULLPTR, "executor is NULL");
+  executor->ev_before = static_cast<cudaEvent_t>(event_before);
+  executor->ev_after = static_cast<cudaEvent_t>(event_after);
+  return ok();
+}
 
 bsa_status bsa_executor_destroy(bsa_executor* executor) {
   delete executor;
@@ -547,7 +556,9 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   what = "preprocess";
   if ((e = launch_preprocess(p, st)) != cudaSuccess) goto launch_fail;
   what = "backward";
+  if (ex->ev_before && (e = cudaEventRecord(ex->ev_before, st)) != cudaSuccess) goto launch_fail;
   if ((e = launch_bwd(p, maps, st)) != cudaSuccess) goto launch_fail;
+  if (ex->ev_after && (e = cudaEventRecord(ex->ev_after, st)) != cudaSuccess) goto launch_fail;
   what = "finalize";
   if ((e = launch_finalize(p, st)) != cudaSuccess) goto launch_fail;
   return ok();
@@ -747,7 +758,9 @@ bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* execu
   cudaError_t e = cudaMemcpyAsync(ws + ex->off_info, ex->info.data(), ex->info.size() * 4,
                                   cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, kHdrWords * 4, st);
+  if (e == cudaSuccess && ex->ev_before) e = cudaEventRecord(ex->ev_before, st);
   if (e == cudaSuccess) e = launch_fwd(f, maps, st);
+  if (e == cudaSuccess && ex->ev_after) e = cudaEventRecord(ex->ev_after, st);
   if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "forward launch failed: %s", cudaGetErrorString(e));
   return ok();
 }

@@ -135,6 +135,13 @@ bsa_status bsa_fwd_workspace_size(
 bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* executor,
                    void* stream);
 
+/* Measurement hook (the pages have no counterpart): asks the run call of
+ * `executor` to record `event_before` on its stream just before the main
+ * tensor-core kernel (backward or forward) and `event_after` just after it.
+ * Both are caller-created cudaEvent_t handles (NULL = do not record). */
+bsa_status bsa_executor_set_timing_events(bsa_executor* executor, void* event_before,
+                                          void* event_after);
+
 /* Frees an executor that was never passed to a run call. NULL is a no-op. */
 bsa_status bsa_executor_destroy(bsa_executor* executor);
 
