@@ -171,11 +171,11 @@ def make_inputs(w, dev):
     dout, q, k, v = (torch.from_numpy(x).to(dt).to(dev) for x in w.tensors())
     mask = None if w.mask is None else torch.from_numpy(w.mask).to(dev)
     seq = dict(actual_seq_lengths=w.seq_q, actual_seq_lengths_kv=w.seq_kv)
-    out, lse, _ = bsa.block_sparse_attention_fwd(q, k, v, block_sparse_mask=mask,
+    out, lse, fws = bsa.block_sparse_attention_fwd(q, k, v, block_sparse_mask=mask,
                                                  block_shape=[w.bx, w.by], layout=w.layout,
                                                  num_key_value_heads=w.N2, scale_value=w.scale,
                                                  **seq)
-    torch.cuda.synchronize()
+    bsa.bsa_check_status(fws)
     return dict(dout=dout, query=q, key=k, value=v, attention_out=out, softmax_lse=lse,
                 block_sparse_mask=mask), seq
 

@@ -122,6 +122,21 @@ bool encode_map(CUtensorMap* m, const void* base, int dtype, int layout, int64_t
   return r == CUDA_SUCCESS;
 }
 
+// fp32 [rows, D] view of the dQ accumulator for the TMA reduce-add: box of
+// 32 columns (128 bytes) x 32 rows, 128-byte swizzle.
+bool encode_acc_map(CUtensorMap* m, void* base, int64_t D, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(D * 4)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int query_num_sms(bsa_status* st) {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -532,7 +547,8 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   if (!encode_map(&maps.q, ex->q, g.dtype, g.layout, g.D, rows_q, heads_q) ||
       !encode_map(&maps.dout, ex->dout, g.dtype, g.layout, g.D, rows_q, heads_q) ||
       !encode_map(&maps.k, ex->k, g.dtype, g.layout, g.D, rows_k, heads_k) ||
-      !encode_map(&maps.v, ex->v, g.dtype, g.layout, g.D, rows_k, heads_k))
+      !encode_map(&maps.v, ex->v, g.dtype, g.layout, g.D, rows_k, heads_k) ||
+      !encode_acc_map(&maps.dqacc, p.dqacc, g.D, (int64_t)g.N1 * std::max(p.Rq, 1)))
     return fail(BSA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed");
 
   cudaError_t e = cudaMemcpyAsync(ws + ex->off_info, ex->info.data(), ex->info.size() * 4,

@@ -131,7 +131,7 @@ template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-          const Plan p) {
+          const __grid_constant__ CUtensorMap tm_acc, const Plan p) {
   using S = Smem<D>;
   using E = Elem<DT>;
   using T = typename E::T;
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_acc);
   }
   tc_fence_before();
   __syncthreads();
@@ -561,21 +562,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t ent = p.entries[e];
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
-        const bool valid = (it * 128 + r) < Lq;
         if (!mbar_wait(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
         tc_fence_after();
-        float* dst = p.dqacc + ((int64_t)h * p.Rq + p.qrow[ii.b] + it * 128 + r) * D;
+        // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp stages
+        // its 32 rows, 64 columns at a time, in the dS buffer (8 KB per warp:
+        // two 32x32 fp32 boxes, 128-byte swizzled). The buffer is free here:
+        // the dQ MMA that read dS has completed, and the softmax warps only
+        // rewrite it after the next dP MMA, which waits for this drain. Rows
+        // past the query length carry exact zeros (dS = 0 there) and land in
+        // the padded part of the accumulator.
+        uint8_t* stage = sdS + qd * 8192;
+        const int grow = h * p.Rq + p.qrow[ii.b] + it * 128 + qd * 32;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + kColP + 32 * c, x);
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + 32 * c);
+        for (int hf = 0; hf < D / 64; ++hf) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_off + kColP + 64 * hf + 32 * c, x);
+            uint8_t* rowp = stage + c * 4096 + lane * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              atomicAdd(d4 + j, make_float4(__uint_as_float(x[4 * j]), __uint_as_float(x[4 * j + 1]),
-                                            __uint_as_float(x[4 * j + 2]), __uint_as_float(x[4 * j + 3])));
+              *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
           }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tm_acc, stage, 64 * hf, grow);
+            tma_reduce_add_2d(&tm_acc, stage + 4096, 64 * hf + 32, grow);
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
@@ -649,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++itc;
     }
     if (where) record_error(p.header, where);
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -668,7 +687,7 @@ cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
   int grid = p.num_sms;
   if (p.max_items < grid) grid = p.max_items;
   if (grid < 1) grid = 1;
-  k_bwd<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, p);
+  k_bwd<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, p);
   return cudaGetLastError();
 }
 

@@ -283,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    uint32_t n = 0, itc = 0;
+    uint32_t n = 0, itc = 0;  // n: K/V stages (end markers included)
+    uint32_t m = 0;           // m: computed key tiles (S/P buffers, PV commits)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ);
     while (true) {
@@ -299,15 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (true) {
         const int st = n & 1;
         if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
-        const int m = meta[st];
-        if (m < 0) {
+        const int mt = meta[st];
+        if (mt < 0) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
           ++n;
           break;
         }
-        const uint32_t sb = st;
-        if (!mbar_wait(&bars[kPvDone0 + sb], ((n >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
+        const uint32_t sb = m & 1;
+        if (!mbar_wait(&bars[kPvDone0 + sb], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
         const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&bars[kSFull0 + sb]);
         }
         __syncwarp();
-        if (!mbar_wait(&bars[kPReady0 + sb], (n >> 1) & 1, abort_flag)) { where = kErrWaitP; break; }
+        if (!mbar_wait(&bars[kPReady0 + sb], (m >> 1) & 1, abort_flag)) { where = kErrWaitP; break; }
         if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
         tc_fence_after();
         if (lane == 0) {  // O += P V: A = P (TMEM, packed in the S buffer), B = V (MN-major)
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         ++j;
         ++n;
+        ++m;
       }
       if (where) break;
       if (lane == 0) {
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- softmax
     const int s = warp * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    uint32_t n = 0, itc = 0;
+    uint32_t n = 0, itc = 0, m_step = 0;  // stages / computed key tiles (as in the MMA warp)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
@@ -376,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
         if (mt < 0) { ++n; break; }
         const int jt = mt & 0xFFFFFF, bits = mt >> 24;
-        const uint32_t sb = st;
+        const uint32_t sb = m_step & 1;
         const uint32_t colS = sb ? kColS1 : kColS0;
-        if (!mbar_wait(&bars[kSFull0 + sb], (n >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
+        if (!mbar_wait(&bars[kSFull0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
         const int t_lim = Lk - jt * 128;
         const int s_sub = p.rb == 2 ? (s >> 6) : 0;
@@ -400,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool grow = mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY);
         if (__any_sync(0xffffffffu, grow) && j > 0) {
           // rescale O rows whose max grew, after the previous PV has landed
-          const uint32_t pb = (n - 1) & 1;
-          if (!mbar_wait(&bars[kPvDone0 + pb], ((n - 1) >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+          const uint32_t pb = (m_step - 1) & 1;
+          if (!mbar_wait(&bars[kPvDone0 + pb], ((m_step - 1) >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
           tc_fence_after();
           const float alpha = grow ? ex2_approx(m - mx) : 1.f;
 #pragma unroll
@@ -446,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars[kPReady0 + sb]);
         ++j;
         ++n;
+        ++m_step;
       }
       if (where) break;
       // epilogue: Out = O / l, lse = (m + log2 l) * ln 2

@@ -155,12 +155,18 @@ __global__ void k_scan(const int* in, int* out, int n) {
 //  1. colptr = exclusive scan of the grouped column counts;
 //  2. per key tile gc (all G heads of the group): n = its active tiles; a
 //     column longer than the chunk length L (and while partial slots remain)
-//     is split into ceil(n/L) equal chunks that add into an fp32 slot;
-//  3. items: split chunks first (the longest work), then one item per
-//     non-empty column in (b, g, jt) order.
-__global__ void k_plan(Plan p) {
+//     is split into ceil(n/L) balanced chunks that add into an fp32 slot;
+//  3. items are ordered longest first (counting sort on the item length), so
+//     the persistent CTAs pick the long work before the short work.
+__device__ __forceinline__ int chunk_begin(int n, int chunks, int c) {
+  return (int)(((int64_t)c * n) / chunks);
+}
+
+__global__ void __launch_bounds__(1024) k_plan(Plan p) {
+  constexpr int kBuckets = 1024;  // item length bucket (lengths >= 1023 share one)
   __shared__ int ws[32];
   __shared__ int s_L;
+  __shared__ int hist[kBuckets];
   int carry = 0;
   for (int base = 0; base < p.NC; base += blockDim.x) {
     const int i = base + threadIdx.x;
@@ -177,10 +183,11 @@ __global__ void k_plan(Plan p) {
     if (L < p.min_chunk) L = p.min_chunk;
     s_L = L;
   }
+  hist[threadIdx.x] = 0;
   __syncthreads();
   const int L = s_L;
-  // pass 0: slots; pass 1: split items; pass 2: single items
-  int slot_carry = 0, split_carry = 0;
+  // pass 1: split decision, slots, length histogram (descending buckets)
+  int slot_carry = 0;
   for (int base = 0; base < p.NGC; base += blockDim.x) {
     const int gc = base + threadIdx.x;
     int n = 0;
@@ -189,39 +196,41 @@ __global__ void k_plan(Plan p) {
     int tot;
     const int sidx = block_exclusive_scan(want, ws, &tot) + slot_carry;
     slot_carry += tot;
-    const int split = want && (sidx < p.max_slots);
-    const int chunks = split ? (n + L - 1) / L : 0;
-    const int cidx = block_exclusive_scan(chunks, ws, &tot) + split_carry;
-    split_carry += tot;
     if (gc < p.NGC) {
+      const int split = want && (sidx < p.max_slots);
       p.colinfo[gc] = (n == 0) ? -1 : (split ? sidx : -2);
-      if (split) {
-        const int e0 = p.colptr[gc * p.G];
-        for (int c = 0; c < chunks; ++c) {  // balanced: every chunk is non-empty
-          const int b0 = e0 + (int)(((int64_t)c * n) / chunks);
-          const int b1 = e0 + (int)(((int64_t)(c + 1) * n) / chunks);
-          p.items[cidx + c] = make_int4(gc, b0, b1, sidx);
-        }
+      const int chunks = split ? (n + L - 1) / L : (n > 0 ? 1 : 0);
+      for (int c = 0; c < chunks; ++c) {
+        const int len = chunk_begin(n, chunks, c + 1) - chunk_begin(n, chunks, c);
+        atomicAdd(&hist[kBuckets - 1 - min(len, kBuckets - 1)], 1);
       }
     }
   }
-  const int n_split_items = split_carry;
-  int single_carry = 0;
+  __syncthreads();
+  int total_items;
+  {
+    const int v = hist[threadIdx.x];
+    const int ex = block_exclusive_scan(v, ws, &total_items);
+    hist[threadIdx.x] = ex;  // bucket start offsets
+  }
+  __syncthreads();
+  // pass 2: place the items
   for (int base = 0; base < p.NGC; base += blockDim.x) {
     const int gc = base + threadIdx.x;
-    int single = 0, n = 0, e0 = 0;
-    if (gc < p.NGC) {
-      e0 = p.colptr[gc * p.G];
-      n = p.colptr[(gc + 1) * p.G] - e0;
-      single = (p.colinfo[gc] == -2) ? 1 : 0;
+    if (gc >= p.NGC) continue;
+    const int info = p.colinfo[gc];
+    if (info == -1) continue;
+    const int e0 = p.colptr[gc * p.G];
+    const int n = p.colptr[(gc + 1) * p.G] - e0;
+    const int chunks = info >= 0 ? (n + L - 1) / L : 1;
+    for (int c = 0; c < chunks; ++c) {
+      const int b0 = chunk_begin(n, chunks, c), b1 = chunk_begin(n, chunks, c + 1);
+      const int pos = atomicAdd(&hist[kBuckets - 1 - min(b1 - b0, kBuckets - 1)], 1);
+      p.items[pos] = make_int4(gc, e0 + b0, e0 + b1, info >= 0 ? info : -1);
     }
-    int tot;
-    const int idx = block_exclusive_scan(single, ws, &tot) + single_carry + n_split_items;
-    single_carry += tot;
-    if (single) p.items[idx] = make_int4(gc, e0, e0 + n, -1);
   }
   if (threadIdx.x == 0) {
-    p.header[kHdrNumItems] = n_split_items + single_carry;
+    p.header[kHdrNumItems] = total_items;
     p.header[kHdrTotalTiles] = T;
     p.header[kHdrSlotsUsed] = min(slot_carry, p.max_slots);
     p.header[kHdrChunkLen] = L;

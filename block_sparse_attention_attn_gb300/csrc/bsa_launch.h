@@ -40,6 +40,7 @@ cudaError_t launch_finalize(const Plan& p, cudaStream_t st);
 // boxes, 128-byte swizzle): BNSD (d, s, b*N+h), TND (d, h, token).
 struct BwdMaps {
   CUtensorMap q, k, v, dout;
+  CUtensorMap dqacc;  // fp32 [N1*Rq rows, D], box 32 x 32, 128-byte swizzle (reduce-add)
 };
 cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st);
 size_t bwd_smem_bytes(int D);

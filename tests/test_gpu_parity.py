@@ -213,6 +213,15 @@ def test_large_workload_sampled(name):
     check(f"{name}:dk", np.array(got_k), np.array(ref_k))
     check(f"{name}:dv", np.array(got_v), np.array(ref_v))
     assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    # the companion forward on the full workload (many query tiles per CTA)
+    mask = None if w.mask is None else torch.from_numpy(w.mask).to(DEV)
+    fo, fl, fws = bsa.block_sparse_attention_fwd(
+        q.to(DEV), k.to(DEV), v.to(DEV), block_sparse_mask=mask, block_shape=[w.bx, w.by],
+        actual_seq_lengths=w.seq_q, actual_seq_lengths_kv=w.seq_kv, layout=w.layout,
+        num_key_value_heads=w.N2, scale_value=w.scale)
+    bsa.bsa_check_status(fws)
+    check(f"{name}:fwd_out", f64(fo), f64(tout))
+    np.testing.assert_allclose(f64(fl), f64(tlse), rtol=1e-4, atol=2e-3)
 
 
 # ------------------------------------------------------------- compaction
