@@ -98,6 +98,7 @@ struct Elem<kDtF16> {
 __device__ __forceinline__ void record_error(int* header, int where) {
   atomicCAS(&header[kHdrErrorWhere], 0, where);
   atomicExch(&header[kHdrError], 1);
+  atomicAdd(&header[kHdrErrorCounts + (where & 15)], 1);  // every failing wait, by code
 }
 
 // Zero rows [r0, 128) of a [128 x 64*panels] swizzled tile (full 128-byte rows,

@@ -28,7 +28,8 @@ enum HeaderWord {
   kHdrTotalTiles = 3,  // active tiles
   kHdrSlotsUsed = 4,   // split columns that got an fp32 partial slot
   kHdrChunkLen = 5,    // split threshold used
-  kHdrErrorWhere = 6,  // code of the wait that gave up
+  kHdrErrorWhere = 6,  // code of the first wait that gave up
+  kHdrErrorCounts = 16, // [16, 32): number of failed waits per code
   kHdrWords = 64
 };
 

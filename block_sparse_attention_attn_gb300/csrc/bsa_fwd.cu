@@ -76,6 +76,7 @@ struct Elem<kDtF16> {
 __device__ __forceinline__ void record_error(int* header, int where) {
   atomicCAS(&header[kHdrErrorWhere], 0, where);
   atomicExch(&header[kHdrError], 1);
+  atomicAdd(&header[kHdrErrorCounts + (where & 15)], 1);  // every failing wait, by code
 }
 
 __device__ __forceinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
@@ -339,6 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++m;
       }
       if (where) break;
+      // every item waits for the previous epilogue exactly once (a parity wait
+      // cannot tell phase c from phase c-2, so no item may skip it)
+      if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
       if (lane == 0) {
         tc_commit(&bars[kOFull]);
         tc_commit(&bars[kQEmpty]);

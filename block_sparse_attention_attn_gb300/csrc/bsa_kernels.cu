@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     p.header[kHdrWorkCounter] = 0;
     p.header[kHdrError] = 0;
     p.header[kHdrErrorWhere] = 0;
+    for (int i = 0; i < 16; ++i) p.header[kHdrErrorCounts + i] = 0;
   }
 }
 
