@@ -165,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kKvEmpty], 1);
     mbar_init(&bars[kQFull0], 2);
     mbar_init(&bars[kQFull1], 2);
-    mbar_init(&bars[kQEmpty0], 1);
-    mbar_init(&bars[kQEmpty1], 1);
+    mbar_init(&bars[kQEmpty0], 5);  // dK MMA commit + 4 drain warps (dQ staging done)
+    mbar_init(&bars[kQEmpty1], 5);
     mbar_init(&bars[kQAux0], 1);
     mbar_init(&bars[kQAux1], 1);
     mbar_init(&bars[kSFull], 1);
@@ -246,9 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c1 = p.layout == kLayoutBNSD ? ii.jt * 128 : ii.g;
         const int c2 = p.layout == kLayoutBNSD ? ii.b * p.N2 + ii.g : p.cu_k[ii.b] + ii.jt * 128;
 #pragma unroll
+        const uint64_t pol = l2_policy_evict_first();  // K/V: read once per item
         for (int pn = 0; pn < kPanels; ++pn) {
-          tma_load_3d(sK + pn * kPanel, &tm_k, &bars[kKvTma], pn * 64, c1, c2);
-          tma_load_3d(sV + pn * kPanel, &tm_v, &bars[kKvTma], pn * 64, c1, c2);
+          tma_load_3d_hint(sK + pn * kPanel, &tm_k, &bars[kKvTma], pn * 64, c1, c2, pol);
+          tma_load_3d_hint(sV + pn * kPanel, &tm_v, &bars[kKvTma], pn * 64, c1, c2, pol);
         }
       }
       for (int e = ii.e0; e < ii.e1 && ok; ++e) {
@@ -565,40 +566,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = ii.g * p.G + entry_hl(ent);
         if (!mbar_wait(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
         tc_fence_after();
-        // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp stages
-        // its 32 rows, 64 columns at a time, in the dS buffer (8 KB per warp:
-        // two 32x32 fp32 boxes, 128-byte swizzled). The buffer is free here:
-        // the dQ MMA that read dS has completed, and the softmax warps only
-        // rewrite it after the next dP MMA, which waits for this drain. Rows
-        // past the query length carry exact zeros (dS = 0 there) and land in
-        // the padded part of the accumulator.
-        uint8_t* stage = sdS + qd * 8192;
+        // dQ tile -> fp32 accumulator. The tile is copied from TMEM into the
+        // Q/dO buffers of its own pipeline stage (exactly 128 x D fp32 = two
+        // tiles of 16-bit Q and dO), which are dead here: the dK and dV MMAs,
+        // their only readers, completed before dq_full. TMEM is released at
+        // once, then TMA reduce-adds drain the staged boxes (32 rows x 32
+        // fp32, 128-byte swizzled) while the next tile computes; the stage
+        // goes back to the producer when the copies have read it. Rows past
+        // the query length carry exact zeros (dS = 0 there) and land in the
+        // padded part of the accumulator.
+        const int st = n & 1;
+        uint8_t* stq = sQ0 + st * S::kTileBytes;
+        uint8_t* stdo = sdO0 + st * S::kTileBytes;
         const int grow = h * p.Rq + p.qrow[ii.b] + it * 128 + qd * 32;
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lane_off + kColP + 32 * c, x);
+          const int off = (qd * (D / 32) + c) * 4096;
+          uint8_t* box = off < S::kTileBytes ? stq + off : stdo + (off - S::kTileBytes);
+          uint8_t* rowp = box + lane * 128;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_off + kColP + 64 * hf + 32 * c, x);
-            uint8_t* rowp = stage + c * 4096 + lane * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
-                  make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_2d(&tm_acc, stage, 64 * hf, grow);
-            tma_reduce_add_2d(&tm_acc, stage + 4096, 64 * hf + 32, grow);
-            bulk_commit_group();
-            bulk_wait_read_all();
-          }
-          __syncwarp();
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
         }
         tc_fence_before();
+        fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kDqEmpty]);
+        if (lane == 0) {
+          mbar_arrive(&bars[kDqEmpty]);  // TMEM columns free for the next dP
+#pragma unroll
+          const uint64_t pol = l2_policy_evict_last();  // keep dQ accumulator rows in L2
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            const int off = (qd * (D / 32) + c) * 4096;
+            uint8_t* box = off < S::kTileBytes ? stq + off : stdo + (off - S::kTileBytes);
+            tma_reduce_add_2d_hint(&tm_acc, box, 32 * c, grow, pol);
+          }
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(&bars[kQEmpty0 + st]);  // stage buffers may be reloaded
+        }
+        __syncwarp();
         ++n;
       }
       if (where) break;
