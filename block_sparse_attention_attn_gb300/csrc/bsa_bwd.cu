@@ -64,7 +64,8 @@ struct Smem {
   static constexpr int oLse = odS + 2 * kPanel;
   static constexpr int oDv = oLse + kStages * 128 * 4;
   static constexpr int oBar = oDv + kStages * 128 * 4;
-  static constexpr int oMisc = oBar + kNumBars * 8;
+  static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;  // int4 slots need 16 B
+  static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
   static constexpr int kBytes = oMisc + 64;
 };
 
@@ -596,7 +597,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&bars[kDqEmpty]);  // TMEM columns free for the next dP
-#pragma unroll
           const uint64_t pol = l2_policy_evict_last();  // keep dQ accumulator rows in L2
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {

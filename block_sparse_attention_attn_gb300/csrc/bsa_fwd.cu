@@ -48,7 +48,8 @@ struct Smem {
   static constexpr int oK = oQ + kTileBytes;       // [2]
   static constexpr int oV = oK + 2 * kTileBytes;   // [2]
   static constexpr int oBar = oV + 2 * kTileBytes;
-  static constexpr int oMisc = oBar + kNumBars * 8;
+  static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;  // int4 slots need 16 B
+  static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
   static constexpr int kBytes = oMisc + 128;
 };
 
