@@ -36,7 +36,7 @@ FALLBACK_PEAK = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="w1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
