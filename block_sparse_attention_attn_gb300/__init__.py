@@ -6,6 +6,7 @@ marshals arguments into that library; importing it never loads CUDA, and every
 compute call raises if the library has not been built.
 """
 from .binding import (bsa_grad_workspace_size, bsa_grad, bsa_fwd_workspace_size,  # noqa: F401
-                      bsa_fwd, bsa_mask_compact, bsa_check_status, BsaError,
+                      bsa_fwd, bsa_mask_compact, bsa_mask_compact_noalloc, bsa_check_status,
+                      BsaError,
                       block_sparse_attention_grad, block_sparse_attention_fwd,
                       load_library, library_path)

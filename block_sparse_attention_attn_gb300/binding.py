@@ -66,13 +66,15 @@ def load_library():
     lib.bsa_mask_compact_workspace_size.argtypes = [T, i64, i64, P(u64)]
     lib.bsa_mask_compact.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp, vp, vp,
                                      u64, vp]
+    lib.bsa_mask_compact_noalloc.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp,
+                                             vp, vp]
     lib.bsa_check_status.argtypes = [vp, vp]
     lib.bsa_last_error.restype = ctypes.c_char_p
     lib.bsa_version.restype = ctypes.c_int32
     for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
                  "bsa_executor_destroy", "bsa_executor_set_timing_events",
                  "bsa_mask_compact_workspace_size", "bsa_mask_compact",
-                 "bsa_check_status"):
+                 "bsa_mask_compact_noalloc", "bsa_check_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -227,6 +229,22 @@ def bsa_mask_compact(mask: torch.Tensor, bx: int, by: int, actual_seq_lengths=No
     torch.cuda.synchronize(dev)
     nnz = int(row_ptr[-1].item())
     return row_ptr, col_idx[:nnz], col_ptr, row_idx[:nnz]
+
+
+def bsa_mask_compact_noalloc(mask: torch.Tensor, bx: int, by: int, row_ptr, col_idx, col_ptr,
+                             row_idx, actual_seq_lengths=None, actual_seq_lengths_kv=None,
+                             stream=None):
+    """The allocation-free compaction: writes the CSR/CSC into the given int32
+    device tensors (col_idx/row_idx sized for the dense bound) using only the
+    library's built-in scratch array. For callers that cannot allocate device
+    memory; calls that overlap on the GPU race on the shared scratch."""
+    lib = load_library()
+    d = _desc(mask)
+    sq, nsq = _i64_array(actual_seq_lengths)
+    sk, nsk = _i64_array(actual_seq_lengths_kv)
+    _check(lib.bsa_mask_compact_noalloc(d[0], int(bx), int(by), sq, nsq, sk, nsk,
+                                        row_ptr.data_ptr(), col_idx.data_ptr(),
+                                        col_ptr.data_ptr(), row_idx.data_ptr(), _stream(stream)))
 
 
 def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_lse,

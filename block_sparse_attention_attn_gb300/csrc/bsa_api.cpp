@@ -297,6 +297,8 @@ bool rows_vectorizable(const bsa_tensor* t) {
 
 }  // namespace
 
+void bsa::set_last_error(const char* msg) { g_last_error = msg; }
+
 // ---------------------------------------------------------------------------
 // executor
 // ---------------------------------------------------------------------------

@@ -29,6 +29,9 @@ struct CompactArgs {
   int plain;           // 1: store the tile index only; 0: packed entry
 };
 
+// Sets the thread's bsa_last_error() text (used by entry points outside bsa_api.cpp).
+void set_last_error(const char* msg);
+
 cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st);
 cudaError_t launch_rows(const CompactArgs& a, int fill, cudaStream_t st);
 cudaError_t launch_scan(const int* in, int* out, int n, cudaStream_t st);

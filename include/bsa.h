@@ -23,8 +23,8 @@
  *     recorded in the workspace and reported by bsa_check_status.
  *   - Every call returns a bsa_status; on failure bsa_last_error() returns a
  *     one-line explanation (thread-local, valid until the next call).
- *   - No call allocates device memory: all scratch lives in the caller's
- *     workspace.
+ *   - No call allocates device memory: scratch lives in the caller's workspace
+ *     (bsa_mask_compact_noalloc: in an array built into the library).
  */
 #ifndef BSA_H_
 #define BSA_H_
@@ -162,6 +162,24 @@ bsa_status bsa_mask_compact(const bsa_tensor* block_sparse_mask, int64_t bx, int
                             int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
                             int32_t* row_idx, void* workspace, uint64_t workspace_size,
                             void* stream);
+
+/* bsa_mask_compact_noalloc - the compaction of bsa_mask_compact for callers that
+ * cannot allocate device memory (a caller-owned pool that forbids new
+ * allocations, an embedded runtime without a device allocator, a fixed memory
+ * budget). The pages have no counterpart of this call. Same arguments and
+ * outputs as bsa_mask_compact minus the workspace: the scratch is a 4 MiB array
+ * built into the library (held by every GPU that loads it until exit); the call
+ * allocates no device memory. Rejects with 161002 masks whose scratch
+ * (4*(2*B + B*N*(Mq+1) + B*N*(Mk+1)) bytes, each part rounded up to 256) does not
+ * fit, and B > 1024. All calls share the array and it keeps the last call's
+ * contents: calls that overlap on the GPU race. The first call on a device
+ * looks up the array's address (with that device current); make it before any
+ * stream capture. Asynchronous on `stream`. */
+bsa_status bsa_mask_compact_noalloc(const bsa_tensor* block_sparse_mask, int64_t bx, int64_t by,
+                                    const int64_t* actual_seq_lengths, int64_t n_seq,
+                                    const int64_t* actual_seq_lengths_kv, int64_t n_seq_kv,
+                                    int32_t* row_ptr, int32_t* col_idx, int32_t* col_ptr,
+                                    int32_t* row_idx, void* stream);
 
 /* Synchronizes `stream`, then reads the error word a run call left at the start
  * of `workspace`: BSA_OK, or BSA_ERR_INNER if a kernel gave up a bounded wait
