@@ -63,6 +63,7 @@ def load_library():
     lib.bsa_fwd.argtypes = [vp, u64, vp, vp]
     lib.bsa_executor_destroy.argtypes = [vp]
     lib.bsa_executor_set_timing_events.argtypes = [vp, vp, vp]
+    lib.bsa_executor_set_wait_test.argtypes = [vp, ctypes.c_int32]
     lib.bsa_mask_compact_workspace_size.argtypes = [T, i64, i64, P(u64)]
     lib.bsa_mask_compact.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp, vp, vp,
                                      u64, vp]
@@ -73,6 +74,7 @@ def load_library():
     lib.bsa_version.restype = ctypes.c_int32
     for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
                  "bsa_executor_destroy", "bsa_executor_set_timing_events",
+                 "bsa_executor_set_wait_test",
                  "bsa_mask_compact_workspace_size", "bsa_mask_compact",
                  "bsa_mask_compact_noalloc", "bsa_check_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -136,6 +138,11 @@ class Executor:
         _check(lib.bsa_executor_set_timing_events(
             self.handle, None if before is None else before.cuda_event,
             None if after is None else after.cuda_event))
+
+    def set_wait_test(self, enable: bool = True):
+        """Failure-path test: the run's backward kernel waits once on a barrier
+        nothing completes; bsa_check_status then reports 561002."""
+        _check(load_library().bsa_executor_set_wait_test(self.handle, 1 if enable else 0))
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:

@@ -398,6 +398,13 @@ bsa_status bsa_executor_set_timing_events(bsa_executor* executor, void* event_be
   return ok();
 }
 
+bsa_status bsa_executor_set_wait_test(bsa_executor* executor, int32_t enable) {
+  if (executor == nullptr) return fail(BSA_ERR_PARAM_NULLPTR, "executor is NULL");
+  if (executor->kind != 1) return fail(BSA_ERR_PARAM_INVALID, "not a backward executor");
+  executor->plan.wait_test = enable ? 1 : 0;
+  return ok();
+}
+
 bsa_status bsa_executor_destroy(bsa_executor* executor) {
   delete executor;
   return ok();

@@ -49,7 +49,7 @@ enum Bar {
   kSFull, kDpFull, kPReady, kDsReady, kDkDone, kDqFull, kDqEmpty, kDsFree,
   kAccFull, kAccEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
-  kDrainBar,
+  kDrainBar, kNeverBar,
   kNumBars
 };
 
@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kItemEmpty0], 13);
     mbar_init(&bars[kItemEmpty1], 13);
     mbar_init(&bars[kDrainBar], 1);
+    mbar_init(&bars[kNeverBar], 1);  // nothing arrives here (wait_test)
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
@@ -348,6 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (raw.x < 0) break;
       const ItemInfo ii = decode_item(p, raw);
       if (ii.e0 >= ii.e1) { ++itc; continue; }
+      // test of the bounded waits: a barrier no one arrives at runs out, the CTA
+      // unwinds and the host reads the error code
+      if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) { where = kErrWaitTest; break; }
       if (!mbar_wait(&bars[kKvFull], itc & 1, abort_flag)) { where = kErrWaitKV; break; }
       tc_fence_after();
       bool first = true;

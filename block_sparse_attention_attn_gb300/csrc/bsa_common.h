@@ -47,6 +47,7 @@ enum ErrWhere {
   kErrWaitDQ = 9,
   kErrWaitAcc = 10,
   kErrWaitMisc = 11,
+  kErrWaitTest = 12,     // the deliberate wait of the wait_test switch
 };
 
 // Entry of a backward work list: query tile `it` of local head `hl`, with the
@@ -111,6 +112,7 @@ struct Plan {
   int max_items, max_slots, max_entries;
   int num_sms;
   int min_chunk;         // smallest split chunk
+  int wait_test;         // test of the bounded waits: 1 = one wait on a barrier nothing completes
 };
 
 }  // namespace bsa

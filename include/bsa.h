@@ -142,6 +142,13 @@ bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* execu
 bsa_status bsa_executor_set_timing_events(bsa_executor* executor, void* event_before,
                                           void* event_after);
 
+/* Test of the failure path (the pages have no counterpart): with enable != 0 the
+ * backward kernel of this executor's run waits once on a barrier nothing
+ * completes. The wait gives up after its bound (about 1 s), every warp unwinds,
+ * the run's outputs are invalid and bsa_check_status returns 561002; the CUDA
+ * context stays usable. Backward executors only. */
+bsa_status bsa_executor_set_wait_test(bsa_executor* executor, int32_t enable);
+
 /* Frees an executor that was never passed to a run call. NULL is a no-op. */
 bsa_status bsa_executor_destroy(bsa_executor* executor);
 

@@ -270,3 +270,28 @@ def test_forward_full(layout, dtype, B, N1, N2, D, bx, by, sq, skv):
     got_lse = f64(lse)
     np.testing.assert_array_equal(np.isneginf(got_lse), ~fin)
     np.testing.assert_allclose(got_lse[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
+
+
+# ------------------------------------------------------------ failure path
+def test_bounded_wait_reports_error_and_context_survives():
+    """A wait on a barrier nothing completes gives up after its bound; the host
+    reads 561002 and the next run on the same context is correct."""
+    w = small_workload(B=1, N1=2, N2=1, D=128, bx=128, by=128, seq_q=(256,), seq_kv=(256,),
+                       p=1.0, seed=41)
+    dout, q, k, v = host_inputs(w)
+    out, lse = oracle_forward(w, q, k, v)
+    tout, tlse = rounded_out_lse(w, out, lse)
+    g = [t.to(DEV) for t in (dout, q, k, v, tout, tlse)]
+    mask = torch.from_numpy(w.mask).to(DEV)
+    dq, dk, dv = (torch.empty_like(g[i]) for i in (1, 2, 3))
+    size, ex = bsa.bsa_grad_workspace_size(*g, mask, None, [128, 128], None, None, "BNSD", "BNSD",
+                                           1, 0, w.scale, dq=dq, dk=dk, dv=dv)
+    ex.set_wait_test(True)
+    ws = torch.empty(size, dtype=torch.uint8, device=DEV)
+    bsa.bsa_grad(ws, size, ex)
+    with pytest.raises(bsa.BsaError) as err:
+        bsa.bsa_check_status(ws)
+    assert err.value.status == 561002
+    hdr = ws[:128].view(torch.int32).cpu().tolist()
+    assert hdr[6] == 12 or hdr[16 + 12] > 0       # the test wait is among the recorded codes
+    full_case(w)                                   # the context still computes correctly

@@ -112,3 +112,7 @@ def test_run_call_rejects_null_executor(lib):
     assert lib.bsa_fwd(None, 0, None, None) == B.BSA_ERR_PARAM_NULLPTR
     assert "executor" in lib.bsa_last_error().decode()
     assert lib.bsa_executor_destroy(None) == 0
+
+
+def test_wait_test_switch_needs_an_executor(lib):
+    assert lib.bsa_executor_set_wait_test(None, 1) == B.BSA_ERR_PARAM_NULLPTR
