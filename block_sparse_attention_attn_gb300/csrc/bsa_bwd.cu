@@ -46,6 +46,7 @@ constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColP = 384;
 enum Bar {
   kKvTma = 0, kKvFull, kKvEmpty,
   kQFull0, kQFull1, kQEmpty0, kQEmpty1, kQAux0, kQAux1,
+  kDoFull, kDoEmpty, kDoAux,
   kSFull, kDpFull, kPReady, kDsReady, kDkDone, kDqFull, kDqEmpty, kDsFree,
   kAccFull, kAccEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
@@ -53,6 +54,11 @@ enum Bar {
   kNumBars
 };
 
+// Shared memory (D = 128: 224 KB of tiles): K, V (per item), Q in a 2-stage
+// ring (with its lse/D rows), one dO buffer, the dS tile (A operand of the dQ
+// MMA) and a 32 KB dQ staging buffer. The fp32 dQ tile (128 x D) is staged in
+// 32-column boxes: the first 64 columns in the dS buffer and the rest in the
+// staging buffer when D = 128; all of it in the staging buffer when D = 64.
 template <int D>
 struct Smem {
   static constexpr int kTileBytes = (D / 64) * kPanel;
@@ -60,8 +66,9 @@ struct Smem {
   static constexpr int oV = oK + kTileBytes;
   static constexpr int oQ = oV + kTileBytes;
   static constexpr int odO = oQ + kStages * kTileBytes;
-  static constexpr int odS = odO + kStages * kTileBytes;
-  static constexpr int oLse = odS + 2 * kPanel;
+  static constexpr int odS = odO + kTileBytes;
+  static constexpr int oStg = odS + 2 * kPanel;
+  static constexpr int oLse = oStg + 2 * kPanel;
   static constexpr int oDv = oLse + kStages * 128 * 4;
   static constexpr int oBar = oDv + kStages * 128 * 4;
   static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;  // int4 slots need 16 B
@@ -138,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using E = Elem<DT>;
   using T = typename E::T;
   constexpr int kPanels = D / 64;
-  constexpr uint32_t kTileTx = 2u * S::kTileBytes;  // two tiles per barrier
   constexpr uint32_t kIdS = idesc_f16(128, 128, E::kAB, 0, 0);   // S^T, dP^T
   constexpr uint32_t kIdKV = idesc_f16(128, D, E::kAB, 0, 1);    // dV, dK (A in TMEM)
   constexpr uint32_t kIdQ = idesc_f16(128, D, E::kAB, 1, 1);     // dQ
@@ -166,10 +172,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kKvEmpty], 1);
     mbar_init(&bars[kQFull0], 2);
     mbar_init(&bars[kQFull1], 2);
-    mbar_init(&bars[kQEmpty0], 5);  // dK MMA commit + 4 drain warps (dQ staging done)
-    mbar_init(&bars[kQEmpty1], 5);
+    mbar_init(&bars[kQEmpty0], 1);  // dK MMA commit (the last reader of Q)
+    mbar_init(&bars[kQEmpty1], 1);
     mbar_init(&bars[kQAux0], 1);
     mbar_init(&bars[kQAux1], 1);
+    mbar_init(&bars[kDoFull], 1);
+    mbar_init(&bars[kDoEmpty], 1);  // dV MMA commit (the last reader of dO)
+    mbar_init(&bars[kDoAux], 1);
     mbar_init(&bars[kSFull], 1);
     mbar_init(&bars[kDpFull], 1);
     mbar_init(&bars[kPReady], 8);
@@ -177,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kDkDone], 1);
     mbar_init(&bars[kDqFull], 1);
     mbar_init(&bars[kDqEmpty], 4);
-    mbar_init(&bars[kDsFree], 1);
+    mbar_init(&bars[kDsFree], 4);  // each drain warp: its dQ boxes in the dS buffer were read
     mbar_init(&bars[kAccFull], 1);
     mbar_init(&bars[kAccEmpty], 4);
     mbar_init(&bars[kItemFull0], 1);
@@ -207,15 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + S::oK;
   uint8_t* sV = smem + S::oV;
   uint8_t* sQ0 = smem + S::oQ;
-  uint8_t* sdO0 = smem + S::odO;
+  uint8_t* sdO = smem + S::odO;
   uint8_t* sdS = smem + S::odS;
+  uint8_t* sStg = smem + S::oStg;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     uint32_t n = 0, itc = 0;
-    uint32_t aux_cnt[2] = {0u, 0u};
-    uint32_t last_q_par[2] = {0u, 0u};
+    uint32_t aux_cnt[2] = {0u, 0u}, do_aux_cnt = 0;
+    uint32_t last_q_par[2] = {0u, 0u}, last_do_par = 0;
     int pending_q[2] = {0, 0}, pending_q_aux[2] = {0, 0};
+    int pending_do = 0, pending_do_aux = 0;
     int pending_kv = 0;
     bool ok = true;
     while (ok) {
@@ -244,10 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       pending_kv = 1;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[kKvTma], kTileTx);
+        mbar_arrive_expect_tx(&bars[kKvTma], 2u * S::kTileBytes);
         const int c1 = p.layout == kLayoutBNSD ? ii.jt * 128 : ii.g;
         const int c2 = p.layout == kLayoutBNSD ? ii.b * p.N2 + ii.g : p.cu_k[ii.b] + ii.jt * 128;
-#pragma unroll
         const uint64_t pol = l2_policy_evict_first();  // K/V: read once per item
         for (int pn = 0; pn < kPanels; ++pn) {
           tma_load_3d_hint(sK + pn * kPanel, &tm_k, &bars[kKvTma], pn * 64, c1, c2, pol);
@@ -259,25 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
         const int st = n & 1;
+        const int q0 = it * 128;
+        const bool tail = (Lq - q0) < 128;
+        const int c1 = p.layout == kLayoutBNSD ? q0 : h;
+        const int c2 = p.layout == kLayoutBNSD ? ii.b * p.N1 + h : p.cu_q[ii.b] + q0;
+        // Q (stage st) with its lse / D rows
         if (!mbar_wait(&bars[kQEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
           record_error(p.header, kErrWaitQ);
           ok = false;
           break;
         }
-        const int q0 = it * 128;
-        const bool tail = (Lq - q0) < 128;
         uint8_t* sQ = sQ0 + st * S::kTileBytes;
-        uint8_t* sdO = sdO0 + st * S::kTileBytes;
         if (lane == 0) {
           uint64_t* tb = tail ? &bars[kQAux0 + st] : &bars[kQFull0 + st];
-          mbar_arrive_expect_tx(tb, kTileTx);
-          const int c1 = p.layout == kLayoutBNSD ? q0 : h;
-          const int c2 = p.layout == kLayoutBNSD ? ii.b * p.N1 + h : p.cu_q[ii.b] + q0;
-#pragma unroll
-          for (int pn = 0; pn < kPanels; ++pn) {
-            tma_load_3d(sQ + pn * kPanel, &tm_q, tb, pn * 64, c1, c2);
-            tma_load_3d(sdO + pn * kPanel, &tm_do, tb, pn * 64, c1, c2);
-          }
+          mbar_arrive_expect_tx(tb, S::kTileBytes);
+          for (int pn = 0; pn < kPanels; ++pn) tma_load_3d(sQ + pn * kPanel, &tm_q, tb, pn * 64, c1, c2);
         }
         last_q_par[st] = (n >> 1) & 1;
         pending_q[st] = tail ? 0 : 1;
@@ -299,13 +305,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           aux_cnt[st]++;
           pending_q_aux[st] = 0;
           zero_rows(sQ, kPanels, Lq - q0, lane);
-          zero_rows(sdO, kPanels, Lq - q0, lane);
           fence_async_smem();
           __syncwarp();
         }
         if (lane == 0) {
           mbar_arrive(&bars[kQFull0 + st]);
           if (tail) mbar_arrive(&bars[kQFull0 + st]);
+        }
+        // dO (single buffer): free once the previous tile's dV MMA completed
+        if (!mbar_wait(&bars[kDoEmpty], (n & 1) ^ 1, abort_flag)) {
+          record_error(p.header, kErrWaitQ);
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint64_t* tb = tail ? &bars[kDoAux] : &bars[kDoFull];
+          mbar_arrive_expect_tx(tb, S::kTileBytes);
+          for (int pn = 0; pn < kPanels; ++pn) tma_load_3d(sdO + pn * kPanel, &tm_do, tb, pn * 64, c1, c2);
+        }
+        last_do_par = n & 1;
+        pending_do = tail ? 0 : 1;
+        pending_do_aux = tail ? 1 : 0;
+        if (tail) {
+          if (!mbar_wait(&bars[kDoAux], do_aux_cnt & 1, abort_flag)) {
+            record_error(p.header, kErrWaitQ);
+            ok = false;
+            break;
+          }
+          do_aux_cnt++;
+          pending_do_aux = 0;
+          zero_rows(sdO, kPanels, Lq - q0, lane);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kDoFull]);
         }
         if (e == ii.e0) {
           // K/V of this item: wait for the copy, clear rows past the key length
@@ -333,6 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pending_q[st]) mbar_wait_drain(&bars[kQFull0 + st], last_q_par[st]);
         if (pending_q_aux[st]) mbar_wait_drain(&bars[kQAux0 + st], aux_cnt[st] & 1);
       }
+      if (pending_do) mbar_wait_drain(&bars[kDoFull], last_do_par);
+      if (pending_do_aux) mbar_wait_drain(&bars[kDoAux], do_aux_cnt & 1);
       if (pending_kv) mbar_wait_drain(&bars[kKvTma], (itc & 1));
     }
   } else if (warp == kMmaWarp) {
@@ -358,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = ii.e0; e < ii.e1; ++e) {
         const int st = n & 1;
         const uint32_t aQ = smem_u32(sQ0 + st * S::kTileBytes);
-        const uint32_t adO = smem_u32(sdO0 + st * S::kTileBytes);
+        const uint32_t adO = smem_u32(sdO);
         if (!mbar_wait(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
         tc_fence_after();
         if (lane == 0) {  // S^T = K Q^T
@@ -372,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (!mbar_wait(&bars[kDqEmpty], (n & 1) ^ 1, abort_flag)) { where = kErrWaitDQ; break; }
+        if (!mbar_wait(&bars[kDoFull], n & 1, abort_flag)) { where = kErrWaitQ; break; }
         tc_fence_after();
         if (lane == 0) {  // dP^T = V dO^T
 #pragma unroll
@@ -395,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + kColDV, tmem + acol, sdesc_sw128(adO + k * 2048, kPanel, 1024), kIdKV,
                    (first && k == 0) ? 0u : 1u);
           }
+          tc_commit(&bars[kDoEmpty]);  // dO may be reloaded once dP and dV completed
         }
         __syncwarp();
         if (!mbar_wait(&bars[kDsReady], n & 1, abort_flag)) { where = kErrWaitDS; break; }
@@ -420,7 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc_sw128(aK + k * 2048, kPanel, 1024), kIdQ, k > 0);
           }
           tc_commit(&bars[kDqFull]);
-          tc_commit(&bars[kDsFree]);
         }
         __syncwarp();
         first = false;
@@ -571,30 +606,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = ii.g * p.G + entry_hl(ent);
         if (!mbar_wait(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
         tc_fence_after();
-        // dQ tile -> fp32 accumulator. The tile is copied from TMEM into the
-        // Q/dO buffers of its own pipeline stage (exactly 128 x D fp32 = two
-        // tiles of 16-bit Q and dO), which are dead here: the dK and dV MMAs,
-        // their only readers, completed before dq_full. TMEM is released at
-        // once, then TMA reduce-adds drain the staged boxes (32 rows x 32
-        // fp32, 128-byte swizzled) while the next tile computes; the stage
-        // goes back to the producer when the copies have read it. Rows past
-        // the query length carry exact zeros (dS = 0 there) and land in the
-        // padded part of the accumulator.
-        const int st = n & 1;
-        uint8_t* stq = sQ0 + st * S::kTileBytes;
-        uint8_t* stdo = sdO0 + st * S::kTileBytes;
+        // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp copies its
+        // 32 rows from TMEM into 32x32 fp32 boxes (128-byte swizzled): columns
+        // [0, 64) into the dS buffer and [64, 128) into the staging buffer
+        // when D = 128 (D = 64: staging buffer only), releases TMEM for the
+        // next dP, and issues the reduce-adds as two bulk groups. The dS half
+        // must be read before the softmax warps write the next dS (ds_free);
+        // the staging half is waited for before this warp stages again. Rows
+        // past the query length carry exact zeros (dS = 0 there) and land in
+        // the padded part of the accumulator.
         const int grow = h * p.Rq + p.qrow[ii.b] + it * 128 + qd * 32;
+        uint8_t* boxes_ds = sdS + qd * 8192;
+        uint8_t* boxes_stg = sStg + qd * 8192;
+        if (lane == 0) bulk_wait_read_all();  // previous tile's staging boxes were read
+        __syncwarp();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + kColP + 32 * c, x);
-          const int off = (qd * (D / 32) + c) * 4096;
-          uint8_t* box = off < S::kTileBytes ? stq + off : stdo + (off - S::kTileBytes);
-          uint8_t* rowp = box + lane * 128;
+        for (int hf = 0; hf < D / 64; ++hf) {
+          uint8_t* boxes = (D == 128 && hf == 0) ? boxes_ds : boxes_stg;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_off + kColP + 64 * hf + 32 * c, x);
+            uint8_t* rowp = boxes + c * 4096 + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+          }
         }
         tc_fence_before();
         fence_async_smem();
@@ -602,15 +640,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           mbar_arrive(&bars[kDqEmpty]);  // TMEM columns free for the next dP
           const uint64_t pol = l2_policy_evict_last();  // keep dQ accumulator rows in L2
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            const int off = (qd * (D / 32) + c) * 4096;
-            uint8_t* box = off < S::kTileBytes ? stq + off : stdo + (off - S::kTileBytes);
-            tma_reduce_add_2d_hint(&tm_acc, box, 32 * c, grow, pol);
+          if (D == 128) {
+            tma_reduce_add_2d_hint(&tm_acc, boxes_ds, 0, grow, pol);
+            tma_reduce_add_2d_hint(&tm_acc, boxes_ds + 4096, 32, grow, pol);
+            bulk_commit_group();
+            tma_reduce_add_2d_hint(&tm_acc, boxes_stg, 64, grow, pol);
+            tma_reduce_add_2d_hint(&tm_acc, boxes_stg + 4096, 96, grow, pol);
+            bulk_commit_group();
+            bulk_wait_read_1();                 // the dS-buffer group has been read
+          } else {
+            tma_reduce_add_2d_hint(&tm_acc, boxes_stg, 0, grow, pol);
+            tma_reduce_add_2d_hint(&tm_acc, boxes_stg + 4096, 32, grow, pol);
+            bulk_commit_group();
           }
-          bulk_commit_group();
-          bulk_wait_read_all();
-          mbar_arrive(&bars[kQEmpty0 + st]);  // stage buffers may be reloaded
+          mbar_arrive(&bars[kDsFree]);
         }
         __syncwarp();
         ++n;
