@@ -137,6 +137,40 @@ bool encode_acc_map(CUtensorMap* m, void* base, int64_t D, int64_t rows) {
   return r == CUDA_SUCCESS;
 }
 
+// Output view of dK or dV for TMA stores of 32-row x 64-column boxes (128-byte
+// swizzle): BNSD (d, s, n, b), TND (d, n, token), each dimension with the
+// tensor's own stride. Returns false (the kernel then stores with plain
+// per-row writes) when the layout is not expressible: unit d stride, 16-byte
+// aligned base and strides are required.
+bool encode_out_map(CUtensorMap* m, const bsa_tensor* t, int layout) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(t->data) & 15u) != 0) return false;
+  const int nd = t->ndim;
+  if (nd != (layout == kLayoutBNSD ? 4 : 3) || t->stride[nd - 1] != 1) return false;
+  for (int i = 0; i < nd - 1; ++i)
+    if ((t->stride[i] * 2) % 16 != 0 || t->stride[i] * 2 >= ((int64_t)1 << 40)) return false;
+  const CUtensorMapDataType dt =
+      t->dtype == BSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t dims[4];
+  cuuint64_t strides[3];
+  cuuint32_t box[4];
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (layout == kLayoutBNSD) {  // shape [B, N, S, D]
+    dims[0] = t->shape[3]; dims[1] = t->shape[2]; dims[2] = t->shape[1]; dims[3] = t->shape[0];
+    strides[0] = t->stride[2] * 2; strides[1] = t->stride[1] * 2; strides[2] = t->stride[0] * 2;
+    box[0] = 64; box[1] = 32; box[2] = 1; box[3] = 1;
+  } else {  // shape [T, N, D]
+    dims[0] = t->shape[2]; dims[1] = t->shape[1]; dims[2] = t->shape[0];
+    strides[0] = t->stride[1] * 2; strides[1] = t->stride[0] * 2;
+    box[0] = 64; box[1] = 1; box[2] = 32;
+  }
+  CUresult r = fn(m, dt, nd, t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int query_num_sms(bsa_status* st) {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -317,6 +351,7 @@ struct bsa_executor {
            off_colptr = 0, off_entries = 0, off_items = 0, off_colinfo = 0, off_slots = 0;
   uint64_t ws_size = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
+  CUtensorMap map_dk{}, map_dv{};  // dK / dV store views (valid when plan.dkv_tma)
 };
 
 namespace {
@@ -486,6 +521,8 @@ bsa_status bsa_grad_workspace_size(
   }
   p.dq_vec = rows_vectorizable(dq) ? 1 : 0;
   p.dkv_vec = (rows_vectorizable(dk) && rows_vectorizable(dv)) ? 1 : 0;
+  p.dkv_tma = (encode_out_map(&ex->map_dk, dk, g.layout) && encode_out_map(&ex->map_dv, dv, g.layout))
+                  ? 1 : 0;
   // work geometry
   p.NGC = g.B * g.N2 * p.Mk_t;
   p.NC = p.NGC * g.G;
@@ -559,6 +596,8 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
       !encode_map(&maps.v, ex->v, g.dtype, g.layout, g.D, rows_k, heads_k) ||
       !encode_acc_map(&maps.dqacc, p.dqacc, g.D, (int64_t)g.N1 * std::max(p.Rq, 1)))
     return fail(BSA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed");
+  maps.dk = ex->map_dk;
+  maps.dv = ex->map_dv;
 
   cudaError_t e = cudaMemcpyAsync(ws + ex->off_info, ex->info.data(), ex->info.size() * 4,
                                   cudaMemcpyHostToDevice, st);

@@ -11,20 +11,28 @@
 //
 // Design (one persistent CTA per SM, 448 threads, warp-specialised):
 //   warp 12     TMA producer: K/V tiles of the key tile (once per work item),
-//               then a 2-stage ring of Q/dO tiles plus their lse/D rows.
+//               then a 2-stage ring of Q tiles (with their lse/D rows) and
+//               one dO buffer.
 //   warp 13     tcgen05 MMA issuer (one thread) and TMEM owner (512 columns).
 //   warps 0-7   "softmax" warpgroups: TMEM lane t = key row t; warpgroup w
 //               handles query columns [64w, 64w+64): P^T (into TMEM, packed, as
-//               the A operand of the dV MMA), dS^T (into TMEM for the dK MMA
-//               and into shared memory for the dQ MMA).
-//   warps 8-11  drain: dQ tile TMEM -> fp32 atomics; at the end of a work
-//               item, dK/dV TMEM -> output (or fp32 slot for split columns).
+//               the A operand of the dV MMA) and dS (into shared memory, the
+//               operand of both the dQ and the dK MMA).
+//   warps 8-11  drain: dQ tile TMEM -> fp32 accumulator (TMA reduce-add); at
+//               the end of a work item, dK/dV TMEM -> output (or fp32 slot for
+//               split columns).
 // A work item is one key tile (b, kv head g, jt) with the query tiles of all
 // G query heads of the group that select it (so the GQA sum happens in TMEM),
 // or a chunk of such a list when the planner split a long column.
 //
+// MMA order for tile n of an item: dP(n), dV(n), S(n+1), dQ(n), dK(n). S of
+// the next tile is issued as soon as dV(n) has read P^T(n) out of the S
+// columns, so the softmax warps compute P(n+1) while the tensor pipe runs
+// dQ(n) and dK(n); dQ(n) goes first so the drain empties its TMEM columns
+// while dK(n) runs.
+//
 // TMEM columns: [0,128) dV^T, [128,256) dK^T, [256,384) S^T -> P^T,
-// [384,512) dP^T -> dS^T, later reused for dQ.
+// [384,512) dP^T, then dQ once the softmax warps have read dP^T.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -43,11 +51,19 @@ constexpr int kPanel = 128 * 128;  // 128 rows x 128 bytes (64 x 16-bit), one sw
 constexpr int kStages = 2;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColP = 384;
 
+// Offset of K-step k (16 elements) inside a 128-byte-swizzled tile, in the
+// 16-byte units of a shared-memory descriptor's address field: K-major tiles
+// step 32 bytes within a 64-element panel, MN-major tiles step 16 rows.
+__host__ __device__ constexpr uint64_t kmaj_step(int k) {
+  return static_cast<uint64_t>(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t mn_step(int k) { return static_cast<uint64_t>((k * 2048) >> 4); }
+
 enum Bar {
-  kKvTma = 0, kKvFull, kKvEmpty,
+  kBufFull0 = 0, kBufFull1, kBufAux0, kBufAux1, kBufEmpty0, kBufEmpty1,
   kQFull0, kQFull1, kQEmpty0, kQEmpty1, kQAux0, kQAux1,
   kDoFull, kDoEmpty, kDoAux,
-  kSFull, kDpFull, kPReady, kDsReady, kDkDone, kDqFull, kDqEmpty, kDsFree,
+  kSFull, kDpFull, kPReady, kDsReady, kDvDone, kDqFull, kDqEmpty, kDsFree,
   kAccFull, kAccEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
   kDrainBar, kNeverBar,
@@ -55,10 +71,9 @@ enum Bar {
 };
 
 // Shared memory (D = 128: 224 KB of tiles): K, V (per item), Q in a 2-stage
-// ring (with its lse/D rows), one dO buffer, the dS tile (A operand of the dQ
-// MMA) and a 32 KB dQ staging buffer. The fp32 dQ tile (128 x D) is staged in
-// 32-column boxes: the first 64 columns in the dS buffer and the rest in the
-// staging buffer when D = 128; all of it in the staging buffer when D = 64.
+// ring (with its lse/D rows), one dO buffer, the dS tile (operand of the dQ
+// and dK MMAs) and a 32 KB dQ staging buffer. The fp32 dQ tile (128 x D) is
+// staged in 32 x 32 boxes, 64 columns at a time.
 template <int D>
 struct Smem {
   static constexpr int kTileBytes = (D / 64) * kPanel;
@@ -111,7 +126,7 @@ __device__ __forceinline__ void record_error(int* header, int where) {
 
 // Zero rows [r0, 128) of a [128 x 64*panels] swizzled tile (full 128-byte rows,
 // so the swizzle does not matter). Executed by one warp.
-__device__ __forceinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
+__device__ __noinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
   const int nrows = 128 - r0;
   const int n16 = nrows * 8;  // 16-byte chunks per panel
   for (int pnl = 0; pnl < panels; ++pnl) {
@@ -136,17 +151,33 @@ __device__ __forceinline__ ItemInfo decode_item(const Plan& p, int4 it) {
   return r;
 }
 
+// Claims the next work item from the device queue (lane 0) and hands it to
+// every lane of the warp; x = -1 marks the end of the work.
+__device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
+  int4 it = make_int4(-1, 0, 0, -1);
+  if (lane == 0) {
+    const int idx = atomicAdd(&p.header[kHdrWorkCounter], 1);
+    if (idx < p.header[kHdrNumItems]) it = p.items[idx];
+  }
+  it.x = __shfl_sync(0xffffffffu, it.x, 0);
+  it.y = __shfl_sync(0xffffffffu, it.y, 0);
+  it.z = __shfl_sync(0xffffffffu, it.z, 0);
+  it.w = __shfl_sync(0xffffffffu, it.w, 0);
+  return it;
+}
+
 template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-          const __grid_constant__ CUtensorMap tm_acc, const Plan p) {
+          const __grid_constant__ CUtensorMap tm_acc, const __grid_constant__ CUtensorMap tm_dk,
+          const __grid_constant__ CUtensorMap tm_dv, const Plan p) {
   using S = Smem<D>;
   using E = Elem<DT>;
   using T = typename E::T;
   constexpr int kPanels = D / 64;
   constexpr uint32_t kIdS = idesc_f16(128, 128, E::kAB, 0, 0);   // S^T, dP^T
-  constexpr uint32_t kIdKV = idesc_f16(128, D, E::kAB, 0, 1);    // dV, dK (A in TMEM)
+  constexpr uint32_t kIdKV = idesc_f16(128, D, E::kAB, 0, 1);    // dV (A in TMEM), dK
   constexpr uint32_t kIdQ = idesc_f16(128, D, E::kAB, 1, 1);     // dQ
 
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -167,9 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(&bars[kKvTma], 1);
-    mbar_init(&bars[kKvFull], 1);
-    mbar_init(&bars[kKvEmpty], 1);
+    mbar_init(&bars[kBufFull0], 1);   // K/V buffer loaded (TMA bytes, or producer after zeroing)
+    mbar_init(&bars[kBufFull1], 1);
+    mbar_init(&bars[kBufAux0], 1);    // K/V buffer bytes of a key tile that ends early
+    mbar_init(&bars[kBufAux1], 1);
+    mbar_init(&bars[kBufEmpty0], 1);  // MMA commit after the buffer's last reader
+    mbar_init(&bars[kBufEmpty1], 1);
     mbar_init(&bars[kQFull0], 2);
     mbar_init(&bars[kQFull1], 2);
     mbar_init(&bars[kQEmpty0], 1);  // dK MMA commit (the last reader of Q)
@@ -183,10 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kDpFull], 1);
     mbar_init(&bars[kPReady], 8);
     mbar_init(&bars[kDsReady], 8);
-    mbar_init(&bars[kDkDone], 1);
+    mbar_init(&bars[kDvDone], 1);   // dV MMA commit (P^T read, S columns free)
     mbar_init(&bars[kDqFull], 1);
     mbar_init(&bars[kDqEmpty], 4);
-    mbar_init(&bars[kDsFree], 4);  // each drain warp: its dQ boxes in the dS buffer were read
+    mbar_init(&bars[kDsFree], 1);  // dK MMA commit (the last reader of the dS tile)
     mbar_init(&bars[kAccFull], 1);
     mbar_init(&bars[kAccEmpty], 4);
     mbar_init(&bars[kItemFull0], 1);
@@ -207,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_acc);
+    if (p.dkv_tma) {
+      tma_prefetch_desc(&tm_dk);
+      tma_prefetch_desc(&tm_dv);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -220,51 +258,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sdS = smem + S::odS;
   uint8_t* sStg = smem + S::oStg;
 
+  // K and V of a work item live in the two key-tile buffers, with roles that
+  // alternate from item to item: item ic keeps K in buffer (ic & 1) and V in
+  // the other one. The next item's K is then loaded into the buffer whose V
+  // was last read by the current item's final dP, and its V into the buffer
+  // whose K was last read by the final dQ, so both loads overlap the end of
+  // the current item.
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t n = 0, itc = 0;
-    uint32_t aux_cnt[2] = {0u, 0u}, do_aux_cnt = 0;
-    uint32_t last_q_par[2] = {0u, 0u}, last_do_par = 0;
+    uint32_t n = 0, fc = 0, ic = 0;  // tiles, ring slots filled, non-empty items
+    uint32_t aux_cnt[2] = {0u, 0u}, do_aux_cnt = 0, buf_aux_cnt[2] = {0u, 0u};
+    uint32_t last_q_par[2] = {0u, 0u}, last_do_par = 0, last_buf_par[2] = {0u, 0u};
     int pending_q[2] = {0, 0}, pending_q_aux[2] = {0, 0};
     int pending_do = 0, pending_do_aux = 0;
-    int pending_kv = 0;
+    int pending_buf[2] = {0, 0}, pending_buf_aux[2] = {0, 0};
     bool ok = true;
+    // Items are claimed one ahead, so the next key tile's K/V can be
+    // prefetched into L2 while the current item runs.
+    int4 next = claim_item(p, lane);
+    auto kv_coords = [&](const ItemInfo& it, int& c1, int& c2) {
+      c1 = p.layout == kLayoutBNSD ? it.jt * 128 : it.g;
+      c2 = p.layout == kLayoutBNSD ? it.b * p.N2 + it.g : p.cu_k[it.b] + it.jt * 128;
+    };
+    // K or V of item `it` into buffer `bi` (free once the previous item's last
+    // reader of that buffer completed); a key tile that ends early is loaded
+    // through the aux barrier, its rows past the key length are cleared and
+    // then the full barrier is released by hand.
+    auto load_buf = [&](int bi, const CUtensorMap* tm, const ItemInfo& it, int t_valid) -> bool {
+      if (!mbar_wait(&bars[kBufEmpty0 + bi], (ic & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitKV);
+        return false;
+      }
+      const bool tail = t_valid < 128;
+      uint8_t* dst = bi == 0 ? sK : sV;
+      if (lane == 0) {
+        int c1, c2;
+        kv_coords(it, c1, c2);
+        uint64_t* tb = tail ? &bars[kBufAux0 + bi] : &bars[kBufFull0 + bi];
+        mbar_arrive_expect_tx(tb, S::kTileBytes);
+        const uint64_t pol = l2_policy_evict_first();  // K/V: read once per item
+        for (int pn = 0; pn < kPanels; ++pn)
+          tma_load_3d_hint(dst + pn * kPanel, tm, tb, pn * 64, c1, c2, pol);
+      }
+      last_buf_par[bi] = ic & 1;
+      pending_buf[bi] = tail ? 0 : 1;
+      pending_buf_aux[bi] = tail ? 1 : 0;
+      if (tail) {
+        if (!mbar_wait(&bars[kBufAux0 + bi], buf_aux_cnt[bi] & 1, abort_flag)) {
+          record_error(p.header, kErrWaitKV);
+          return false;
+        }
+        buf_aux_cnt[bi]++;
+        pending_buf_aux[bi] = 0;
+        zero_rows(dst, kPanels, t_valid, lane);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBufFull0 + bi]);
+      }
+      return true;
+    };
     while (ok) {
-      const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
+      const int4 raw = next;
+      const int slot = fc & 1;
+      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((fc >> 1) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitItem);
         break;
       }
       if (lane == 0) {
-        const int idx = atomicAdd(&p.header[kHdrWorkCounter], 1);
-        int4 it = make_int4(-1, 0, 0, -1);
-        if (idx < p.header[kHdrNumItems]) it = p.items[idx];
-        item_slot[slot] = it;
+        item_slot[slot] = raw;
         mbar_arrive(&bars[kItemFull0 + slot]);
       }
-      __syncwarp();
-      const int4 raw = item_slot[slot];
+      ++fc;
       if (raw.x < 0) break;
+      next = claim_item(p, lane);
       const ItemInfo ii = decode_item(p, raw);
-      if (ii.e0 >= ii.e1) { ++itc; continue; }
+      if (ii.e0 >= ii.e1) continue;
       const int Lq = p.lq[ii.b], Lk = p.lk[ii.b];
       const int t_valid = Lk - ii.jt * 128;
-      if (!mbar_wait(&bars[kKvEmpty], (itc & 1) ^ 1, abort_flag)) {
-        record_error(p.header, kErrWaitKV);
-        break;
-      }
-      pending_kv = 1;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[kKvTma], 2u * S::kTileBytes);
-        const int c1 = p.layout == kLayoutBNSD ? ii.jt * 128 : ii.g;
-        const int c2 = p.layout == kLayoutBNSD ? ii.b * p.N2 + ii.g : p.cu_k[ii.b] + ii.jt * 128;
-        const uint64_t pol = l2_policy_evict_first();  // K/V: read once per item
-        for (int pn = 0; pn < kPanels; ++pn) {
-          tma_load_3d_hint(sK + pn * kPanel, &tm_k, &bars[kKvTma], pn * 64, c1, c2, pol);
-          tma_load_3d_hint(sV + pn * kPanel, &tm_v, &bars[kKvTma], pn * 64, c1, c2, pol);
-        }
-      }
+      const int kb = ic & 1;
       for (int e = ii.e0; e < ii.e1 && ok; ++e) {
+        if (e == ii.e0 && next.x >= 0 && lane == 0) {
+          // the next item's K/V into L2, one item before they are loaded
+          const ItemInfo nx = decode_item(p, next);
+          if (nx.e0 < nx.e1) {
+            int c1, c2;
+            kv_coords(nx, c1, c2);
+            for (int pn = 0; pn < kPanels; ++pn) {
+              tma_prefetch_l2_3d(&tm_k, pn * 64, c1, c2);
+              tma_prefetch_l2_3d(&tm_v, pn * 64, c1, c2);
+            }
+          }
+        }
         const int32_t ent = p.entries[e];
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
@@ -312,6 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars[kQFull0 + st]);
           if (tail) mbar_arrive(&bars[kQFull0 + st]);
         }
+        // K of the item: its buffer is free once the previous item's last dP
+        // (which read V from it) completed
+        if (e == ii.e0 && !load_buf(kb, &tm_k, ii, t_valid)) {
+          ok = false;
+          break;
+        }
         // dO (single buffer): free once the previous tile's dV MMA completed
         if (!mbar_wait(&bars[kDoEmpty], (n & 1) ^ 1, abort_flag)) {
           record_error(p.header, kErrWaitQ);
@@ -339,139 +429,187 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kDoFull]);
         }
-        if (e == ii.e0) {
-          // K/V of this item: wait for the copy, clear rows past the key length
-          if (!mbar_wait(&bars[kKvTma], itc & 1, abort_flag)) {
-            record_error(p.header, kErrWaitKV);
-            ok = false;
-            break;
-          }
-          pending_kv = 0;
-          if (t_valid < 128) {
-            zero_rows(sK, kPanels, t_valid, lane);
-            zero_rows(sV, kPanels, t_valid, lane);
-            fence_async_smem();
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kKvFull]);
+        // V of the item: its buffer held the previous item's K (last read by
+        // the final dQ MMA)
+        if (e == ii.e0 && !load_buf(kb ^ 1, &tm_v, ii, t_valid)) {
+          ok = false;
+          break;
         }
         ++n;
       }
-      ++itc;
+      ++ic;
     }
     if (*abort_flag) {
       // let copies still in flight land before the CTA exits
       for (int st = 0; st < 2; ++st) {
         if (pending_q[st]) mbar_wait_drain(&bars[kQFull0 + st], last_q_par[st]);
         if (pending_q_aux[st]) mbar_wait_drain(&bars[kQAux0 + st], aux_cnt[st] & 1);
+        if (pending_buf[st]) mbar_wait_drain(&bars[kBufFull0 + st], last_buf_par[st]);
+        if (pending_buf_aux[st]) mbar_wait_drain(&bars[kBufAux0 + st], buf_aux_cnt[st] & 1);
       }
       if (pending_do) mbar_wait_drain(&bars[kDoFull], last_do_par);
       if (pending_do_aux) mbar_wait_drain(&bars[kDoAux], do_aux_cnt & 1);
-      if (pending_kv) mbar_wait_drain(&bars[kKvTma], (itc & 1));
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    uint32_t n = 0, itc = 0;
-    const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), adS = smem_u32(sdS);
+    uint32_t n = 0, fc = 0, ic = 0;  // tiles, ring slots read, non-empty items
+    const uint32_t aBuf0 = smem_u32(sK), aBuf1 = smem_u32(sV);
+    const uint32_t adS = smem_u32(sdS), adO = smem_u32(sdO);
     int where = 0;
-    while (true) {
-      const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
-      const int4 raw = item_slot[slot];
+    // next non-empty item from the ring (its entry range [e0, e1)): 1 item,
+    // 0 end of work, -1 wait failed
+    auto fetch = [&](int& e0, int& e1) -> int {
+      while (true) {
+        const int slot = fc & 1;
+        if (!mbar_wait(&bars[kItemFull0 + slot], (fc >> 1) & 1, abort_flag)) return -1;
+        const int4 raw = item_slot[slot];
+        __syncwarp();
+        if (elect_one()) mbar_arrive(&bars[kItemEmpty0 + slot]);
+        ++fc;
+        if (raw.x < 0) return 0;
+        e0 = raw.y;
+        e1 = raw.z;
+        if (e0 < e1) return 1;
+      }
+    };
+    // S^T(m) = K Q(m)^T into the S columns
+    auto issue_s = [&](uint32_t m, uint32_t aK) {
+      const uint32_t aQ = smem_u32(sQ0 + (m & 1) * S::kTileBytes);
+      if (elect_one()) {
+        const uint64_t dA = sdesc_sw128(aK, 16, 1024), dB = sdesc_sw128(aQ, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          mma_ss(tmem + kColS, dA + kmaj_step(k), dB + kmaj_step(k), kIdS, k > 0);
+        }
+        tc_commit(&bars[kSFull]);
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
-      if (raw.x < 0) break;
-      const ItemInfo ii = decode_item(p, raw);
-      if (ii.e0 >= ii.e1) { ++itc; continue; }
-      // test of the bounded waits: a barrier no one arrives at runs out, the CTA
-      // unwinds and the host reads the error code
-      if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) { where = kErrWaitTest; break; }
-      if (!mbar_wait(&bars[kKvFull], itc & 1, abort_flag)) { where = kErrWaitKV; break; }
-      tc_fence_after();
+    };
+    int ce0 = 0, ce1 = 0;
+    int have = fetch(ce0, ce1);
+    if (have < 0) where = kErrWaitItem;
+    if (have > 0) {  // S of the very first tile
+      // test of the bounded waits: a barrier no one arrives at runs out, the
+      // CTA unwinds and the host reads the error code
+      if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) where = kErrWaitTest;
+      else if (!mbar_wait(&bars[kBufFull0], 0, abort_flag)) where = kErrWaitKV;
+      else if (!mbar_wait(&bars[kQFull0], 0, abort_flag)) where = kErrWaitQ;
+      else {
+        tc_fence_after();
+        issue_s(0, aBuf0);
+      }
+    }
+    while (have > 0 && !where) {
+      const int kb = ic & 1, vb = kb ^ 1;
+      const uint32_t aK = kb ? aBuf1 : aBuf0, aV = kb ? aBuf0 : aBuf1;
+      int ne0 = 0, ne1 = 0;
+      int have_next = 0;
       bool first = true;
-      for (int e = ii.e0; e < ii.e1; ++e) {
+      for (int e = ce0; e < ce1; ++e) {
+        const bool last = e + 1 == ce1;
         const int st = n & 1;
         const uint32_t aQ = smem_u32(sQ0 + st * S::kTileBytes);
-        const uint32_t adO = smem_u32(sdO);
-        if (!mbar_wait(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
-        tc_fence_after();
-        if (lane == 0) {  // S^T = K Q^T
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-            mma_ss(tmem + kColS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024),
-                   kIdS, k > 0);
-          }
-          tc_commit(&bars[kSFull]);
-        }
-        __syncwarp();
+        // dP^T = V dO^T: the dP columns hold dQ of the previous tile until
+        // the drain warps have read it
         if (!mbar_wait(&bars[kDqEmpty], (n & 1) ^ 1, abort_flag)) { where = kErrWaitDQ; break; }
+        if (first && !mbar_wait(&bars[kBufFull0 + vb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
         if (!mbar_wait(&bars[kDoFull], n & 1, abort_flag)) { where = kErrWaitQ; break; }
         tc_fence_after();
-        if (lane == 0) {  // dP^T = V dO^T
+        if (elect_one()) {  // dP^T = V dO^T
+          const uint64_t dV = sdesc_sw128(aV, 16, 1024), dO = sdesc_sw128(adO, 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kPanel + (k & 3) * 32;
-            mma_ss(tmem + kColP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(adO + off, 16, 1024),
-                   kIdS, k > 0);
+            mma_ss(tmem + kColP, dV + kmaj_step(k), dO + kmaj_step(k), kIdS, k > 0);
           }
           tc_commit(&bars[kDpFull]);
+          if (last) tc_commit(&bars[kBufEmpty0 + vb]);  // V read for the last time
         }
         __syncwarp();
         if (!mbar_wait(&bars[kPReady], n & 1, abort_flag)) { where = kErrWaitP; break; }
         // the first dV/dK MMAs of an item overwrite the accumulators: the drain
         // warps must have read the previous item's dK/dV
-        if (first && !mbar_wait(&bars[kAccEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        if (first && !mbar_wait(&bars[kAccEmpty], (ic & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
         tc_fence_after();
-        if (lane == 0) {  // dV^T += P^T dO  (A = P^T in TMEM, packed)
+        if (elect_one()) {  // dV^T += P^T dO  (A = P^T in TMEM, packed)
+          const uint64_t dOmn = sdesc_sw128(adO, kPanel, 1024);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t acol = kColS + 64 * (k >> 2) + 8 * (k & 3);
-            mma_ts(tmem + kColDV, tmem + acol, sdesc_sw128(adO + k * 2048, kPanel, 1024), kIdKV,
-                   (first && k == 0) ? 0u : 1u);
+            mma_ts(tmem + kColDV, tmem + acol, dOmn + mn_step(k), kIdKV, (first && k == 0) ? 0u : 1u);
           }
           tc_commit(&bars[kDoEmpty]);  // dO may be reloaded once dP and dV completed
+          tc_commit(&bars[kDvDone]);
         }
         __syncwarp();
+        // S of the next tile once dV has read P^T out of the S columns. After
+        // the item's last tile the next item's K (in this item's V buffer) is
+        // used only if it has already landed; otherwise its S follows dQ/dK.
+        bool s_pending = false;
+        if (last) {
+          have_next = fetch(ne0, ne1);
+          if (have_next < 0) { where = kErrWaitItem; break; }
+          if (have_next > 0) {
+            if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) { where = kErrWaitTest; break; }
+            s_pending = true;
+          }
+        }
+        if (!last || s_pending) {
+          if (!mbar_wait(&bars[kDvDone], n & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        }
+        if (!last || (s_pending && mbar_test(&bars[kBufFull0 + vb], (ic + 1) & 1))) {
+          if (!mbar_wait(&bars[kQFull0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1, abort_flag)) {
+            where = kErrWaitQ;
+            break;
+          }
+          tc_fence_after();
+          issue_s(n + 1, last ? aV : aK);
+          s_pending = false;
+        }
         if (!mbar_wait(&bars[kDsReady], n & 1, abort_flag)) { where = kErrWaitDS; break; }
         tc_fence_after();
-        if (lane == 0) {  // dK^T += dS^T Q  (A = dS^T in TMEM, packed)
+        if (elect_one()) {
+          // dQ = dS K  (A = dS, MN-major; B = K, MN-major) into the dP columns,
+          // which the softmax warps have read before they signalled dS
+          const uint64_t dSmn = sdesc_sw128(adS, kPanel, 1024), dKmn = sdesc_sw128(aK, kPanel, 1024);
+          const uint64_t dSk = sdesc_sw128(adS, 16, 1024), dQmn = sdesc_sw128(aQ, kPanel, 1024);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t acol = kColP + 64 * (k >> 2) + 8 * (k & 3);
-            mma_ts(tmem + kColDK, tmem + acol, sdesc_sw128(aQ + k * 2048, kPanel, 1024), kIdKV,
-                   (first && k == 0) ? 0u : 1u);
-          }
-          tc_commit(&bars[kDkDone]);
-          tc_commit(&bars[kQEmpty0 + st]);
-        }
-        __syncwarp();
-        // dQ reuses the dS^T columns: wait until the dK MMAs have read them
-        if (!mbar_wait(&bars[kDkDone], n & 1, abort_flag)) { where = kErrWaitMisc; break; }
-        tc_fence_after();
-        if (lane == 0) {  // dQ = dS K  (A = dS from smem, MN-major; B = K, MN-major)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            mma_ss(tmem + kColP, sdesc_sw128(adS + k * 2048, kPanel, 1024),
-                   sdesc_sw128(aK + k * 2048, kPanel, 1024), kIdQ, k > 0);
+            mma_ss(tmem + kColP, dSmn + mn_step(k), dKmn + mn_step(k), kIdQ, k > 0);
           }
           tc_commit(&bars[kDqFull]);
+          if (last) tc_commit(&bars[kBufEmpty0 + kb]);  // K read for the last time
+          // dK^T += dS^T Q  (A = dS^T, K-major: the same shared-memory tile)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            mma_ss(tmem + kColDK, dSk + kmaj_step(k), dQmn + mn_step(k), kIdKV,
+                   (first && k == 0) ? 0u : 1u);
+          }
+          tc_commit(&bars[kQEmpty0 + st]);
+          tc_commit(&bars[kDsFree]);
+          if (last) tc_commit(&bars[kAccFull]);
         }
         __syncwarp();
+        if (s_pending) {  // the next item's first S, now that its K has landed
+          if (!mbar_wait(&bars[kBufFull0 + vb], (ic + 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+          if (!mbar_wait(&bars[kQFull0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1, abort_flag)) {
+            where = kErrWaitQ;
+            break;
+          }
+          tc_fence_after();
+          issue_s(n + 1, aV);
+        }
         first = false;
         ++n;
       }
       if (where) break;
-      if (lane == 0) {
-        tc_commit(&bars[kAccFull]);
-        tc_commit(&bars[kKvEmpty]);
-      }
-      __syncwarp();
-      ++itc;
+      ++ic;
+      ce0 = ne0;
+      ce1 = ne1;
+      have = have_next;
     }
     if (where) record_error(p.header, where);
     if (*abort_flag) {  // wait for MMAs still in flight before TMEM is freed
-      if (lane == 0) tc_commit(&bars[kDrainBar]);
+      if (elect_one()) tc_commit(&bars[kDrainBar]);
       __syncwarp();
       mbar_wait_drain(&bars[kDrainBar], 0);
     }
@@ -562,9 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[2 * j4] = E::pack(ds[0], ds[1]);
             pk[2 * j4 + 1] = E::pack(ds[2], ds[3]);
           }
-          tmem_st16(tmem + lane_off + kColP + 64 * wg + 16 * c, pk);
-          // dS (M = query s, K = key t) for the dQ MMA: panel wg, row t,
-          // 16-byte chunk cc holds s = 64 wg + 8 cc .. +7, swizzled by t & 7.
+          // dS into shared memory: panel wg, row t, 16-byte chunk cc holds
+          // s = 64 wg + 8 cc .. +7, swizzled by t & 7 -- the MN-major A
+          // operand (M = query s) of the dQ MMA and the K-major A operand
+          // (M = key t) of the dK MMA.
           uint8_t* rowp = sdS + wg * kPanel + t * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -588,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qd = warp & 3;
     const int r = qd * 32 + lane;  // TMEM lane: query row (dQ) / key row (dK, dV)
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    uint32_t n = 0, itc = 0;
+    uint32_t n = 0, itc = 0, ic = 0;  // tiles, ring slots read, non-empty items
     int where = 0;
     while (true) {
       const int slot = itc & 1;
@@ -599,68 +738,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (raw.x < 0) break;
       const ItemInfo ii = decode_item(p, raw);
       if (ii.e0 >= ii.e1) { ++itc; continue; }
-      const int Lq = p.lq[ii.b], Lk = p.lk[ii.b];
+      const int Lk = p.lk[ii.b];
       for (int e = ii.e0; e < ii.e1; ++e) {
         const int32_t ent = p.entries[e];
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
         if (!mbar_wait(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
         tc_fence_after();
-        // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp copies its
-        // 32 rows from TMEM into 32x32 fp32 boxes (128-byte swizzled): columns
-        // [0, 64) into the dS buffer and [64, 128) into the staging buffer
-        // when D = 128 (D = 64: staging buffer only), releases TMEM for the
-        // next dP, and issues the reduce-adds as two bulk groups. The dS half
-        // must be read before the softmax warps write the next dS (ds_free);
-        // the staging half is waited for before this warp stages again. Rows
-        // past the query length carry exact zeros (dS = 0 there) and land in
-        // the padded part of the accumulator.
+        // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp owns 32
+        // rows and an 8 KB part of the staging buffer: two 32 x 32 fp32 boxes
+        // (128-byte swizzled), i.e. 64 columns at a time. With D = 128 the
+        // columns [64, 128) wait in registers while the first boxes are read,
+        // so the TMEM columns go back to the next dP at once. Rows past the
+        // query length carry exact zeros (dS = 0 there) and land in the padded
+        // part of the accumulator.
         const int grow = h * p.Rq + p.qrow[ii.b] + it * 128 + qd * 32;
-        uint8_t* boxes_ds = sdS + qd * 8192;
-        uint8_t* boxes_stg = sStg + qd * 8192;
-        if (lane == 0) bulk_wait_read_all();  // previous tile's staging boxes were read
+        uint8_t* boxes = sStg + qd * 8192;
+        uint8_t* rowp = boxes + lane * 128;
+        if (lane == 0) bulk_wait_read_all();  // the previous tile's boxes were read
         __syncwarp();
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf) {
-          uint8_t* boxes = (D == 128 && hf == 0) ? boxes_ds : boxes_stg;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lane_off + kColP + 32 * c, x);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_off + kColP + 64 * hf + 32 * c, x);
-            uint8_t* rowp = boxes + c * 4096 + lane * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
-                  make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-          }
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(rowp + c * 4096 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        }
+        uint32_t hold[2][32];
+        if constexpr (D == 128) {
+          tmem_ld32(tmem + lane_off + kColP + 64, hold[0]);
+          tmem_ld32(tmem + lane_off + kColP + 96, hold[1]);
         }
         tc_fence_before();
         fence_async_smem();
         __syncwarp();
+        const uint64_t pol = l2_policy_evict_last();  // keep dQ accumulator rows in L2
         if (lane == 0) {
           mbar_arrive(&bars[kDqEmpty]);  // TMEM columns free for the next dP
-          const uint64_t pol = l2_policy_evict_last();  // keep dQ accumulator rows in L2
-          if (D == 128) {
-            tma_reduce_add_2d_hint(&tm_acc, boxes_ds, 0, grow, pol);
-            tma_reduce_add_2d_hint(&tm_acc, boxes_ds + 4096, 32, grow, pol);
-            bulk_commit_group();
-            tma_reduce_add_2d_hint(&tm_acc, boxes_stg, 64, grow, pol);
-            tma_reduce_add_2d_hint(&tm_acc, boxes_stg + 4096, 96, grow, pol);
-            bulk_commit_group();
-            bulk_wait_read_1();                 // the dS-buffer group has been read
-          } else {
-            tma_reduce_add_2d_hint(&tm_acc, boxes_stg, 0, grow, pol);
-            tma_reduce_add_2d_hint(&tm_acc, boxes_stg + 4096, 32, grow, pol);
+          tma_reduce_add_2d_hint(&tm_acc, boxes, 0, grow, pol);
+          tma_reduce_add_2d_hint(&tm_acc, boxes + 4096, 32, grow, pol);
+          bulk_commit_group();
+        }
+        if constexpr (D == 128) {
+          if (lane == 0) bulk_wait_read_all();  // the first boxes were read
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(rowp + c * 4096 + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(hold[c][4 * j], hold[c][4 * j + 1], hold[c][4 * j + 2],
+                             hold[c][4 * j + 3]);
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d_hint(&tm_acc, boxes, 64, grow, pol);
+            tma_reduce_add_2d_hint(&tm_acc, boxes + 4096, 96, grow, pol);
             bulk_commit_group();
           }
-          mbar_arrive(&bars[kDsFree]);
         }
         __syncwarp();
         ++n;
       }
       if (where) break;
       // dK / dV of the key tile
-      if (!mbar_wait(&bars[kAccFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
+      if (!mbar_wait(&bars[kAccFull], ic & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const int trow = ii.jt * 128 + r;
       const bool row_ok = (p.layout == kLayoutBNSD) ? (trow < p.Skv) : (trow < Lk);
@@ -678,42 +823,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         sdv = p.dv_st[2];
       }
       float* slot_base = ii.slot >= 0 ? p.slots + (int64_t)ii.slot * 2 * 128 * D : nullptr;
+      // Whole tiles go out through the staging buffer as TMA stores: each warp
+      // packs its 32 rows into 32 x 64 boxes (128-byte swizzled) and stores
+      // them; a TND tile that ends inside the sequence, split columns (fp32
+      // slots) and outputs without a store view take the per-row path.
+      const bool tma_out = p.dkv_tma && slot_base == nullptr &&
+                           (p.layout == kLayoutBNSD || ii.jt * 128 + 128 <= Lk);
+      if (tma_out) {
+        uint8_t* boxes = sStg + qd * 8192;
+        const int trow0 = ii.jt * 128 + qd * 32;
+        if (lane == 0) bulk_wait_read_all();  // dQ boxes of the last tile were read
+        __syncwarp();
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? kColDK : kColDV;
-        const float mul = which == 0 ? p.scale : 1.f;
-        T* out = static_cast<T*>(which == 0 ? p.dk : p.dv) + (which == 0 ? ok_off : ov_off);
-        const int64_t sd = which == 0 ? sdk : sdv;
+        for (int which = 0; which < 2; ++which) {
+          if (D == 128 && which == 1) {  // the dK boxes must be read before dV reuses them
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+          const uint32_t col = which == 0 ? kColDK : kColDV;
+          const float mul = which == 0 ? p.scale : 1.f;
+          uint8_t* wb = (D == 64) ? boxes + which * 4096 : boxes;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + col + 32 * c, x);
-          if (slot_base != nullptr) {
-            if (r < Lk - ii.jt * 128) {
-              float4* d4 = reinterpret_cast<float4*>(slot_base + (which * 128 + r) * D + 32 * c);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_off + col + 32 * c, x);
+            uint8_t* rowp = wb + (c >> 1) * 4096 + lane * 128;
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                atomicAdd(d4 + j, make_float4(__uint_as_float(x[4 * j]) * mul,
-                                              __uint_as_float(x[4 * j + 1]) * mul,
-                                              __uint_as_float(x[4 * j + 2]) * mul,
-                                              __uint_as_float(x[4 * j + 3]) * mul));
+            for (int q = 0; q < 4; ++q) {
+              uint4 u;
+              u.x = E::pack(__uint_as_float(x[8 * q]) * mul, __uint_as_float(x[8 * q + 1]) * mul);
+              u.y = E::pack(__uint_as_float(x[8 * q + 2]) * mul, __uint_as_float(x[8 * q + 3]) * mul);
+              u.z = E::pack(__uint_as_float(x[8 * q + 4]) * mul, __uint_as_float(x[8 * q + 5]) * mul);
+              u.w = E::pack(__uint_as_float(x[8 * q + 6]) * mul, __uint_as_float(x[8 * q + 7]) * mul);
+              *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + q) ^ (lane & 7)) << 4)) = u;
             }
-          } else if (row_ok) {
-            if (p.dkv_vec) {
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const CUtensorMap* tm = which == 0 ? &tm_dk : &tm_dv;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint4 u;
-                u.x = E::pack(__uint_as_float(x[8 * j]) * mul, __uint_as_float(x[8 * j + 1]) * mul);
-                u.y = E::pack(__uint_as_float(x[8 * j + 2]) * mul, __uint_as_float(x[8 * j + 3]) * mul);
-                u.z = E::pack(__uint_as_float(x[8 * j + 4]) * mul, __uint_as_float(x[8 * j + 5]) * mul);
-                u.w = E::pack(__uint_as_float(x[8 * j + 6]) * mul, __uint_as_float(x[8 * j + 7]) * mul);
-                *reinterpret_cast<uint4*>(out + 32 * c + 8 * j) = u;
+            for (int bx = 0; bx < D / 64; ++bx) {
+              if (p.layout == kLayoutBNSD)
+                tma_store_4d(tm, wb + bx * 4096, bx * 64, trow0, ii.g, ii.b);
+              else
+                tma_store_3d(tm, wb + bx * 4096, bx * 64, ii.g, p.cu_k[ii.b] + trow0);
+            }
+            bulk_commit_group();
+          }
+        }
+      } else {  // rare: kept compact (not unrolled)
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = which == 0 ? kColDK : kColDV;
+          const float mul = which == 0 ? p.scale : 1.f;
+          T* out = static_cast<T*>(which == 0 ? p.dk : p.dv) + (which == 0 ? ok_off : ov_off);
+          const int64_t sd = which == 0 ? sdk : sdv;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_off + col + 32 * c, x);
+            if (slot_base != nullptr) {
+              if (r < Lk - ii.jt * 128) {
+                float4* d4 = reinterpret_cast<float4*>(slot_base + (which * 128 + r) * D + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  atomicAdd(d4 + j, make_float4(__uint_as_float(x[4 * j]) * mul,
+                                                __uint_as_float(x[4 * j + 1]) * mul,
+                                                __uint_as_float(x[4 * j + 2]) * mul,
+                                                __uint_as_float(x[4 * j + 3]) * mul));
               }
-            } else {
+            } else if (row_ok) {
+              if (p.dkv_vec) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const uint32_t pk = E::pack(__uint_as_float(x[j]) * mul, 0.f);
-                out[(32 * c + j) * sd] = *reinterpret_cast<const T*>(&pk);
+                for (int j = 0; j < 4; ++j) {
+                  uint4 u;
+                  u.x = E::pack(__uint_as_float(x[8 * j]) * mul, __uint_as_float(x[8 * j + 1]) * mul);
+                  u.y = E::pack(__uint_as_float(x[8 * j + 2]) * mul, __uint_as_float(x[8 * j + 3]) * mul);
+                  u.z = E::pack(__uint_as_float(x[8 * j + 4]) * mul, __uint_as_float(x[8 * j + 5]) * mul);
+                  u.w = E::pack(__uint_as_float(x[8 * j + 6]) * mul, __uint_as_float(x[8 * j + 7]) * mul);
+                  *reinterpret_cast<uint4*>(out + 32 * c + 8 * j) = u;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const uint32_t pk = E::pack(__uint_as_float(x[j]) * mul, 0.f);
+                  out[(32 * c + j) * sd] = *reinterpret_cast<const T*>(&pk);
+                }
               }
             }
           }
@@ -723,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kAccEmpty]);
       ++itc;
+      ++ic;
     }
     if (where) record_error(p.header, where);
     if (lane == 0) bulk_wait_all();
@@ -745,7 +942,7 @@ cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
   int grid = p.num_sms;
   if (p.max_items < grid) grid = p.max_items;
   if (grid < 1) grid = 1;
-  k_bwd<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, p);
+  k_bwd<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, m.dk, m.dv, p);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,7 @@ struct Plan {
   int64_t mask_sb, mask_sh, mask_si;    // mask strides (b, h, i); j stride 1
   int64_t dq_st[4], dk_st[4], dv_st[4]; // output strides (elements), layout order
   int dq_vec, dkv_vec;                  // outputs allow 16-byte row stores
+  int dkv_tma;                          // dK / dV written by TMA stores (BwdMaps dk, dv)
   // per-batch info in the workspace (int32 [B] each)
   const int* lq;
   const int* lk;

@@ -44,6 +44,7 @@ cudaError_t launch_finalize(const Plan& p, cudaStream_t st);
 struct BwdMaps {
   CUtensorMap q, k, v, dout;
   CUtensorMap dqacc;  // fp32 [N1*Rq rows, D], box 32 x 32, 128-byte swizzle (reduce-add)
+  CUtensorMap dk, dv; // outputs, box 64 x 32 rows, 128-byte swizzle: BNSD (d, s, n, b), TND (d, n, t)
 };
 cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st);
 size_t bwd_smem_bytes(int D);
