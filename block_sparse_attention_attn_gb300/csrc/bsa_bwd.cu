@@ -151,6 +151,17 @@ __device__ __forceinline__ ItemInfo decode_item(const Plan& p, int4 it) {
   return r;
 }
 
+// S^T = K Q^T for one tile (K-major K and Q tiles), then a commit to `bar`.
+// Kept out of line: it is issued from three places in the MMA warp.
+template <int D>
+__device__ __noinline__ void mma_s_tile(uint32_t d_tmem, uint32_t aK, uint32_t aQ, uint32_t idesc,
+                                        uint64_t* bar) {
+  const uint64_t dA = sdesc_sw128(aK, 16, 1024), dB = sdesc_sw128(aQ, 16, 1024);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) mma_ss(d_tmem, dA + kmaj_step(k), dB + kmaj_step(k), idesc, k > 0);
+  tc_commit(bar);
+}
+
 // Claims the next work item from the device queue (lane 0) and hands it to
 // every lane of the warp; x = -1 marks the end of the work.
 __device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
@@ -396,11 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars[kQFull0 + st]);
           if (tail) mbar_arrive(&bars[kQFull0 + st]);
         }
-        // K of the item: its buffer is free once the previous item's last dP
-        // (which read V from it) completed
-        if (e == ii.e0 && !load_buf(kb, &tm_k, ii, t_valid)) {
-          ok = false;
-          break;
+        // K and V of the item: K's buffer is free once the previous item's
+        // last dP (which read V from it) completed, V's once its last dQ did
+        if (e == ii.e0) {
+#pragma unroll 1
+          for (int w = 0; w < 2 && ok; ++w) ok = load_buf(kb ^ w, w == 0 ? &tm_k : &tm_v, ii, t_valid);
+          if (!ok) break;
         }
         // dO (single buffer): free once the previous tile's dV MMA completed
         if (!mbar_wait(&bars[kDoEmpty], (n & 1) ^ 1, abort_flag)) {
@@ -428,12 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kDoFull]);
-        }
-        // V of the item: its buffer held the previous item's K (last read by
-        // the final dQ MMA)
-        if (e == ii.e0 && !load_buf(kb ^ 1, &tm_v, ii, t_valid)) {
-          ok = false;
-          break;
         }
         ++n;
       }
@@ -474,15 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // S^T(m) = K Q(m)^T into the S columns
     auto issue_s = [&](uint32_t m, uint32_t aK) {
-      const uint32_t aQ = smem_u32(sQ0 + (m & 1) * S::kTileBytes);
-      if (elect_one()) {
-        const uint64_t dA = sdesc_sw128(aK, 16, 1024), dB = sdesc_sw128(aQ, 16, 1024);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          mma_ss(tmem + kColS, dA + kmaj_step(k), dB + kmaj_step(k), kIdS, k > 0);
-        }
-        tc_commit(&bars[kSFull]);
-      }
+      if (elect_one())
+        mma_s_tile<D>(tmem + kColS, aK, smem_u32(sQ0 + (m & 1) * S::kTileBytes), kIdS, &bars[kSFull]);
       __syncwarp();
     };
     int ce0 = 0, ce1 = 0;
@@ -630,16 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (raw.x < 0) break;
       const ItemInfo ii = decode_item(p, raw);
       if (ii.e0 >= ii.e1) { ++itc; continue; }
-      const int Lq = p.lq[ii.b], Lk = p.lk[ii.b];
+      const int Lk = p.lk[ii.b];
       const bool t_ok = (ii.jt * 128 + t) < Lk;
       for (int e = ii.e0; e < ii.e1; ++e) {
-        const int32_t ent = p.entries[e];
-        const int it = entry_it(ent);
-        const int sub = entry_sub(ent);
+        const int sub = entry_sub(p.entries[e]);
         const int s_sub = (p.rb == 2) ? wg : 0;
         const int t_sub = (p.cb == 2) ? (t >> 6) : 0;
-        const bool row_on = t_ok && ((sub >> (s_sub * 2 + t_sub)) & 1);
-        const int s_lim = Lq - it * 128;
+        // key row t of this thread takes part (inside the key length, in a
+        // selected sub-block); query columns past the query length need no
+        // test: their lse rows hold +inf, so P is exactly 0 there
+        const uint32_t rmask = (t_ok && ((sub >> (s_sub * 2 + t_sub)) & 1)) ? 0xFFFFFFFFu : 0u;
         const int st = n & 1;
         if (!mbar_wait(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
         if (!mbar_wait(&bars[kSFull], n & 1, abort_flag)) { where = kErrWaitS; break; }
@@ -654,20 +653,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t x[32];
           tmem_ld32(tmem + lane_off + kColS + 64 * wg + 32 * c, x);
           const int s0 = 64 * wg + 32 * c;
-          const bool full = row_on && (s_lim >= s0 + 32);
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const float4 l4 = reinterpret_cast<const float4*>(lse2 + s0)[j4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            float pv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int j = 4 * j4 + u;
-              pv[u] = ex2_approx(fmaf(__uint_as_float(x[j]), p.scale_log2, -lv[u]));
-              if (!full) pv[u] = (row_on && (s0 + j) < s_lim) ? pv[u] : 0.f;
-            }
-            Ppk[16 * c + 2 * j4] = E::pack(pv[0], pv[1]);
-            Ppk[16 * c + 2 * j4 + 1] = E::pack(pv[2], pv[3]);
+            const float p0 = ex2_approx(fmaf(__uint_as_float(x[4 * j4]), p.scale_log2, -l4.x));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 1]), p.scale_log2, -l4.y));
+            const float p2 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 2]), p.scale_log2, -l4.z));
+            const float p3 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 3]), p.scale_log2, -l4.w));
+            Ppk[16 * c + 2 * j4] = E::pack(p0, p1) & rmask;
+            Ppk[16 * c + 2 * j4 + 1] = E::pack(p2, p3) & rmask;
           }
           uint32_t pk[16];
 #pragma unroll
@@ -834,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int trow0 = ii.jt * 128 + qd * 32;
         if (lane == 0) bulk_wait_read_all();  // dQ boxes of the last tile were read
         __syncwarp();
-#pragma unroll
+#pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           if (D == 128 && which == 1) {  // the dK boxes must be read before dV reuses them
             if (lane == 0) bulk_wait_read_all();

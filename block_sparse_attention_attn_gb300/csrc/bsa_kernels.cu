@@ -298,7 +298,9 @@ __global__ void __launch_bounds__(256) k_preprocess(Plan p) {
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
   if (sub == 0) {
-    float l2 = 0.f;
+    // rows past the query length: +inf, so that P = exp2(x - lse2) is exactly
+    // zero in their columns of the backward
+    float l2 = __int_as_float(0x7f800000);
     if (valid) {
       int64_t li;
       if (p.layout == kLayoutBNSD)
