@@ -537,6 +537,24 @@ bsa_status bsa_grad_workspace_size(
   p.max_slots = std::min(p.NGC, 2 * num_sms + 1);
   p.max_items = p.NGC + 2 * num_sms + p.max_slots + 1;
   p.min_chunk = 16;
+  {
+    // Waves of consecutive (batch, kv head) groups whose dQ accumulator, Q and
+    // dO rows (8 bytes per element) fit in about half of L2: items run wave by
+    // wave, so the accumulator rows a reduce-add hits are still cached.
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) {
+      cudaGetLastError();
+      l2 = 64 << 20;
+    }
+    int64_t rows = 0;
+    for (int b = 0; b < g.B; ++b) rows += (int64_t)g.N1 * g.lq[b];
+    const int64_t bytes = rows * g.D * 8;
+    const int64_t budget = std::max<int64_t>((int64_t)l2 / 2, 1);
+    int64_t nw = (bytes + budget - 1) / budget;
+    nw = std::min<int64_t>(std::max<int64_t>(nw, 1), std::min(32, g.B * g.N2));
+    p.n_waves = (int)nw;
+  }
   // workspace layout
   uint64_t off = align256(kHdrWords * 4);
   ex->off_info = off; off = align256(off + ex->info.size() * 4);

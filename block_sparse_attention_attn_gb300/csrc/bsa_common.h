@@ -113,6 +113,7 @@ struct Plan {
   int max_items, max_slots, max_entries;
   int num_sms;
   int min_chunk;         // smallest split chunk
+  int n_waves;           // work items are ordered in this many waves of (b, kv head)
   int wait_test;         // test of the bounded waits: 1 = one wait on a barrier nothing completes
 };
 

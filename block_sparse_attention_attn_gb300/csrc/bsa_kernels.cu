@@ -163,10 +163,19 @@ __device__ __forceinline__ int chunk_begin(int n, int chunks, int c) {
 }
 
 __global__ void __launch_bounds__(1024) k_plan(Plan p) {
-  constexpr int kBuckets = 1024;  // item length bucket (lengths >= 1023 share one)
+  // Items are ordered by (wave, length descending): a wave is a run of
+  // consecutive (b, kv head) groups (p.n_waves of them, equal counts), and
+  // within a wave the longest items go first. Lengths >= kLenB - 1 share a
+  // bucket.
+  constexpr int kLenB = 256, kMaxWaves = 32, kKeys = kLenB * kMaxWaves;
   __shared__ int ws[32];
   __shared__ int s_L;
-  __shared__ int hist[kBuckets];
+  __shared__ int hist[kKeys];
+  const int nbg = p.NGC / p.Mk_t;
+  auto key_of = [&](int gc, int len) {
+    const int w = (int)((int64_t)(gc / p.Mk_t) * p.n_waves / nbg);
+    return w * kLenB + (kLenB - 1 - min(len, kLenB - 1));
+  };
   int carry = 0;
   for (int base = 0; base < p.NC; base += blockDim.x) {
     const int i = base + threadIdx.x;
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     if (L < p.min_chunk) L = p.min_chunk;
     s_L = L;
   }
-  hist[threadIdx.x] = 0;
+  for (int i = threadIdx.x; i < kKeys; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int L = s_L;
   // pass 1: split decision, slots, length histogram (descending buckets)
@@ -202,16 +211,18 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
       const int chunks = split ? (n + L - 1) / L : (n > 0 ? 1 : 0);
       for (int c = 0; c < chunks; ++c) {
         const int len = chunk_begin(n, chunks, c + 1) - chunk_begin(n, chunks, c);
-        atomicAdd(&hist[kBuckets - 1 - min(len, kBuckets - 1)], 1);
+        atomicAdd(&hist[key_of(gc, len)], 1);
       }
     }
   }
   __syncthreads();
-  int total_items;
-  {
-    const int v = hist[threadIdx.x];
-    const int ex = block_exclusive_scan(v, ws, &total_items);
-    hist[threadIdx.x] = ex;  // bucket start offsets
+  int total_items = 0;
+  for (int base = 0; base < kKeys; base += blockDim.x) {  // bucket start offsets
+    const int v = hist[base + threadIdx.x];
+    int tot;
+    const int ex = block_exclusive_scan(v, ws, &tot);
+    hist[base + threadIdx.x] = total_items + ex;
+    total_items += tot;
   }
   __syncthreads();
   // pass 2: place the items
@@ -225,7 +236,7 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     const int chunks = info >= 0 ? (n + L - 1) / L : 1;
     for (int c = 0; c < chunks; ++c) {
       const int b0 = chunk_begin(n, chunks, c), b1 = chunk_begin(n, chunks, c + 1);
-      const int pos = atomicAdd(&hist[kBuckets - 1 - min(b1 - b0, kBuckets - 1)], 1);
+      const int pos = atomicAdd(&hist[key_of(gc, b1 - b0)], 1);
       p.items[pos] = make_int4(gc, e0 + b0, e0 + b1, info >= 0 ? info : -1);
     }
   }
