@@ -348,7 +348,8 @@ struct bsa_executor {
   std::vector<int> info;  // per-batch arrays copied into the workspace
   int n_info_off[7] = {};  // offsets (ints) of lq, lk, cu_q, cu_k, qrow, krow, qtile_b
   uint64_t off_info = 0, off_lse2 = 0, off_dvec = 0, off_dqacc = 0, off_colcnt = 0,
-           off_colptr = 0, off_entries = 0, off_items = 0, off_colinfo = 0, off_slots = 0;
+           off_colptr = 0, off_entries = 0, off_items = 0, off_colinfo = 0, off_fin = 0,
+           off_slots = 0;
   uint64_t ws_size = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
   CUtensorMap map_dk{}, map_dv{};  // dK / dV store views (valid when plan.dkv_tma)
@@ -566,6 +567,7 @@ bsa_status bsa_grad_workspace_size(
   ex->off_entries = off; off = align256(off + (uint64_t)p.max_entries * 4);
   ex->off_items = off; off = align256(off + (uint64_t)p.max_items * 16);
   ex->off_colinfo = off; off = align256(off + (uint64_t)p.NGC * 4);
+  ex->off_fin = off; off = align256(off + (uint64_t)p.NGC * 4);
   ex->off_slots = off; off = align256(off + (uint64_t)p.max_slots * 2 * kTile * g.D * 4);
   ex->ws_size = off;
   *workspace_size = off;
@@ -601,6 +603,7 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   p.entries = reinterpret_cast<int32_t*>(ws + ex->off_entries);
   p.items = reinterpret_cast<int4*>(ws + ex->off_items);
   p.colinfo = reinterpret_cast<int*>(ws + ex->off_colinfo);
+  p.fin_tiles = reinterpret_cast<int*>(ws + ex->off_fin);
   p.slots = reinterpret_cast<float*>(ws + ex->off_slots);
 
   BwdMaps maps;

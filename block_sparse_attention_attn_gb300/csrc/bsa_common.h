@@ -29,6 +29,7 @@ enum HeaderWord {
   kHdrSlotsUsed = 4,   // split columns that got an fp32 partial slot
   kHdrChunkLen = 5,    // split threshold used
   kHdrErrorWhere = 6,  // code of the first wait that gave up
+  kHdrFinTiles = 7,    // key tiles the finalize kernel writes (unselected or split)
   kHdrErrorCounts = 16, // [16, 32): number of failed waits per code
   kHdrWords = 64
 };
@@ -107,6 +108,7 @@ struct Plan {
   int32_t* entries;      // [max_entries]
   int4* items;           // [max_items] {gcol, e_begin, e_end, slot}
   int* colinfo;          // [NGC] -1 empty, -2 single item, >=0 slot
+  int* fin_tiles;        // [NGC] key tiles (gc) with colinfo != -2, count in the header
   float* slots;          // [max_slots][2][128][D] fp32 dK, dV partials
   int NC;                // B*N2*Mk_t*G grouped columns
   int NGC;               // B*N2*Mk_t key tiles

@@ -195,8 +195,9 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
   for (int i = threadIdx.x; i < kKeys; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int L = s_L;
-  // pass 1: split decision, slots, length histogram (descending buckets)
-  int slot_carry = 0;
+  // pass 1: split decision, slots, length histogram (descending buckets), and
+  // the list of key tiles the finalize kernel writes (no entries, or split)
+  int slot_carry = 0, fin_carry = 0;
   for (int base = 0; base < p.NGC; base += blockDim.x) {
     const int gc = base + threadIdx.x;
     int n = 0;
@@ -205,8 +206,12 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     int tot;
     const int sidx = block_exclusive_scan(want, ws, &tot) + slot_carry;
     slot_carry += tot;
+    const int split = want && (sidx < p.max_slots);
+    const int fin = (gc < p.NGC) && (n == 0 || split);
+    const int fidx = block_exclusive_scan(fin, ws, &tot) + fin_carry;
+    fin_carry += tot;
+    if (fin) p.fin_tiles[fidx] = gc;
     if (gc < p.NGC) {
-      const int split = want && (sidx < p.max_slots);
       p.colinfo[gc] = (n == 0) ? -1 : (split ? sidx : -2);
       const int chunks = split ? (n + L - 1) / L : (n > 0 ? 1 : 0);
       for (int c = 0; c < chunks; ++c) {
@@ -244,6 +249,7 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     p.header[kHdrNumItems] = total_items;
     p.header[kHdrTotalTiles] = T;
     p.header[kHdrSlotsUsed] = min(slot_carry, p.max_slots);
+    p.header[kHdrFinTiles] = fin_carry;
     p.header[kHdrChunkLen] = L;
     p.header[kHdrWorkCounter] = 0;
     p.header[kHdrError] = 0;
@@ -252,17 +258,9 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
   }
 }
 
-// Zero the fp32 partial slots of split columns (one block per slot).
-__global__ void k_zero_slots(Plan p) {
-  const int slot = blockIdx.x;
-  if (slot >= p.header[kHdrSlotsUsed]) return;
-  float4* s = reinterpret_cast<float4*>(p.slots + (int64_t)slot * 2 * kTile * p.D);
-  const int n4 = 2 * kTile * p.D / 4;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
 // --------------------------------------------------------------------------
 // preprocess: D_s = sum_d dout_sd * out_sd, lse2_s = lse_s * log2(e); zero dQacc
+// and the fp32 slots of split columns
 // --------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float2 to_f2(uint32_t u);
@@ -279,6 +277,13 @@ __device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_preprocess(Plan p) {
+  {  // the fp32 partial slots of split columns start at zero
+    const int64_t n4 = (int64_t)p.header[kHdrSlotsUsed] * 2 * kTile * D / 4;
+    float4* sl = reinterpret_cast<float4*>(p.slots);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x)
+      sl[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   constexpr int TPR = D / 8;  // threads per row, 8 elements (16 B) each
   constexpr int RPB = 256 / TPR;
   const int sub = threadIdx.x % TPR;
@@ -384,7 +389,7 @@ __device__ __forceinline__ int batch_of_token(const int* cu, int B, int tok) {
 
 // dq[b,h,s,:] = scale * dQacc (0 on padding rows), any output strides.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) k_finalize_dq(Plan p) {
+__device__ __forceinline__ void finalize_dq_rows(const Plan& p) {
   constexpr int TPR = D / 8;
   constexpr int RPB = 256 / TPR;
   const int sub = threadIdx.x % TPR;
@@ -423,38 +428,34 @@ __global__ void __launch_bounds__(256) k_finalize_dq(Plan p) {
   }
 }
 
-// dk/dv rows of key tiles the backward kernel did not write: zeros for tiles
-// no query selects, the fp32 slot (dK already scaled) for split tiles.
+// dk/dv rows of the key tiles the backward kernel did not write (the list
+// fin_tiles from the planner): zeros for tiles no query selects, the fp32 slot
+// (dK already scaled) for split tiles.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) k_finalize_dkdv(Plan p) {
+__device__ __forceinline__ void finalize_dkdv_tiles(const Plan& p) {
   constexpr int TPR = D / 8;
   constexpr int RPB = 256 / TPR;
   const int sub = threadIdx.x % TPR;
-  const int64_t nrows = (p.layout == kLayoutBNSD) ? (int64_t)p.B * p.N2 * p.Skv
-                                                  : (int64_t)p.Tkv * p.N2;
+  const int64_t nrows = (int64_t)p.header[kHdrFinTiles] * kTile;
   for (int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; row < nrows;
        row += (int64_t)gridDim.x * RPB) {
-    int b, g, t;
+    const int gc = p.fin_tiles[row / kTile];
+    const int jt = gc % p.Mk_t;
+    const int bg = gc / p.Mk_t;
+    const int g = bg % p.N2, b = bg / p.N2;
+    const int t = jt * kTile + (int)(row % kTile);
     int64_t ok, ov;
     if (p.layout == kLayoutBNSD) {
-      t = (int)(row % p.Skv);
-      const int64_t bg = row / p.Skv;
-      g = (int)(bg % p.N2);
-      b = (int)(bg / p.N2);
+      if (t >= p.Skv) continue;
       ok = b * p.dk_st[0] + g * p.dk_st[1] + t * p.dk_st[2];
       ov = b * p.dv_st[0] + g * p.dv_st[1] + t * p.dv_st[2];
     } else {
-      g = (int)(row % p.N2);
-      const int tok = (int)(row / p.N2);
-      b = batch_of_token(p.cu_k, p.B, tok);
-      t = tok - p.cu_k[b];
+      if (t >= p.lk[b]) continue;
+      const int64_t tok = (int64_t)p.cu_k[b] + t;
       ok = tok * p.dk_st[0] + g * p.dk_st[1];
       ov = tok * p.dv_st[0] + g * p.dv_st[1];
     }
-    const int jt = t / kTile;
-    const int gc = (b * p.N2 + g) * p.Mk_t + jt;
     const int info = p.colinfo[gc];
-    if (info == -2) continue;
     float xk[8], xv[8];
     if (info >= 0 && t < p.lk[b]) {
       const float* sl = p.slots + (int64_t)info * 2 * kTile * D;
@@ -473,6 +474,12 @@ __global__ void __launch_bounds__(256) k_finalize_dkdv(Plan p) {
     store8<T>(p.dk, ok + sub * 8 * p.dk_st[li], p.dk_st[li], p.dkv_vec != 0, xk);
     store8<T>(p.dv, ov + sub * 8 * p.dv_st[li], p.dv_st[li], p.dkv_vec != 0, xv);
   }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_finalize(Plan p) {
+  finalize_dq_rows<T, D>(p);
+  finalize_dkdv_tiles<T, D>(p);
 }
 
 // --------------------------------------------------------------------------
@@ -501,7 +508,6 @@ cudaError_t launch_plan(const Plan& p, cudaStream_t st) {
   k_plan<<<1, 1024, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.max_slots > 0) k_zero_slots<<<p.max_slots, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -524,10 +530,7 @@ cudaError_t launch_preprocess(const Plan& p, cudaStream_t st) {
 template <typename T, int D>
 static cudaError_t launch_fin_t(const Plan& p, cudaStream_t st) {
   const int grid = p.num_sms * 8;
-  k_finalize_dq<T, D><<<grid, 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  k_finalize_dkdv<T, D><<<grid, 256, 0, st>>>(p);
+  k_finalize<T, D><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
