@@ -171,6 +171,22 @@ bool encode_out_map(CUtensorMap* m, const bsa_tensor* t, int layout) {
   return r == CUDA_SUCCESS;
 }
 
+// One non-blocking side stream per device (created once, never destroyed):
+// the backward's preprocess runs there, between events, while the mask
+// compaction and the planner run on the caller's stream.
+constexpr int kMaxSideDevices = 64;
+cudaStream_t side_stream(int dev) {
+  static cudaStream_t streams[kMaxSideDevices] = {};
+  static std::once_flag once[kMaxSideDevices];
+  if (dev < 0 || dev >= kMaxSideDevices) return nullptr;
+  std::call_once(once[dev], [dev] {
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess) streams[dev] = s;
+    else cudaGetLastError();
+  });
+  return streams[dev];
+}
+
 int query_num_sms(bsa_status* st) {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -352,6 +368,11 @@ struct bsa_executor {
            off_slots = 0;
   uint64_t ws_size = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;      // owned: side-stream preprocess
+  ~bsa_executor() {
+    if (ev_fork) cudaEventDestroy(ev_fork);
+    if (ev_join) cudaEventDestroy(ev_join);
+  }
   CUtensorMap map_dk{}, map_dv{};  // dK / dV store views (valid when plan.dkv_tma)
 };
 
@@ -570,6 +591,14 @@ bsa_status bsa_grad_workspace_size(
   ex->off_fin = off; off = align256(off + (uint64_t)p.NGC * 4);
   ex->off_slots = off; off = align256(off + (uint64_t)p.max_slots * 2 * kTile * g.D * 4);
   ex->ws_size = off;
+  // events of the side-stream preprocess (without them everything runs on
+  // the caller's stream)
+  if (cudaEventCreateWithFlags(&ex->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ex->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (ex->ev_fork) cudaEventDestroy(ex->ev_fork);
+    ex->ev_fork = ex->ev_join = nullptr;
+  }
   *workspace_size = off;
   *executor = ex;
   return ok();
@@ -632,14 +661,35 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.col_slots = p.Mk_t; ca.row_slots = p.Mq_t;
   ca.lq = p.lq; ca.lk = p.lk;
   ca.counts = p.colcnt; ca.ptr = p.colptr; ca.out = p.entries; ca.plain = 0;
-  const char* what = "column count";
+  ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
+  // The preprocess (bandwidth-bound) runs on a side stream while the mask
+  // compaction and the planner (latency-bound, one block) run on `st`.
+  cudaStream_t side = nullptr;
+  {
+    int dev = 0;
+    if (ex->ev_fork && cudaGetDevice(&dev) == cudaSuccess) side = side_stream(dev);
+    cudaGetLastError();
+  }
+  const char* what = "preprocess";
+  if (side) {
+    if ((e = cudaEventRecord(ex->ev_fork, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(side, ex->ev_fork, 0)) != cudaSuccess ||
+        (e = launch_preprocess(p, side)) != cudaSuccess ||
+        (e = cudaEventRecord(ex->ev_join, side)) != cudaSuccess)
+      goto launch_fail;
+  }
+  what = "column count";
   if ((e = launch_columns(ca, 0, st)) != cudaSuccess) goto launch_fail;
   what = "planner";
   if ((e = launch_plan(p, st)) != cudaSuccess) goto launch_fail;
   what = "column fill";
   if ((e = launch_columns(ca, 1, st)) != cudaSuccess) goto launch_fail;
   what = "preprocess";
-  if ((e = launch_preprocess(p, st)) != cudaSuccess) goto launch_fail;
+  if (side) {
+    if ((e = cudaStreamWaitEvent(st, ex->ev_join, 0)) != cudaSuccess) goto launch_fail;
+  } else if ((e = launch_preprocess(p, st)) != cudaSuccess) {
+    goto launch_fail;
+  }
   what = "backward";
   if (ex->ev_before && (e = cudaEventRecord(ex->ev_before, st)) != cudaSuccess) goto launch_fail;
   if ((e = launch_bwd(p, maps, st)) != cudaSuccess) goto launch_fail;

@@ -43,6 +43,13 @@ __device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int
 // One warp per column (b, g, jt, hl) with index ((b*N2+g)*col_slots + jt)*G + hl.
 // fill == 0: counts[col] = active tiles; fill == 1: writes the entries.
 __global__ void k_columns(CompactArgs a, int fill) {
+  if (fill && a.zero != nullptr) {  // e.g. the fp32 slots of split columns
+    const int64_t n4 = (int64_t)(*a.zero_count) * a.zero_per / 4;
+    float4* z = reinterpret_cast<float4*>(a.zero);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x)
+      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const int warps = blockDim.x >> 5;
   const int col = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -260,7 +267,6 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
 
 // --------------------------------------------------------------------------
 // preprocess: D_s = sum_d dout_sd * out_sd, lse2_s = lse_s * log2(e); zero dQacc
-// and the fp32 slots of split columns
 // --------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float2 to_f2(uint32_t u);
@@ -277,13 +283,6 @@ __device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_preprocess(Plan p) {
-  {  // the fp32 partial slots of split columns start at zero
-    const int64_t n4 = (int64_t)p.header[kHdrSlotsUsed] * 2 * kTile * D / 4;
-    float4* sl = reinterpret_cast<float4*>(p.slots);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-         i += (int64_t)gridDim.x * blockDim.x)
-      sl[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   constexpr int TPR = D / 8;  // threads per row, 8 elements (16 B) each
   constexpr int RPB = 256 / TPR;
   const int sub = threadIdx.x % TPR;
