@@ -33,7 +33,7 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAK = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 
 
-LAUNCHES_PER_STEP = 6  # kernels of one bsa_grad call
+LAUNCHES_PER_STEP = 7  # kernels of one bsa_grad call
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -299,8 +299,8 @@ def bench_ours(args, rank, world, local):
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        # per step: mask compaction (count, fill), planner, preprocess,
-        # backward, finalize
+        # per step: info upload, mask compaction (count, fill), planner,
+        # preprocess, backward, finalize
         "gpu_launches": LAUNCHES_PER_STEP * n,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),

@@ -649,8 +649,8 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   maps.dk = ex->map_dk;
   maps.dv = ex->map_dv;
 
-  cudaError_t e = cudaMemcpyAsync(ws + ex->off_info, ex->info.data(), ex->info.size() * 4,
-                                  cudaMemcpyHostToDevice, st);
+  cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
+                                reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "copy of sequence info: %s", cudaGetErrorString(e));
   CompactArgs ca{};
   ca.mask = p.mask; ca.sb = p.mask_sb; ca.sh = p.mask_sh; ca.si = p.mask_si;
@@ -890,8 +890,8 @@ bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* execu
       !encode_map(&maps.k, ex->k, g.dtype, g.layout, g.D, rows_k, heads_k) ||
       !encode_map(&maps.v, ex->v, g.dtype, g.layout, g.D, rows_k, heads_k))
     return fail(BSA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed");
-  cudaError_t e = cudaMemcpyAsync(ws + ex->off_info, ex->info.data(), ex->info.size() * 4,
-                                  cudaMemcpyHostToDevice, st);
+  cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
+                                reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, kHdrWords * 4, st);
   if (e == cudaSuccess && ex->ev_before) e = cudaEventRecord(ex->ev_before, st);
   if (e == cudaSuccess) e = launch_fwd(f, maps, st);

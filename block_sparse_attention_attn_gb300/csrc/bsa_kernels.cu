@@ -7,6 +7,8 @@
 //     and lse*log2(e), plus zeroing of the fp32 dQ accumulator;
 //   * the finalize kernels: fp32 dQ (and split-column dK/dV) -> output dtype,
 //     zeros for padding rows and for key tiles no query selects.
+#include <cstring>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
   // consecutive (b, kv head) groups (p.n_waves of them, equal counts), and
   // within a wave the longest items go first. Lengths >= kLenB - 1 share a
   // bucket.
-  constexpr int kLenB = 256, kMaxWaves = 32, kKeys = kLenB * kMaxWaves;
+  constexpr int kLenB = 64, kMaxWaves = 32, kKeys = kLenB * kMaxWaves;
   __shared__ int ws[32];
   __shared__ int s_L;
   __shared__ int hist[kKeys];
@@ -479,6 +481,33 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) k_finalize(Plan p) {
   finalize_dq_rows<T, D>(p);
   finalize_dkdv_tiles<T, D>(p);
+}
+
+// --------------------------------------------------------------------------
+// small host arrays into device memory through kernel parameters (no copy
+// from pageable memory, which would first synchronize the stream)
+// --------------------------------------------------------------------------
+template <int N>
+struct UploadBuf {
+  int v[N];
+};
+template <int N>
+__global__ void k_upload(UploadBuf<N> u, int n, int* dst) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = u.v[i];
+}
+template <int N>
+static cudaError_t upload_t(const int* host, int n, int* dst, cudaStream_t st) {
+  UploadBuf<N> u;
+  std::memcpy(u.v, host, sizeof(int) * n);
+  k_upload<N><<<1, 256, 0, st>>>(u, n, dst);
+  return cudaGetLastError();
+}
+cudaError_t launch_upload(const int* host, int n, int* dst, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (n <= 256) return upload_t<256>(host, n, dst, st);
+  if (n <= 2048) return upload_t<2048>(host, n, dst, st);
+  if (n <= 7680) return upload_t<7680>(host, n, dst, st);  // 30 KB of parameters
+  return cudaMemcpyAsync(dst, host, sizeof(int) * n, cudaMemcpyHostToDevice, st);
 }
 
 // --------------------------------------------------------------------------
