@@ -9,11 +9,12 @@
 //     dQ   = dS K                  -> fp32 accumulator in global memory (atomics)
 // with D = rowsum(dO o attentionOut) from the preprocess kernel.
 //
-// Design (one persistent CTA per SM, 448 threads, warp-specialised):
+// Design (one persistent CTA per SM, 480 threads, warp-specialised):
 //   warp 12     TMA producer: K/V tiles of the key tile (once per work item),
 //               then a 2-stage ring of Q tiles (with their lse/D rows) and
 //               one dO buffer.
-//   warp 13     tcgen05 MMA issuer (one thread) and TMEM owner (512 columns).
+//   warp 13     tcgen05 MMA issuer for dP, dV and S (one thread) and TMEM
+//               owner (512 columns); warp 14 issues dQ and dK.
 //   warps 0-7   "softmax" warpgroups: TMEM lane t = key row t; warpgroup w
 //               handles query columns [64w, 64w+64): P^T (into TMEM, packed, as
 //               the A operand of the dV MMA) and dS (into shared memory, the
@@ -43,9 +44,10 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int kMmaWarp = 13;   // dP, dV, S; TMEM owner
+constexpr int kMma2Warp = 14;  // dQ, dK
 constexpr int kDrainWarp0 = 8;
 constexpr int kPanel = 128 * 128;  // 128 rows x 128 bytes (64 x 16-bit), one swizzle span
 constexpr int kStages = 2;
@@ -66,7 +68,7 @@ enum Bar {
   kSFull, kDpFull, kPReady, kDsReady, kDvDone, kDqFull, kDqEmpty, kDsFree,
   kAccFull, kAccEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
-  kDrainBar, kNeverBar,
+  kDrainBar, kDrainBar2, kNeverBar,
   kNumBars
 };
 
@@ -232,13 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kDqFull], 1);
     mbar_init(&bars[kDqEmpty], 4);
     mbar_init(&bars[kDsFree], 1);  // dK MMA commit (the last reader of the dS tile)
-    mbar_init(&bars[kAccFull], 1);
+    mbar_init(&bars[kAccFull], 2);   // last dV (MMA warp) and last dK (second MMA warp)
     mbar_init(&bars[kAccEmpty], 4);
     mbar_init(&bars[kItemFull0], 1);
     mbar_init(&bars[kItemFull1], 1);
-    mbar_init(&bars[kItemEmpty0], 13);
-    mbar_init(&bars[kItemEmpty1], 13);
+    mbar_init(&bars[kItemEmpty0], 14);
+    mbar_init(&bars[kItemEmpty1], 14);
     mbar_init(&bars[kDrainBar], 1);
+    mbar_init(&bars[kDrainBar2], 1);
     mbar_init(&bars[kNeverBar], 1);  // nothing arrives here (wait_test)
     mbar_fence_init();
   }
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     uint32_t n = 0, fc = 0, ic = 0;  // tiles, ring slots read, non-empty items
     const uint32_t aBuf0 = smem_u32(sK), aBuf1 = smem_u32(sV);
-    const uint32_t adS = smem_u32(sdS), adO = smem_u32(sdO);
+    const uint32_t adO = smem_u32(sdO);
     int where = 0;
     // next non-empty item from the ring (its entry range [e0, e1)): 1 item,
     // 0 end of work, -1 wait failed
@@ -506,8 +509,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool first = true;
       for (int e = ce0; e < ce1; ++e) {
         const bool last = e + 1 == ce1;
-        const int st = n & 1;
-        const uint32_t aQ = smem_u32(sQ0 + st * S::kTileBytes);
         // dP^T = V dO^T: the dP columns hold dQ of the previous tile until
         // the drain warps have read it
         if (!mbar_wait(&bars[kDqEmpty], (n & 1) ^ 1, abort_flag)) { where = kErrWaitDQ; break; }
@@ -538,33 +539,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&bars[kDoEmpty]);  // dO may be reloaded once dP and dV completed
           tc_commit(&bars[kDvDone]);
+          if (last) tc_commit(&bars[kAccFull]);  // dV of the item complete
         }
         __syncwarp();
-        // S of the next tile once dV has read P^T out of the S columns. After
-        // the item's last tile the next item's K (in this item's V buffer) is
-        // used only if it has already landed; otherwise its S follows dQ/dK.
-        bool s_pending = false;
+        // S of the next tile -- after the item's last tile, of the next
+        // item, whose K sits in this item's V buffer -- once dV has read P^T
+        // out of the S columns
+        bool next_s = !last;
         if (last) {
           have_next = fetch(ne0, ne1);
           if (have_next < 0) { where = kErrWaitItem; break; }
           if (have_next > 0) {
             if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) { where = kErrWaitTest; break; }
-            s_pending = true;
+            if (!mbar_wait(&bars[kBufFull0 + vb], (ic + 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+            next_s = true;
           }
         }
-        if (!last || s_pending) {
+        if (next_s) {
           if (!mbar_wait(&bars[kDvDone], n & 1, abort_flag)) { where = kErrWaitMisc; break; }
-        }
-        if (!last || (s_pending && mbar_test(&bars[kBufFull0 + vb], (ic + 1) & 1))) {
           if (!mbar_wait(&bars[kQFull0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1, abort_flag)) {
             where = kErrWaitQ;
             break;
           }
           tc_fence_after();
           issue_s(n + 1, last ? aV : aK);
-          s_pending = false;
         }
+        first = false;
+        ++n;
+      }
+      if (where) break;
+      ++ic;
+      ce0 = ne0;
+      ce1 = ne1;
+      have = have_next;
+    }
+    if (where) record_error(p.header, where);
+    if (*abort_flag) {  // wait for MMAs still in flight before TMEM is freed
+      if (elect_one()) tc_commit(&bars[kDrainBar]);
+      __syncwarp();
+      mbar_wait_drain(&bars[kDrainBar], 0);
+    }
+  } else if (warp == kMma2Warp) {
+    // ------------------------------------------------ MMA issuer: dQ and dK
+    // A second issuing warp keeps the tensor pipe fed while the first one
+    // waits for P, dO or the S columns, and vice versa. The two share no
+    // barrier phase: dQ and dK follow dS, which the softmax warps signal only
+    // after the S and dP MMAs of the tile have completed.
+    uint32_t n = 0, itc = 0, ic = 0;  // tiles, ring slots read, non-empty items
+    const uint32_t aBuf0 = smem_u32(sK), aBuf1 = smem_u32(sV), adS = smem_u32(sdS);
+    int where = 0;
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int4 raw = item_slot[slot];
+      __syncwarp();
+      if (elect_one()) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      ++itc;
+      if (raw.x < 0) break;
+      const int e0 = raw.y, e1 = raw.z;
+      if (e0 >= e1) continue;
+      const int kb = ic & 1;
+      const uint32_t aK = kb ? aBuf1 : aBuf0;
+      for (int e = e0; e < e1; ++e) {
+        const bool first = e == e0, last = e + 1 == e1;
+        const int st = n & 1;
+        const uint32_t aQ = smem_u32(sQ0 + st * S::kTileBytes);
         if (!mbar_wait(&bars[kDsReady], n & 1, abort_flag)) { where = kErrWaitDS; break; }
+        if (first) {  // this item's K, and dK of the previous item read out
+          if (!mbar_wait(&bars[kBufFull0 + kb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
+          if (!mbar_wait(&bars[kAccEmpty], (ic & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        }
         tc_fence_after();
         if (elect_one()) {
           // dQ = dS K  (A = dS, MN-major; B = K, MN-major) into the dP columns,
@@ -585,32 +629,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&bars[kQEmpty0 + st]);
           tc_commit(&bars[kDsFree]);
-          if (last) tc_commit(&bars[kAccFull]);
+          if (last) tc_commit(&bars[kAccFull]);  // dK of the item complete
         }
         __syncwarp();
-        if (s_pending) {  // the next item's first S, now that its K has landed
-          if (!mbar_wait(&bars[kBufFull0 + vb], (ic + 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
-          if (!mbar_wait(&bars[kQFull0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1, abort_flag)) {
-            where = kErrWaitQ;
-            break;
-          }
-          tc_fence_after();
-          issue_s(n + 1, aV);
-        }
-        first = false;
         ++n;
       }
       if (where) break;
       ++ic;
-      ce0 = ne0;
-      ce1 = ne1;
-      have = have_next;
     }
     if (where) record_error(p.header, where);
-    if (*abort_flag) {  // wait for MMAs still in flight before TMEM is freed
-      if (elect_one()) tc_commit(&bars[kDrainBar]);
+    if (*abort_flag) {  // wait for this warp's MMAs still in flight
+      if (elect_one()) tc_commit(&bars[kDrainBar2]);
       __syncwarp();
-      mbar_wait_drain(&bars[kDrainBar], 0);
+      mbar_wait_drain(&bars[kDrainBar2], 0);
     }
   } else if (warp < kDrainWarp0) {
     // ------------------------------------------------------------- softmax
