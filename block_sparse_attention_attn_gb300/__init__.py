@@ -9,4 +9,5 @@ from .binding import (bsa_grad_workspace_size, bsa_grad, bsa_fwd_workspace_size,
                       bsa_fwd, bsa_mask_compact, bsa_mask_compact_noalloc, bsa_check_status,
                       BsaError,
                       block_sparse_attention_grad, block_sparse_attention_fwd,
+                      block_sparse_attention, BlockSparseAttentionFunction,
                       load_library, library_path)

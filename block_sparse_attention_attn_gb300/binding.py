@@ -64,6 +64,7 @@ def load_library():
     lib.bsa_executor_destroy.argtypes = [vp]
     lib.bsa_executor_set_timing_events.argtypes = [vp, vp, vp]
     lib.bsa_executor_set_wait_test.argtypes = [vp, ctypes.c_int32]
+    lib.bsa_executor_set_deterministic.argtypes = [vp, ctypes.c_int32]
     lib.bsa_mask_compact_workspace_size.argtypes = [T, i64, i64, P(u64)]
     lib.bsa_mask_compact.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp, vp, vp,
                                      u64, vp]
@@ -74,7 +75,7 @@ def load_library():
     lib.bsa_version.restype = ctypes.c_int32
     for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
                  "bsa_executor_destroy", "bsa_executor_set_timing_events",
-                 "bsa_executor_set_wait_test",
+                 "bsa_executor_set_wait_test", "bsa_executor_set_deterministic",
                  "bsa_mask_compact_workspace_size", "bsa_mask_compact",
                  "bsa_mask_compact_noalloc", "bsa_check_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -143,6 +144,11 @@ class Executor:
         """Failure-path test: the run's backward kernel waits once on a barrier
         nothing completes; bsa_check_status then reports 561002."""
         _check(load_library().bsa_executor_set_wait_test(self.handle, 1 if enable else 0))
+
+    def set_deterministic(self, enable: bool = True):
+        """dQ from a separate query-tile pass: bitwise identical results on
+        every run (backward executors only)."""
+        _check(load_library().bsa_executor_set_deterministic(self.handle, 1 if enable else 0))
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:
@@ -258,7 +264,8 @@ def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_
                                 block_sparse_mask=None, block_shape=None,
                                 actual_seq_lengths=None, actual_seq_lengths_kv=None,
                                 layout="BNSD", num_key_value_heads=None, scale_value=None,
-                                dq=None, dk=None, dv=None, workspace=None, stream=None):
+                                dq=None, dk=None, dv=None, workspace=None, stream=None,
+                                deterministic=False):
     """Both stages; allocates outputs/workspace with torch when not given.
     Returns (dq, dk, dv, workspace)."""
     if scale_value is None:
@@ -270,6 +277,8 @@ def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_
         dout, query, key, value, attention_out, softmax_lse, block_sparse_mask, None,
         block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
         num_key_value_heads, 0, scale_value, dq=dq, dk=dk, dv=dv)
+    if deterministic:
+        ex.set_deterministic(True)
     if workspace is None or workspace.numel() < size:
         workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=query.device)
     bsa_grad(workspace, size, ex, stream)
@@ -293,3 +302,47 @@ def block_sparse_attention_fwd(query, key, value, block_sparse_mask=None, block_
         workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=query.device)
     bsa_fwd(workspace, size, ex, stream)
     return out, lse, workspace
+
+
+class BlockSparseAttentionFunction(torch.autograd.Function):
+    """Autograd pairing of the companion forward (Out, lse) and the backward:
+    forward runs bsa_fwd, backward runs bsa_grad on the saved Q, K, V, Out and
+    lse (the page's call sequence, with PyTorch driving it). The mask, block
+    shape, lengths and options are not differentiable."""
+
+    @staticmethod
+    def forward(ctx, query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
+                actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic):
+        if scale_value is None:
+            scale_value = query.shape[-1] ** -0.5
+        query, key, value = query.contiguous(), key.contiguous(), value.contiguous()
+        out, lse, _ = block_sparse_attention_fwd(
+            query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
+            actual_seq_lengths_kv, layout, num_key_value_heads, scale_value)
+        ctx.save_for_backward(query, key, value, out, lse)
+        ctx.mask = block_sparse_mask
+        ctx.args = (block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout,
+                    num_key_value_heads, scale_value, deterministic)
+        return out
+
+    @staticmethod
+    def backward(ctx, dout):
+        query, key, value, out, lse = ctx.saved_tensors
+        (block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout, num_key_value_heads,
+         scale_value, deterministic) = ctx.args
+        dq, dk, dv, ws = block_sparse_attention_grad(
+            dout.contiguous(), query, key, value, out, lse, ctx.mask, block_shape,
+            actual_seq_lengths, actual_seq_lengths_kv, layout, num_key_value_heads, scale_value,
+            deterministic=deterministic)
+        bsa_check_status(ws)
+        return dq, dk, dv, None, None, None, None, None, None, None, None
+
+
+def block_sparse_attention(query, key, value, block_sparse_mask=None, block_shape=None,
+                           actual_seq_lengths=None, actual_seq_lengths_kv=None, layout="BNSD",
+                           num_key_value_heads=None, scale_value=None, deterministic=False):
+    """Differentiable block-sparse attention: Out = softmax(scale*Q K^T over the
+    selected blocks) V; gradients for Q, K and V come from the backward kernels."""
+    return BlockSparseAttentionFunction.apply(
+        query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
+        actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic)

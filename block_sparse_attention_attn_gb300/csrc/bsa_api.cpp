@@ -462,6 +462,13 @@ bsa_status bsa_executor_set_wait_test(bsa_executor* executor, int32_t enable) {
   return ok();
 }
 
+bsa_status bsa_executor_set_deterministic(bsa_executor* executor, int32_t enable) {
+  if (executor == nullptr) return fail(BSA_ERR_PARAM_NULLPTR, "executor is NULL");
+  if (executor->kind != 1) return fail(BSA_ERR_PARAM_INVALID, "not a backward executor");
+  executor->plan.det = enable ? 1 : 0;
+  return ok();
+}
+
 bsa_status bsa_executor_destroy(bsa_executor* executor) {
   delete executor;
   return ok();
@@ -693,6 +700,10 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   what = "backward";
   if (ex->ev_before && (e = cudaEventRecord(ex->ev_before, st)) != cudaSuccess) goto launch_fail;
   if ((e = launch_bwd(p, maps, st)) != cudaSuccess) goto launch_fail;
+  if (p.det) {
+    what = "deterministic dQ";
+    if ((e = launch_bwd_dq(p, maps, st)) != cudaSuccess) goto launch_fail;
+  }
   if (ex->ev_after && (e = cudaEventRecord(ex->ev_after, st)) != cudaSuccess) goto launch_fail;
   what = "finalize";
   if ((e = launch_finalize(p, st)) != cudaSuccess) goto launch_fail;

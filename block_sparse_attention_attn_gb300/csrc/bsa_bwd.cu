@@ -612,12 +612,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (elect_one()) {
           // dQ = dS K  (A = dS, MN-major; B = K, MN-major) into the dP columns,
-          // which the softmax warps have read before they signalled dS
+          // which the softmax warps have read before they signalled dS (not in
+          // the deterministic mode, where a separate pass computes dQ)
           const uint64_t dSmn = sdesc_sw128(adS, kPanel, 1024), dKmn = sdesc_sw128(aK, kPanel, 1024);
           const uint64_t dSk = sdesc_sw128(adS, 16, 1024), dQmn = sdesc_sw128(aQ, kPanel, 1024);
+          if (!p.det) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            mma_ss(tmem + kColP, dSmn + mn_step(k), dKmn + mn_step(k), kIdQ, k > 0);
+            for (int k = 0; k < 8; ++k) {
+              mma_ss(tmem + kColP, dSmn + mn_step(k), dKmn + mn_step(k), kIdQ, k > 0);
+            }
           }
           tc_commit(&bars[kDqFull]);
           if (last) tc_commit(&bars[kBufEmpty0 + kb]);  // K read for the last time
@@ -770,6 +773,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = ii.g * p.G + entry_hl(ent);
         if (!mbar_wait(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
         tc_fence_after();
+        if (p.det) {  // no dQ here: the columns go straight back to the next dP
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kDqEmpty]);
+          ++n;
+          continue;
+        }
         // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp owns 32
         // rows and an 8 KB part of the staging buffer: two 32 x 32 fp32 boxes
         // (128-byte swizzled), i.e. 64 columns at a time. With D = 128 the

@@ -1,0 +1,561 @@
+// bsa_bwd_dq.cu - deterministic dQ pass of the block-sparse attention backward
+// on the sm_103a tensor cores. For every query tile it walks the selected key
+// tiles in ascending order and accumulates
+//     dQ = scale * sum_j dS_j K_j,   dS_j = P_j o (dP_j - D),
+//     P_j = exp(scale * Q K_j^T - lse),   dP_j = dO V_j^T
+// (backward formulas of the aclnnBlockSparseAttentionGrad page, section
+// 计算公式) in TMEM, so the result does not depend on the order in which
+// other CTAs finish: no fp32 reduce-adds, the same bits on every run. The
+// key-tile-stationary kernel then computes dK and dV only.
+//
+// One persistent CTA per SM, 192 threads:
+//   warp 4      producer: Q and dO of the query tile, then K/V tiles of the
+//               selected key tiles (found by scanning the mask row) through a
+//               2-stage TMA ring;
+//   warp 5      MMA issuer and TMEM owner: S = Q K^T, dP = dO V^T (shared-
+//               memory operands), dQ += dS K (dS read from TMEM);
+//   warps 0-3   TMEM lane s = query row s: P and dS (lse and D are per-thread
+//               values here), then the dQ epilogue.
+// TMEM columns: [0,128) S, then dS packed in place; [128,256) dP;
+// [256,256+D) dQ.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bsa_common.h"
+#include "bsa_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace bsa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kProdWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kPanel = 128 * 128;
+constexpr uint32_t kColS = 0, kColP = 128, kColQ = 256;
+
+enum Bar {
+  kQFull = 0, kQAux, kQEmpty,
+  kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kKvAux0, kKvAux1,
+  kSFull, kDpFull, kDsReady, kDqStep, kDqFull, kDqEmpty,
+  kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
+  kDrain,
+  kNumBars
+};
+
+template <int D>
+struct Smem {
+  static constexpr int kTileBytes = (D / 64) * kPanel;
+  static constexpr int oQ = 0;
+  static constexpr int odO = oQ + kTileBytes;
+  static constexpr int oK = odO + kTileBytes;      // [2]
+  static constexpr int oV = oK + 2 * kTileBytes;   // [2]
+  static constexpr int oBar = oV + 2 * kTileBytes;
+  static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;
+  static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
+  static constexpr int kBytes = oMisc + 128;
+};
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<kDtBF16> {
+  using T = __nv_bfloat16;
+  static constexpr int kAB = 1;
+  __device__ static uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+};
+template <>
+struct Elem<kDtF16> {
+  using T = __half;
+  static constexpr int kAB = 0;
+  __device__ static uint32_t pack(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __device__ static float round(float x) { return __half2float(__float2half_rn(x)); }
+};
+
+__device__ __forceinline__ void record_error(int* header, int where) {
+  atomicCAS(&header[kHdrErrorWhere], 0, where);
+  atomicExch(&header[kHdrError], 1);
+  atomicAdd(&header[kHdrErrorCounts + (where & 15)], 1);
+}
+
+__device__ __noinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
+  const int n16 = (128 - r0) * 8;
+  for (int pnl = 0; pnl < panels; ++pnl) {
+    uint4* base = reinterpret_cast<uint4*>(tile + pnl * kPanel + r0 * 128);
+    for (int i = lane; i < n16; i += 32) base[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+struct QItem {
+  int b, h, it;
+};
+
+__device__ __forceinline__ QItem decode(const Plan& p, int idx) {
+  QItem r;
+  r.it = idx % p.Mq_t;
+  const int bh = idx / p.Mq_t;
+  r.h = bh % p.N1;
+  r.b = bh / p.N1;
+  return r;
+}
+
+// Sub-block bits of key tile jt for query tile it of (b, h); 0 when the tile
+// has no selected block inside the valid range.
+__device__ __forceinline__ int q_tile_bits(const Plan& p, int b, int h, int it, int jt, int Lq, int Lk) {
+  int bits = 0;
+  for (int ri = 0; ri < p.rb; ++ri) {
+    const int i = it * p.rb + ri;
+    if (i * p.bx >= Lq) break;
+    for (int cj = 0; cj < p.cb; ++cj) {
+      const int j = jt * p.cb + cj;
+      if (j * p.by >= Lk) break;
+      bool on = true;
+      if (p.has_mask)
+        on = (i < p.Mq && j < p.Mk) &&
+             p.mask[(int64_t)b * p.mask_sb + (int64_t)h * p.mask_sh + (int64_t)i * p.mask_si + j] != 0;
+      if (on) bits |= 1 << (ri * 2 + cj);
+    }
+  }
+  return bits;
+}
+
+template <int D, int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_dq(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+             const Plan p) {
+  using S = Smem<D>;
+  using E = Elem<DT>;
+  using T = typename E::T;
+  constexpr int kPanels = D / 64;
+  constexpr uint32_t kIdS = idesc_f16(128, 128, E::kAB, 0, 0);  // S = Q K^T, dP = dO V^T
+  constexpr uint32_t kIdQ = idesc_f16(128, D, E::kAB, 0, 1);     // dQ += dS K (A in TMEM)
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  int* misc = reinterpret_cast<int*>(smem + S::oMisc);
+  volatile int* abort_flag = misc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 1);
+  int* item_slot = misc + 2;  // [2]
+  int* meta = misc + 4;       // [2] per stage: jt | bits << 24, -1 = end of item
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) record_error(p.header, kErrSmemAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(&bars[kQFull], 1);
+    mbar_init(&bars[kQAux], 1);
+    mbar_init(&bars[kQEmpty], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kKvFull0 + i], 1);
+      mbar_init(&bars[kKvEmpty0 + i], 5);  // MMA (commit or arrive) + 4 softmax warps
+      mbar_init(&bars[kKvAux0 + i], 1);
+      mbar_init(&bars[kItemFull0 + i], 1);
+      mbar_init(&bars[kItemEmpty0 + i], 5);
+    }
+    mbar_init(&bars[kSFull], 1);
+    mbar_init(&bars[kDpFull], 1);
+    mbar_init(&bars[kDsReady], 4);
+    mbar_init(&bars[kDqStep], 1);
+    mbar_init(&bars[kDqFull], 1);
+    mbar_init(&bars[kDqEmpty], 4);
+    mbar_init(&bars[kDrain], 1);
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == kProdWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint8_t* sQ = smem + S::oQ;
+  uint8_t* sdO = smem + S::odO;
+  uint8_t* sK0 = smem + S::oK;
+  uint8_t* sV0 = smem + S::oV;
+  const int n_items = p.B * p.N1 * p.Mq_t;
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    uint32_t n = 0, itc = 0, aux[2] = {0u, 0u}, qaux = 0;
+    bool ok = true;
+    int pend_q = 0, pend_qaux = 0, pend_kv[2] = {0, 0}, pend_aux[2] = {0, 0};
+    uint32_t par_kv[2] = {0u, 0u};
+    while (ok) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitItem);
+        break;
+      }
+      if (lane == 0) {
+        const int idx = atomicAdd(&p.header[kHdrDqCounter], 1);
+        item_slot[slot] = idx < n_items ? idx : -1;
+        mbar_arrive(&bars[kItemFull0 + slot]);
+      }
+      __syncwarp();
+      const int idx = item_slot[slot];
+      if (idx < 0) break;
+      const QItem qi = decode(p, idx);
+      const int Lq = p.lq[qi.b], Lk = p.lk[qi.b];
+      const int q0 = qi.it * 128;
+      const bool has_rows = q0 < Lq;
+      // Q and dO of the query tile (rows past the query length cleared)
+      if (!mbar_wait(&bars[kQEmpty], (itc & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitQ);
+        break;
+      }
+      const bool qtail = (Lq - q0) < 128;
+      if (lane == 0) {
+        uint64_t* tb = qtail ? &bars[kQAux] : &bars[kQFull];
+        mbar_arrive_expect_tx(tb, 2 * S::kTileBytes);
+        const int c1 = p.layout == kLayoutBNSD ? q0 : qi.h;
+        const int c2 = p.layout == kLayoutBNSD ? qi.b * p.N1 + qi.h : p.cu_q[qi.b] + q0;
+        for (int pn = 0; pn < kPanels; ++pn) {
+          tma_load_3d(sQ + pn * kPanel, &tm_q, tb, pn * 64, c1, c2);
+          tma_load_3d(sdO + pn * kPanel, &tm_do, tb, pn * 64, c1, c2);
+        }
+      }
+      pend_q = qtail ? 0 : 1;
+      pend_qaux = qtail ? 1 : 0;
+      if (qtail) {
+        if (!mbar_wait(&bars[kQAux], qaux & 1, abort_flag)) {
+          record_error(p.header, kErrWaitQ);
+          break;
+        }
+        qaux++;
+        pend_qaux = 0;
+        const int r0 = Lq - q0 > 0 ? Lq - q0 : 0;
+        zero_rows(sQ, kPanels, r0, lane);
+        zero_rows(sdO, kPanels, r0, lane);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kQFull]);
+      }
+      const int ncolt = has_rows ? (Lk + 127) / 128 : 0;
+      const int g = qi.h / p.G;
+      for (int jt0 = 0; jt0 < ncolt && ok; jt0 += 32) {
+        const int jt = jt0 + lane;
+        const int bits = jt < ncolt ? q_tile_bits(p, qi.b, qi.h, qi.it, jt, Lq, Lk) : 0;
+        unsigned ball = __ballot_sync(0xffffffffu, bits != 0);
+        while (ball && ok) {
+          const int src = __ffs(ball) - 1;
+          ball &= ball - 1;
+          const int jsel = jt0 + src;
+          const int bsel = __shfl_sync(0xffffffffu, bits, src);
+          const int st = n & 1;
+          if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+            record_error(p.header, kErrWaitKV);
+            ok = false;
+            break;
+          }
+          const bool tail = (Lk - jsel * 128) < 128;
+          uint8_t* sK = sK0 + st * S::kTileBytes;
+          uint8_t* sV = sV0 + st * S::kTileBytes;
+          if (lane == 0) {
+            meta[st] = jsel | (bsel << 24);
+            uint64_t* tb = tail ? &bars[kKvAux0 + st] : &bars[kKvFull0 + st];
+            mbar_arrive_expect_tx(tb, 2 * S::kTileBytes);
+            const int c1 = p.layout == kLayoutBNSD ? jsel * 128 : g;
+            const int c2 = p.layout == kLayoutBNSD ? qi.b * p.N2 + g : p.cu_k[qi.b] + jsel * 128;
+            for (int pn = 0; pn < kPanels; ++pn) {
+              tma_load_3d(sK + pn * kPanel, &tm_k, tb, pn * 64, c1, c2);
+              tma_load_3d(sV + pn * kPanel, &tm_v, tb, pn * 64, c1, c2);
+            }
+          }
+          pend_kv[st] = tail ? 0 : 1;
+          par_kv[st] = (n >> 1) & 1;
+          if (tail) {  // K and V rows past the key length must be finite zeros
+            pend_aux[st] = 1;
+            if (!mbar_wait(&bars[kKvAux0 + st], aux[st] & 1, abort_flag)) {
+              record_error(p.header, kErrWaitKV);
+              ok = false;
+              break;
+            }
+            aux[st]++;
+            pend_aux[st] = 0;
+            zero_rows(sK, kPanels, Lk - jsel * 128, lane);
+            zero_rows(sV, kPanels, Lk - jsel * 128, lane);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kKvFull0 + st]);
+          }
+          ++n;
+        }
+      }
+      if (!ok) break;
+      // end-of-item marker
+      const int st = n & 1;
+      if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+        record_error(p.header, kErrWaitKV);
+        break;
+      }
+      if (lane == 0) {
+        meta[st] = -1;
+        mbar_arrive(&bars[kKvFull0 + st]);
+      }
+      __syncwarp();
+      ++n;
+      ++itc;
+    }
+    if (*abort_flag) {  // let copies still in flight land before the CTA exits
+      if (pend_q) mbar_wait_drain(&bars[kQFull], itc & 1);
+      if (pend_qaux) mbar_wait_drain(&bars[kQAux], qaux & 1);
+      for (int st = 0; st < 2; ++st) {
+        if (pend_kv[st]) mbar_wait_drain(&bars[kKvFull0 + st], par_kv[st]);
+        if (pend_aux[st]) mbar_wait_drain(&bars[kKvAux0 + st], aux[st] & 1);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    uint32_t n = 0, itc = 0;  // n: K/V stages (end markers included)
+    uint32_t m = 0;           // m: computed key tiles
+    int where = 0;
+    const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO);
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int idx = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      if (idx < 0) break;
+      if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
+      int j = 0;
+      while (true) {
+        const int st = n & 1;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int mt = meta[st];
+        if (mt < 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+          ++n;
+          break;
+        }
+        // the S columns hold dS of the previous key tile until its dQ MMA
+        // has read them
+        if (m > 0 && !mbar_wait(&bars[kDqStep], (m - 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        tc_fence_after();
+        const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
+        const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
+        if (lane == 0) {
+          const uint64_t dQk = sdesc_sw128(aQ, 16, 1024), dKk = sdesc_sw128(aK, 16, 1024);
+          const uint64_t dOk = sdesc_sw128(adO, 16, 1024), dVk = sdesc_sw128(aV, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t off = (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
+            mma_ss(tmem + kColS, dQk + off, dKk + off, kIdS, k > 0);
+          }
+          tc_commit(&bars[kSFull]);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t off = (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
+            mma_ss(tmem + kColP, dOk + off, dVk + off, kIdS, k > 0);
+          }
+          tc_commit(&bars[kDpFull]);
+        }
+        __syncwarp();
+        if (!mbar_wait(&bars[kDsReady], m & 1, abort_flag)) { where = kErrWaitDS; break; }
+        // the first dQ MMA of an item overwrites the accumulator: the previous
+        // item's epilogue must have read it
+        if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        tc_fence_after();
+        if (lane == 0) {  // dQ += dS K: A = dS (TMEM, packed in the S columns), B = K (MN-major)
+          const uint64_t dKmn = sdesc_sw128(aK, kPanel, 1024);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColQ, tmem + kColS + 8 * k, dKmn + (uint64_t)((k * 2048) >> 4), kIdQ,
+                   (j == 0 && k == 0) ? 0u : 1u);
+          tc_commit(&bars[kDqStep]);
+          tc_commit(&bars[kKvEmpty0 + st]);
+        }
+        __syncwarp();
+        ++j;
+        ++n;
+        ++m;
+      }
+      if (where) break;
+      // every item waits for the previous epilogue exactly once
+      if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+      if (lane == 0) {
+        tc_commit(&bars[kDqFull]);
+        tc_commit(&bars[kQEmpty]);
+      }
+      __syncwarp();
+      ++itc;
+    }
+    if (where) record_error(p.header, where);
+    if (*abort_flag) {
+      if (lane == 0) tc_commit(&bars[kDrain]);
+      __syncwarp();
+      mbar_wait_drain(&bars[kDrain], 0);
+    }
+  } else {
+    // ----------------------------------------------------- P, dS, epilogue
+    const int s = warp * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t n = 0, itc = 0, m = 0;
+    int where = 0;
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int idx = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      if (idx < 0) break;
+      const QItem qi = decode(p, idx);
+      const int Lq = p.lq[qi.b], Lk = p.lk[qi.b];
+      const int srow = qi.it * 128 + s;
+      const bool s_ok = srow < Lq;
+      // lse2 = lse * log2(e) (+inf past the query length) and D of this row
+      const int64_t prow = (int64_t)qi.h * p.Rq + p.qrow[qi.b] + srow;
+      const float lse2 = s_ok ? p.lse2[prow] : 0.f;
+      const float dsum = s_ok ? p.dvec[prow] : 0.f;
+      const int s_sub = p.rb == 2 ? (s >> 6) : 0;
+      int j = 0;
+      while (true) {
+        const int st = n & 1;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int mt = meta[st];
+        if (mt < 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+          ++n;
+          break;
+        }
+        const int jt = mt & 0xFFFFFF, bits = mt >> 24;
+        if (!mbar_wait(&bars[kSFull], m & 1, abort_flag)) { where = kErrWaitS; break; }
+        if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
+        tc_fence_after();
+        const int t_lim = Lk - jt * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32], y[32];
+          tmem_ld32(tmem + lane_off + kColS + 32 * c, x);
+          tmem_ld32(tmem + lane_off + kColP + 32 * c, y);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float ds[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int t = 32 * c + 2 * k + u;
+              const int t_sub = p.cb == 2 ? (t >> 6) : 0;
+              const bool on = s_ok && t < t_lim && ((bits >> (s_sub * 2 + t_sub)) & 1);
+              // P rounded to the operand type, as in the dV/dK kernel
+              const float pv =
+                  on ? E::round(ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)))
+                     : 0.f;
+              ds[u] = on ? pv * (__uint_as_float(y[2 * k + u]) - dsum) : 0.f;
+            }
+            pk[k] = E::pack(ds[0], ds[1]);
+          }
+          tmem_st16(tmem + lane_off + kColS + 16 * c, pk);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[kDsReady]);
+          mbar_arrive(&bars[kKvEmpty0 + st]);
+        }
+        ++j;
+        ++n;
+        ++m;
+      }
+      if (where) break;
+      // epilogue: dQ = scale * accumulator (zeros when no key tile was selected)
+      if (!mbar_wait(&bars[kDqFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
+      tc_fence_after();
+      const bool write_row = p.layout == kLayoutBNSD ? (srow < p.Sq) : s_ok;
+      int64_t ooff, sd;
+      if (p.layout == kLayoutBNSD) {
+        ooff = qi.b * p.dq_st[0] + qi.h * p.dq_st[1] + (int64_t)srow * p.dq_st[2];
+        sd = p.dq_st[3];
+      } else {
+        ooff = ((int64_t)p.cu_q[qi.b] + srow) * p.dq_st[0] + qi.h * p.dq_st[1];
+        sd = p.dq_st[2];
+      }
+      T* out = static_cast<T*>(p.dq) + ooff;
+      const float mul = (s_ok && j > 0) ? p.scale : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (j > 0) {
+          tmem_ld32(tmem + lane_off + kColQ + 32 * c, o);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = 0u;
+        }
+        if (write_row) {
+          if (p.dq_vec) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 u;
+              u.x = E::pack(__uint_as_float(o[8 * q]) * mul, __uint_as_float(o[8 * q + 1]) * mul);
+              u.y = E::pack(__uint_as_float(o[8 * q + 2]) * mul, __uint_as_float(o[8 * q + 3]) * mul);
+              u.z = E::pack(__uint_as_float(o[8 * q + 4]) * mul, __uint_as_float(o[8 * q + 5]) * mul);
+              u.w = E::pack(__uint_as_float(o[8 * q + 6]) * mul, __uint_as_float(o[8 * q + 7]) * mul);
+              *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = u;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const uint32_t pk = E::pack(__uint_as_float(o[k]) * mul, 0.f);
+              out[(32 * c + k) * sd] = *reinterpret_cast<const T*>(&pk);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kDqEmpty]);
+      ++itc;
+    }
+    if (where) record_error(p.header, where);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DT>
+cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
+  const size_t smem = Smem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int n_items = p.B * p.N1 * p.Mq_t;
+  int grid = p.num_sms;
+  if (n_items < grid) grid = n_items;
+  if (grid < 1) grid = 1;
+  k_bwd_dq<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const Plan& p, const BwdMaps& m, cudaStream_t st) {
+  if (p.dtype == kDtBF16)
+    return p.D == 128 ? launch_t<128, kDtBF16>(p, m, st) : launch_t<64, kDtBF16>(p, m, st);
+  return p.D == 128 ? launch_t<128, kDtF16>(p, m, st) : launch_t<64, kDtF16>(p, m, st);
+}
+
+}  // namespace bsa

@@ -30,6 +30,7 @@ enum HeaderWord {
   kHdrChunkLen = 5,    // split threshold used
   kHdrErrorWhere = 6,  // code of the first wait that gave up
   kHdrFinTiles = 7,    // key tiles the finalize kernel writes (unselected or split)
+  kHdrDqCounter = 8,   // work-queue head of the deterministic dQ pass
   kHdrErrorCounts = 16, // [16, 32): number of failed waits per code
   kHdrWords = 64
 };
@@ -88,6 +89,7 @@ struct Plan {
   int64_t dq_st[4], dk_st[4], dv_st[4]; // output strides (elements), layout order
   int dq_vec, dkv_vec;                  // outputs allow 16-byte row stores
   int dkv_tma;                          // dK / dV written by TMA stores (BwdMaps dk, dv)
+  int det;                              // deterministic dQ: separate query-tile pass, no reduce-adds
   // per-batch info in the workspace (int32 [B] each)
   const int* lq;
   const int* lk;

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     p.header[kHdrFinTiles] = fin_carry;
     p.header[kHdrChunkLen] = L;
     p.header[kHdrWorkCounter] = 0;
+    p.header[kHdrDqCounter] = 0;
     p.header[kHdrError] = 0;
     p.header[kHdrErrorWhere] = 0;
     for (int i = 0; i < 16; ++i) p.header[kHdrErrorCounts + i] = 0;
@@ -329,9 +330,11 @@ __global__ void __launch_bounds__(256) k_preprocess(Plan p) {
     p.dvec[row] = valid ? acc : 0.f;
     p.lse2[row] = l2;
   }
-  float4* dst = reinterpret_cast<float4*>(p.dqacc + row * D) + sub * 2;
-  dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-  dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!p.det) {  // the deterministic dQ pass does not use the accumulator
+    float4* dst = reinterpret_cast<float4*>(p.dqacc + row * D) + sub * 2;
+    dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -479,7 +482,7 @@ __device__ __forceinline__ void finalize_dkdv_tiles(const Plan& p) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) k_finalize(Plan p) {
-  finalize_dq_rows<T, D>(p);
+  if (!p.det) finalize_dq_rows<T, D>(p);  // else dQ came from the deterministic pass
   finalize_dkdv_tiles<T, D>(p);
 }
 

@@ -53,6 +53,8 @@ struct BwdMaps {
   CUtensorMap dk, dv; // outputs, box 64 x 32 rows, 128-byte swizzle: BNSD (d, s, n, b), TND (d, n, t)
 };
 cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st);
+// Deterministic dQ pass (query-tile stationary), used when p.det is set.
+cudaError_t launch_bwd_dq(const Plan& p, const BwdMaps& m, cudaStream_t st);
 size_t bwd_smem_bytes(int D);
 
 struct FwdMaps {

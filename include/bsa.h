@@ -149,6 +149,18 @@ bsa_status bsa_executor_set_timing_events(bsa_executor* executor, void* event_be
  * context stays usable. Backward executors only. */
 bsa_status bsa_executor_set_wait_test(bsa_executor* executor, int32_t enable);
 
+/* Deterministic dQ (backward executors only). With enable != 0 the run
+ * computes dQ in a separate query-tile pass: every query tile walks its
+ * selected key tiles in ascending order and accumulates dS*K in the tensor
+ * memory of one CTA, so dQ, dK and dV are bitwise identical from run to run
+ * (the default path sums dQ with fp32 reduce-adds whose order varies, so only
+ * its rounding differs between runs). Costs about 40 % more tensor-core work
+ * (S and dP are computed twice) and no fp32 dQ accumulator traffic.
+ * Determinism as a documented property of a backward op: the CompressorGrad
+ * page, section 确定性计算; pairing with PyTorch: the
+ * aclnnBlockSparseAttentionGrad page, section 约束说明. */
+bsa_status bsa_executor_set_deterministic(bsa_executor* executor, int32_t enable);
+
 /* Frees an executor that was never passed to a run call. NULL is a no-op. */
 bsa_status bsa_executor_destroy(bsa_executor* executor);
 

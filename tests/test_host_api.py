@@ -116,3 +116,7 @@ def test_run_call_rejects_null_executor(lib):
 
 def test_wait_test_switch_needs_an_executor(lib):
     assert lib.bsa_executor_set_wait_test(None, 1) == B.BSA_ERR_PARAM_NULLPTR
+
+
+def test_deterministic_switch_needs_a_backward_executor(lib):
+    assert lib.bsa_executor_set_deterministic(None, 1) == B.BSA_ERR_PARAM_NULLPTR
