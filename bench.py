@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default="w1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the deterministic dQ mode (separate query-tile pass)")
     return ap.parse_args()
 
 
@@ -182,13 +184,19 @@ def make_inputs(w, dev):
                 block_sparse_mask=mask), seq
 
 
+DETERMINISTIC = False  # set from --deterministic
+
+
 def grad_executor(w, t, seq, dq, dk, dv):
     import block_sparse_attention_attn_gb300 as bsa
-    return bsa.bsa_grad_workspace_size(
+    size, ex = bsa.bsa_grad_workspace_size(
         t["dout"], t["query"], t["key"], t["value"], t["attention_out"], t["softmax_lse"],
         t["block_sparse_mask"], None, [w.bx, w.by], seq["actual_seq_lengths"],
         seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, 0, w.scale,
         dq=dq, dk=dk, dv=dv)
+    if DETERMINISTIC:
+        ex.set_deterministic(True)
+    return size, ex
 
 
 # --------------------------------------------------------------- our arm
@@ -288,12 +296,15 @@ def bench_ours(args, rank, world, local):
                    "Sq": w.Sq, "Skv": w.Skv, "D": w.D, "block": [w.bx, w.by],
                    "active_blocks": summ["active_blocks"], "density": round(summ["density"], 4),
                    "gflop_per_step": round(flops / 1e9, 2), "parallelism": f"replicas x{world}",
-                   "l2": "flushed (512 MB write) before every timed step"},
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "dq_mode": "deterministic (query-tile pass)" if DETERMINISTIC else "fp32 reduce-add"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": committed_traffic(w.name),
-                     "kernel": "k_bwd (tcgen05 backward)", "kernel_ms": round(ms_kern, 4),
+                     "traffic": None if DETERMINISTIC else committed_traffic(w.name),
+                     "kernel": ("k_bwd + k_bwd_dq (tcgen05 backward, deterministic dQ)"
+                                if DETERMINISTIC else "k_bwd (tcgen05 backward)"),
+                     "kernel_ms": round(ms_kern, 4),
                      "peak_source": f"{src}: MEASURED_PEAKS.json bf16_tflops (burst)"
                      if src == "measured" else "fallback 1.9 PFLOP/s bf16"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
@@ -394,6 +405,8 @@ def main():
             return
         print(json.dumps(bench_reference(args, rank, world)), flush=True)
         return
+    global DETERMINISTIC
+    DETERMINISTIC = args.deterministic
     rank, world, local = dist_setup(args.gpus)
     line = bench_ours(args, rank, world, local)
     if rank == 0:
