@@ -32,19 +32,34 @@ R3  Query head h reads key/value head g = h // (N1/N2) (contiguous groups);
 R4  Only tokens below the per-batch actual lengths count; mask bits of blocks
     starting at or beyond them are ignored. Output rows at or beyond the actual
     length (BNSD padding) are 0.
-R5  Inside a selected block every token pair takes part (no token-level mask:
-    attenMaskOptional must be null and maskType 0).
+R5  Inside a selected block every token pair takes part unless the sliding
+    window of R8 excludes it (no other token-level mask: attenMaskOptional must
+    be null and maskType 0).
 R6  A query row with no selected key has Out = 0 and lse = -inf in the forward
     and contributes nothing in the backward (its dQ row is 0).
 R7  In TND, actualSeqLengths are per-batch counts; batch b starts at the
     exclusive prefix sum of the counts.
+R8  preTokens / nextTokens (parameter table rows preTokens, nextTokens: how
+    many earlier / later tokens a token may attend to; FlashAttentionScore
+    page, 参数说明: left / right edge of the sliding window, and 约束说明: the
+    two must overlap). Query s and key t of one sequence, both counted from 0
+    at the start of that sequence, form a pair of the window iff
+    s - preTokens <= t <= s + nextTokens; a pair takes part iff its block is
+    selected AND it lies in the window. preTokens + nextTokens >= 0 (the
+    window is never empty on the diagonal). 2147483647 for both (the only
+    value the page's own build accepts) is no window for any sequence shorter
+    than 2^31. nextTokens = 0 with preTokens = 2147483647 is the causal
+    (lower-triangular, top-left aligned) mask.
 """
 from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["token_mask", "token_mask_at", "head_rows", "forward", "forward_blockrows", "backward",
-           "backward_dq_rows", "backward_dkdv_rows", "compact_mask", "seq_offsets"]
+__all__ = ["token_mask", "token_mask_at", "window_mask", "head_rows", "forward",
+           "forward_blockrows", "backward", "backward_dq_rows", "backward_dkdv_rows",
+           "compact_mask", "seq_offsets", "NO_WINDOW"]
+
+NO_WINDOW = 2147483647   # preTokens / nextTokens value for "no sliding window" (R8)
 
 
 # --------------------------------------------------------------------------
@@ -76,26 +91,38 @@ def _lse_rows(lse, layout, b, h, length, offsets):
                       dtype=np.float64)
 
 
-def token_mask(block_mask, bx, by, Lq, Lk):
+def window_mask(rows, cols, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+    """[len(rows), len(cols)] bool: query position s = rows[i] and key position
+    t = cols[j] (both counted from the start of their sequence) satisfy
+    s - preTokens <= t <= s + nextTokens (reading R8)."""
+    s = np.asarray(rows, dtype=np.int64)[:, None]
+    t = np.asarray(cols, dtype=np.int64)[None, :]
+    # |t - s| < 2^31, so limits beyond +-2^40 act as no limit; clipping them
+    # only keeps the int64 arithmetic away from overflow
+    pre = max(-(1 << 40), min(1 << 40, int(pre_tokens)))
+    nxt = max(-(1 << 40), min(1 << 40, int(next_tokens)))
+    return (t >= s - pre) & (t <= s + nxt)
+
+
+def token_mask(block_mask, bx, by, Lq, Lk, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
     """Token-level [Lq, Lk] bool mask of one (b, h): pair (s, t) takes part iff
     the block (s // bx, t // by) is selected (parameter table,
-    blockSparseMaskOptional). ``None`` = every pair (dense)."""
-    if block_mask is None:
-        return np.ones((Lq, Lk), dtype=bool)
-    bm = np.asarray(block_mask) != 0
-    rows = np.arange(Lq) // bx
-    cols = np.arange(Lk) // by
-    return bm[rows[:, None], cols[None, :]]
+    blockSparseMaskOptional; ``None`` = every block) and (s, t) lies in the
+    sliding window (R8)."""
+    return token_mask_at(block_mask, bx, by, np.arange(Lq), np.arange(Lk),
+                         pre_tokens, next_tokens)
 
 
-def token_mask_at(block_mask, bx, by, rows, cols):
+def token_mask_at(block_mask, bx, by, rows, cols, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
     """The entries [rows x cols] of :func:`token_mask` only (same definition,
     evaluated on the requested query rows and key columns)."""
     rows, cols = np.asarray(rows), np.asarray(cols)
     if block_mask is None:
-        return np.ones((len(rows), len(cols)), dtype=bool)
-    bm = np.asarray(block_mask) != 0
-    return bm[(rows // bx)[:, None], (cols // by)[None, :]]
+        sel = np.ones((len(rows), len(cols)), dtype=bool)
+    else:
+        bm = np.asarray(block_mask) != 0
+        sel = bm[(rows // bx)[:, None], (cols // by)[None, :]]
+    return sel & window_mask(rows, cols, pre_tokens, next_tokens)
 
 
 def _dims(q, k, layout):
@@ -137,7 +164,8 @@ def _head_forward(Qm, Km, Vm, M, scale):
 
 
 def forward(q, k, v, mask=None, block_shape=(128, 128), seq_q=None, seq_kv=None,
-            layout="BNSD", num_kv_heads=None, scale=1.0):
+            layout="BNSD", num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
+            next_tokens=NO_WINDOW):
     """Plain dense-with-mask forward. Returns (out, lse) in the layout's shapes
     (lse with the trailing 1), fp64. Padding rows: out 0, lse -inf (R4, R6)."""
     bx, by = int(block_shape[0]), int(block_shape[1])
@@ -156,7 +184,8 @@ def forward(q, k, v, mask=None, block_shape=(128, 128), seq_q=None, seq_kv=None,
             Qm = head_rows(q, layout, b, h, lq[b], oq)
             Km = head_rows(k, layout, b, g, lk[b], okv)
             Vm = head_rows(v, layout, b, g, lk[b], okv)
-            M = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b])
+            M = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b],
+                           pre_tokens, next_tokens)
             o, l = _head_forward(Qm, Km, Vm, M, scale)
             if layout == "BNSD":
                 out[b, h, :lq[b]] = o
@@ -168,7 +197,8 @@ def forward(q, k, v, mask=None, block_shape=(128, 128), seq_q=None, seq_kv=None,
 
 
 def forward_blockrows(q, k, v, mask=None, block_shape=(128, 128), seq_q=None,
-                      seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0):
+                      seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0,
+                      pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
     """The same forward, evaluated per query block row over that row's selected
     key set K(s) only (every query row of a block row has the same K(s)). Used
     where the dense [Lq, Lk] score matrix would not fit in host memory; pinned
@@ -201,7 +231,7 @@ def forward_blockrows(q, k, v, mask=None, block_shape=(128, 128), seq_q=None,
                     continue
                 keys = np.concatenate([np.arange(j * by, min(lk[b], (j + 1) * by))
                                        for j in sel])
-                M = np.ones((s1 - s0, len(keys)), dtype=bool)
+                M = window_mask(np.arange(s0, s1), keys, pre_tokens, next_tokens)
                 o, l = _head_forward(Qh[s0:s1], Kh[keys], Vh[keys], M, scale)
                 if layout == "BNSD":
                     out[b, h, s0:s1] = o
@@ -231,7 +261,8 @@ def _head_backward(Qm, Km, Vm, dOm, Om, lse, M, scale):
 
 
 def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=None,
-             seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0):
+             seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
+             next_tokens=NO_WINDOW):
     """Full dQ, dK, dV (fp64, the layout's shapes) from the given Out and lse."""
     bx, by = int(block_shape[0]), int(block_shape[1])
     B, lq, lk = _lengths(q, k, layout, seq_q, seq_kv)
@@ -250,7 +281,8 @@ def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=N
             dOm = head_rows(dout, layout, b, h, lq[b], oq)
             Om = head_rows(out, layout, b, h, lq[b], oq)
             L = _lse_rows(lse, layout, b, h, lq[b], oq)
-            M = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b])
+            M = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b],
+                           pre_tokens, next_tokens)
             dQ, dK, dV = _head_backward(Qm, Km, Vm, dOm, Om, L, M, scale)
             if layout == "BNSD":
                 dq[b, h, :lq[b]] = dQ
@@ -265,7 +297,8 @@ def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=N
 
 def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
                      block_shape=(128, 128), seq_q=None, seq_kv=None, layout="BNSD",
-                     num_kv_heads=None, scale=1.0):
+                     num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
+                     next_tokens=NO_WINDOW):
     """dQ[b, h, rows] only (fp64 [len(rows), D]); each row needs only its own
     query, dOut, Out, lse and the keys it selects. Rows at or beyond the actual
     length are 0 (R4)."""
@@ -286,7 +319,8 @@ def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
     L = _lse_rows(lse, layout, b, h, lq[b], oq)[r]
     Km = head_rows(k, layout, b, g, lk[b], okv)
     Vm = head_rows(v, layout, b, g, lk[b], okv)
-    M = token_mask_at(None if mask is None else mask[b, h], bx, by, r, np.arange(lk[b]))
+    M = token_mask_at(None if mask is None else mask[b, h], bx, by, r, np.arange(lk[b]),
+                      pre_tokens, next_tokens)
     dQ, _, _ = _head_backward(Qh, Km, Vm, dOh, Oh, L, M, scale)
     res[ok] = dQ
     return res
@@ -294,7 +328,8 @@ def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
 
 def backward_dkdv_rows(dout, q, k, v, out, lse, b, g, rows, mask=None,
                        block_shape=(128, 128), seq_q=None, seq_kv=None, layout="BNSD",
-                       num_kv_heads=None, scale=1.0):
+                       num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
+                       next_tokens=NO_WINDOW):
     """dK[b, g, rows], dV[b, g, rows] only (fp64), summed over the query heads of
     group g (R3). Each key row needs all query rows that select it."""
     bx, by = int(block_shape[0]), int(block_shape[1])
@@ -316,7 +351,8 @@ def backward_dkdv_rows(dout, q, k, v, out, lse, b, g, rows, mask=None,
         dOm = head_rows(dout, layout, b, h, lq[b], oq)
         Om = head_rows(out, layout, b, h, lq[b], oq)
         L = _lse_rows(lse, layout, b, h, lq[b], oq)
-        M = token_mask_at(None if mask is None else mask[b, h], bx, by, np.arange(lq[b]), t)
+        M = token_mask_at(None if mask is None else mask[b, h], bx, by, np.arange(lq[b]), t,
+                          pre_tokens, next_tokens)
         _, dK, dV = _head_backward(Qm, Kt, Vt, dOm, Om, L, M, scale)
         dk[ok] += dK
         dv[ok] += dV

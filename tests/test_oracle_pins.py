@@ -385,8 +385,8 @@ def test_planted_mistakes_are_caught(kind, monkeypatch):
 def test_planted_block_index_mistake_is_caught(monkeypatch):
     """mask[b, h, j, i] read instead of mask[b, h, i, j]."""
     real = O.token_mask
-    monkeypatch.setattr(O, "token_mask", lambda bm, bx, by, Lq, Lk:
-                        real(None if bm is None else np.asarray(bm).T, bx, by, Lq, Lk))
+    monkeypatch.setattr(O, "token_mask", lambda bm, bx, by, Lq, Lk, *w:
+                        real(None if bm is None else np.asarray(bm).T, bx, by, Lq, Lk, *w))
     with pytest.raises(AssertionError):
         test_backward_matches_sdpa_autograd(2, 2, 40, 40, 8, 8, 8, 1)
 
@@ -423,3 +423,153 @@ def test_token_mask_at_matches_full_expansion():
     np.testing.assert_array_equal(O.token_mask_at(bm, 16, 8, rows, cols), full[rows][:, cols])
     ref = np.repeat(np.repeat(bm != 0, 16, axis=0), 8, axis=1)[:70, :50]   # independent expansion
     np.testing.assert_array_equal(full, ref)
+
+
+# -------------------------------------------- sliding window (reading R8) pins
+def _sdpa_rows(q, k, v, do, tm, scale, G):
+    """torch SDPA + autograd (float64, CPU) per (b, h) on the query rows that
+    have at least one key in the token mask tm [B, N1, S, Skv]; rows without a
+    key are left at 0 (reading R6), which SDPA itself cannot express (NaN)."""
+    B, N1, S, D = q.shape
+    out, dq = np.zeros(q.shape), np.zeros(q.shape)
+    dk, dv = np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(B):
+        for h in range(N1):
+            rows = np.nonzero(tm[b, h].any(axis=1))[0]
+            if len(rows) == 0:
+                continue
+            g = h // G
+            Q = torch.tensor(q[b, h, rows][None, None], requires_grad=True)
+            K = torch.tensor(k[b, g][None, None], requires_grad=True)
+            V = torch.tensor(v[b, g][None, None], requires_grad=True)
+            o = torch.nn.functional.scaled_dot_product_attention(
+                Q, K, V, attn_mask=torch.tensor(tm[b, h][rows][None, None]), scale=scale)
+            o.backward(torch.tensor(do[b, h, rows][None, None]))
+            out[b, h, rows] = o.detach().numpy()[0, 0]
+            dq[b, h, rows] = Q.grad.numpy()[0, 0]
+            dk[b, g] += K.grad.numpy()[0, 0]
+            dv[b, g] += V.grad.numpy()[0, 0]
+    return out, dq, dk, dv
+
+
+@pytest.mark.parametrize("S,Skv", [(37, 37), (29, 50), (50, 29)])
+def test_causal_matches_sdpa_is_causal(S, Skv):
+    """nextTokens = 0, preTokens = no limit, no block mask: torch's is_causal
+    (lower triangle anchored at the top-left corner, also for S != Skv)."""
+    q, k, v, do, _ = _case(N1=4, N2=2, S=S, Skv=Skv, D=8, seed=121)
+    out, lse = O.forward(q, k, v, None, (8, 8), num_kv_heads=2, scale=0.45, next_tokens=0)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, None, (8, 8), num_kv_heads=2, scale=0.45,
+                            next_tokens=0)
+    Q, K, V = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        Q, K.repeat_interleave(2, dim=1), V.repeat_interleave(2, dim=1), is_causal=True,
+        scale=0.45)
+    ref.backward(torch.tensor(do))
+    np.testing.assert_allclose(out, ref.detach().numpy(), rtol=1e-12, atol=1e-13)
+    for a, g in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
+        np.testing.assert_allclose(a, g.numpy(), rtol=1e-10, atol=1e-11)
+
+
+@pytest.mark.parametrize("pre,nxt", [(13, 6), (9, -3), (-2, 5), (0, 0), (3, 40)])
+def test_window_with_blocks_matches_sdpa(pre, nxt):
+    """Window x block mask against SDPA with the token mask built from
+    torch.tril / torch.triu diagonals and np.repeat (not the oracle's formula)."""
+    S, Skv, bx, by = 40, 45, 8, 16
+    q, k, v, do, m = _case(N1=4, N2=2, S=S, Skv=Skv, D=8, bx=bx, by=by, seed=131, p=0.6)
+    blocks = np.repeat(np.repeat(m != 0, bx, axis=2), by, axis=3)[:, :, :S, :Skv]
+    band = torch.ones(S, Skv, dtype=torch.bool).tril(nxt).triu(-pre).numpy()
+    tm = blocks & band[None, None]
+    out, lse = O.forward(q, k, v, m, (bx, by), num_kv_heads=2, scale=0.5, pre_tokens=pre,
+                         next_tokens=nxt)
+    grads = O.backward(do, q, k, v, out, lse, m, (bx, by), num_kv_heads=2, scale=0.5,
+                       pre_tokens=pre, next_tokens=nxt)
+    ref, *rg = _sdpa_rows(q, k, v, do, tm, 0.5, 2)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+    for a, b in zip(grads, rg):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+    keyless = ~tm.any(axis=3)
+    assert np.all(np.isneginf(lse[..., 0][keyless])) and np.all(np.isfinite(lse[..., 0][~keyless]))
+    if pre == 9:   # rows 0..2 see no key of the window at all
+        assert keyless[:, :, :3].all()
+    bo = O.forward_blockrows(q, k, v, m, (bx, by), num_kv_heads=2, scale=0.5, pre_tokens=pre,
+                             next_tokens=nxt)
+    np.testing.assert_allclose(bo[0], out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(np.isneginf(bo[1]), np.isneginf(lse))
+
+
+def test_window_edges_and_no_window():
+    """preTokens >= Lq - 1 and nextTokens >= Lk - 1 reach every pair, so the
+    result equals no window bit for bit; one less on either side drops exactly
+    the corner pair (Lq-1, 0) or (0, Lk-1)."""
+    S, Skv = 24, 30
+    q, k, v, do, m = _case(N1=2, N2=1, S=S, Skv=Skv, D=8, bx=8, by=8, seed=141)
+    kw = dict(num_kv_heads=1, scale=0.4)
+    out, lse = O.forward(q, k, v, m, (8, 8), **kw)
+    base = O.backward(do, q, k, v, out, lse, m, (8, 8), **kw)
+    for pre, nxt in ((S - 1, Skv - 1), (10 ** 6, 10 ** 6), (2 ** 62, 2 ** 62)):
+        o2, l2 = O.forward(q, k, v, m, (8, 8), pre_tokens=pre, next_tokens=nxt, **kw)
+        np.testing.assert_array_equal(o2, out)
+        np.testing.assert_array_equal(l2, lse)
+        for a, b in zip(O.backward(do, q, k, v, out, lse, m, (8, 8), pre_tokens=pre,
+                                   next_tokens=nxt, **kw), base):
+            np.testing.assert_array_equal(a, b)
+    m1 = np.ones_like(m)
+    full = O.token_mask(m1[0, 0], 8, 8, S, Skv)
+    lo = O.token_mask(m1[0, 0], 8, 8, S, Skv, pre_tokens=S - 2, next_tokens=Skv - 1)
+    hi = O.token_mask(m1[0, 0], 8, 8, S, Skv, pre_tokens=S - 1, next_tokens=Skv - 2)
+    assert full.all() and (~lo).sum() == 1 and not lo[S - 1, 0]
+    assert (~hi).sum() == 1 and not hi[0, Skv - 1]
+
+
+def test_tnd_window_restarts_per_sequence():
+    """In TND the window positions count from each sequence's own start: the
+    TND result equals per-sequence BNSD runs with the same window (BNSD itself
+    is pinned to SDPA above)."""
+    lens_q, lens_k = [13, 30, 7], [21, 9, 30]
+    N1, N2, D, bx, by = 4, 2, 8, 8, 8
+    rng = np.random.Generator(np.random.PCG64(151))
+    m = (rng.random((3, N1, 4, 4)) < 0.7).astype(np.uint8)
+    m[:, :, :, 0] = 1
+    qt = _rand((sum(lens_q), N1, D), 152)
+    kt = _rand((sum(lens_k), N2, D), 153)
+    vt = _rand((sum(lens_k), N2, D), 154)
+    dot = _rand((sum(lens_q), N1, D), 155)
+    w = dict(pre_tokens=6, next_tokens=1)
+    out, lse = O.forward(qt, kt, vt, m, (bx, by), lens_q, lens_k, "TND", N2, 0.3, **w)
+    dq, dk, dv = O.backward(dot, qt, kt, vt, out, lse, m, (bx, by), lens_q, lens_k, "TND", N2,
+                            0.3, **w)
+    oq, ok = O.seq_offsets(lens_q), O.seq_offsets(lens_k)
+    to_bnsd = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2))[None]
+    for b in range(3):
+        sl_q, sl_k = slice(oq[b], oq[b + 1]), slice(ok[b], ok[b + 1])
+        o1, l1 = O.forward(to_bnsd(qt[sl_q]), to_bnsd(kt[sl_k]), to_bnsd(vt[sl_k]),
+                           m[b:b + 1], (bx, by), num_kv_heads=N2, scale=0.3, **w)
+        np.testing.assert_allclose(o1[0].transpose(1, 0, 2), out[sl_q], rtol=1e-13, atol=1e-14)
+        g1 = O.backward(to_bnsd(dot[sl_q]), to_bnsd(qt[sl_q]), to_bnsd(kt[sl_k]),
+                        to_bnsd(vt[sl_k]), o1, l1, m[b:b + 1], (bx, by), num_kv_heads=N2,
+                        scale=0.3, **w)
+        for x, y, sl in zip(g1, (dq, dk, dv), (sl_q, sl_k, sl_k)):
+            np.testing.assert_allclose(x[0].transpose(1, 0, 2), y[sl], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("kind", ["swap", "strict", "shifted"])
+def test_planted_window_mistakes_are_caught(kind, monkeypatch):
+    """pre and next exchanged, strict instead of inclusive edges, or the window
+    shifted by one: each fails a window pin."""
+    real = O.window_mask
+
+    def wrong(rows, cols, pre_tokens=O.NO_WINDOW, next_tokens=O.NO_WINDOW):
+        if kind == "swap":
+            return real(rows, cols, next_tokens, pre_tokens)
+        if kind == "strict":
+            return real(rows, cols, pre_tokens - 1, next_tokens - 1)
+        return real(rows, cols, pre_tokens + 1, next_tokens - 1)
+    monkeypatch.setattr(O, "window_mask", wrong)
+    caught = 0
+    for pin in (lambda: test_window_with_blocks_matches_sdpa(13, 6),
+                lambda: test_causal_matches_sdpa_is_causal(37, 37)):
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
+    assert caught >= 1, kind
