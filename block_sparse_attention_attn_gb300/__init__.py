@@ -10,4 +10,4 @@ from .binding import (bsa_grad_workspace_size, bsa_grad, bsa_fwd_workspace_size,
                       BsaError,
                       block_sparse_attention_grad, block_sparse_attention_fwd,
                       block_sparse_attention, BlockSparseAttentionFunction,
-                      load_library, library_path)
+                      load_library, library_path, NO_WINDOW)

@@ -21,6 +21,7 @@ BSA_OK = 0
 BSA_ERR_PARAM_NULLPTR = 161001
 BSA_ERR_PARAM_INVALID = 161002
 BSA_ERR_RUNTIME = 361001
+NO_WINDOW = 2147483647   # preTokens / nextTokens value meaning "no sliding window"
 BSA_ERR_INNER = 561002
 
 _DTYPES = {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3, torch.uint8: 4, torch.bool: 4}
@@ -59,7 +60,7 @@ def load_library():
     lib.bsa_grad.argtypes = [vp, u64, vp, vp]
     lib.bsa_fwd_workspace_size.argtypes = [
         T, T, T, T, P(i64), i64, P(i64), i64, P(i64), i64, ctypes.c_char_p, ctypes.c_char_p,
-        i64, ctypes.c_double, T, T, P(u64), P(vp)]
+        i64, ctypes.c_double, i64, i64, T, T, P(u64), P(vp)]
     lib.bsa_fwd.argtypes = [vp, u64, vp, vp]
     lib.bsa_executor_destroy.argtypes = [vp]
     lib.bsa_executor_set_timing_events.argtypes = [vp, vp, vp]
@@ -159,8 +160,8 @@ def bsa_grad_workspace_size(dout, query, key, value, attention_out, softmax_lse,
                             block_sparse_mask=None, atten_mask=None, block_shape=None,
                             actual_seq_lengths=None, actual_seq_lengths_kv=None,
                             q_layout="BNSD", kv_layout=None, num_key_value_heads=None,
-                            mask_type=0, scale_value=1.0, pre_tokens=2147483647,
-                            next_tokens=2147483647, dq=None, dk=None, dv=None):
+                            mask_type=0, scale_value=1.0, pre_tokens=NO_WINDOW,
+                            next_tokens=NO_WINDOW, dq=None, dk=None, dv=None):
     """First stage of the backward. Returns (workspace_size, Executor)."""
     lib = load_library()
     kv_layout = q_layout if kv_layout is None else kv_layout
@@ -191,7 +192,8 @@ def bsa_grad(workspace: torch.Tensor, workspace_size: int, executor: Executor, s
 def bsa_fwd_workspace_size(query, key, value, block_sparse_mask=None, block_shape=None,
                            actual_seq_lengths=None, actual_seq_lengths_kv=None,
                            q_layout="BNSD", kv_layout=None, num_key_value_heads=None,
-                           scale_value=1.0, attention_out=None, softmax_lse=None):
+                           scale_value=1.0, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW,
+                           attention_out=None, softmax_lse=None):
     lib = load_library()
     kv_layout = q_layout if kv_layout is None else kv_layout
     if num_key_value_heads is None:
@@ -205,7 +207,8 @@ def bsa_fwd_workspace_size(query, key, value, block_sparse_mask=None, block_shap
     _check(lib.bsa_fwd_workspace_size(
         _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ds[3]), bs, nbs, sq, nsq, sk, nsk,
         q_layout.encode(), kv_layout.encode(), int(num_key_value_heads), float(scale_value),
-        _ptr(ds[4]), _ptr(ds[5]), ctypes.byref(ws), ctypes.byref(ex)))
+        int(pre_tokens), int(next_tokens), _ptr(ds[4]), _ptr(ds[5]), ctypes.byref(ws),
+        ctypes.byref(ex)))
     return ws.value, Executor(ex.value, ds)
 
 
@@ -265,9 +268,12 @@ def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_
                                 actual_seq_lengths=None, actual_seq_lengths_kv=None,
                                 layout="BNSD", num_key_value_heads=None, scale_value=None,
                                 dq=None, dk=None, dv=None, workspace=None, stream=None,
-                                deterministic=False):
+                                deterministic=False, pre_tokens=NO_WINDOW,
+                                next_tokens=NO_WINDOW):
     """Both stages; allocates outputs/workspace with torch when not given.
-    Returns (dq, dk, dv, workspace)."""
+    pre_tokens / next_tokens: sliding window (query s and key t of a sequence
+    pair up iff s - pre_tokens <= t <= s + next_tokens; next_tokens=0 is
+    causal). Returns (dq, dk, dv, workspace)."""
     if scale_value is None:
         scale_value = query.shape[-1] ** -0.5
     dq = torch.empty_like(query) if dq is None else dq
@@ -276,7 +282,7 @@ def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_
     size, ex = bsa_grad_workspace_size(
         dout, query, key, value, attention_out, softmax_lse, block_sparse_mask, None,
         block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
-        num_key_value_heads, 0, scale_value, dq=dq, dk=dk, dv=dv)
+        num_key_value_heads, 0, scale_value, pre_tokens, next_tokens, dq=dq, dk=dk, dv=dv)
     if deterministic:
         ex.set_deterministic(True)
     if workspace is None or workspace.numel() < size:
@@ -288,8 +294,10 @@ def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_
 def block_sparse_attention_fwd(query, key, value, block_sparse_mask=None, block_shape=None,
                                actual_seq_lengths=None, actual_seq_lengths_kv=None,
                                layout="BNSD", num_key_value_heads=None, scale_value=None,
-                               out=None, lse=None, workspace=None, stream=None):
-    """Companion forward; returns (out, lse [..., 1] fp32, workspace)."""
+                               out=None, lse=None, workspace=None, stream=None,
+                               pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+    """Companion forward (same sliding window arguments as the backward);
+    returns (out, lse [..., 1] fp32, workspace)."""
     if scale_value is None:
         scale_value = query.shape[-1] ** -0.5
     out = torch.empty_like(query) if out is None else out
@@ -297,7 +305,8 @@ def block_sparse_attention_fwd(query, key, value, block_sparse_mask=None, block_
         lse = torch.empty((*query.shape[:-1], 1), dtype=torch.float32, device=query.device)
     size, ex = bsa_fwd_workspace_size(query, key, value, block_sparse_mask, block_shape,
                                       actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
-                                      num_key_value_heads, scale_value, out, lse)
+                                      num_key_value_heads, scale_value, pre_tokens,
+                                      next_tokens, out, lse)
     if workspace is None or workspace.numel() < size:
         workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=query.device)
     bsa_fwd(workspace, size, ex, stream)
@@ -312,37 +321,42 @@ class BlockSparseAttentionFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
-                actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic):
+                actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic,
+                pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
         if scale_value is None:
             scale_value = query.shape[-1] ** -0.5
         query, key, value = query.contiguous(), key.contiguous(), value.contiguous()
         out, lse, _ = block_sparse_attention_fwd(
             query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
-            actual_seq_lengths_kv, layout, num_key_value_heads, scale_value)
+            actual_seq_lengths_kv, layout, num_key_value_heads, scale_value,
+            pre_tokens=pre_tokens, next_tokens=next_tokens)
         ctx.save_for_backward(query, key, value, out, lse)
         ctx.mask = block_sparse_mask
         ctx.args = (block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout,
-                    num_key_value_heads, scale_value, deterministic)
+                    num_key_value_heads, scale_value, deterministic, pre_tokens, next_tokens)
         return out
 
     @staticmethod
     def backward(ctx, dout):
         query, key, value, out, lse = ctx.saved_tensors
         (block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout, num_key_value_heads,
-         scale_value, deterministic) = ctx.args
+         scale_value, deterministic, pre_tokens, next_tokens) = ctx.args
         dq, dk, dv, ws = block_sparse_attention_grad(
             dout.contiguous(), query, key, value, out, lse, ctx.mask, block_shape,
             actual_seq_lengths, actual_seq_lengths_kv, layout, num_key_value_heads, scale_value,
-            deterministic=deterministic)
+            deterministic=deterministic, pre_tokens=pre_tokens, next_tokens=next_tokens)
         bsa_check_status(ws)
-        return dq, dk, dv, None, None, None, None, None, None, None, None
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None
 
 
 def block_sparse_attention(query, key, value, block_sparse_mask=None, block_shape=None,
                            actual_seq_lengths=None, actual_seq_lengths_kv=None, layout="BNSD",
-                           num_key_value_heads=None, scale_value=None, deterministic=False):
+                           num_key_value_heads=None, scale_value=None, deterministic=False,
+                           pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
     """Differentiable block-sparse attention: Out = softmax(scale*Q K^T over the
-    selected blocks) V; gradients for Q, K and V come from the backward kernels."""
+    selected blocks, inside the sliding window) V; gradients for Q, K and V come
+    from the backward kernels."""
     return BlockSparseAttentionFunction.apply(
         query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
-        actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic)
+        actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic,
+        pre_tokens, next_tokens)

@@ -6,8 +6,9 @@
 // (section 返回值: 161001 for NULL dout/query/key/value/attentionOut or TND
 // without actual sequence lengths, 161002 for unsupported dtype/layout), the
 // parameter table (shapes, dtypes, contiguity, blockShape >= 2 entries > 0,
-// attenMask NULL, maskType 0, pre/nextTokens 2147483647) and the constraints
-// (section 约束说明: N1 % N2 == 0, equal q/kv layouts).
+// attenMask NULL, maskType 0) and the constraints (section 约束说明: N1 % N2 == 0,
+// equal q/kv layouts). preTokens / nextTokens define a sliding window (any
+// pair with preTokens + nextTokens >= 0) instead of being fixed at 2147483647.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -405,6 +406,26 @@ void build_info(bsa_executor* ex) {
   p.n_qtiles = rq / kTile;
 }
 
+// preTokens / nextTokens: any int64 pair whose window overlaps the diagonal
+// (pre + next >= 0; the FlashAttentionScore page asks the two to overlap).
+bsa_status check_window(int64_t pre, int64_t next) {
+  const bool overlap = (pre >= 0 && next >= 0) ||
+                       (pre < 0 && pre != INT64_MIN && next >= -pre) ||
+                       (next < 0 && next != INT64_MIN && pre >= -next);
+  if (!overlap)
+    return fail(BSA_ERR_PARAM_INVALID, "preTokens + nextTokens must be >= 0 (got %lld, %lld)",
+                (long long)pre, (long long)next);
+  return BSA_OK;
+}
+
+// The window limits, clamped, and whether they cut any pair: a window with
+// pre >= Sq - 1 and next >= Skv - 1 (longest sequences) reaches every pair.
+void fill_window(Plan& p, const Geometry& g, int64_t pre, int64_t next) {
+  p.win_pre = std::min(std::max(pre, -kWinClamp), kWinClamp);
+  p.win_next = std::min(std::max(next, -kWinClamp), kWinClamp);
+  p.win = (p.win_pre >= (int64_t)g.Sq - 1 && p.win_next >= (int64_t)g.Skv - 1) ? 0 : 1;
+}
+
 void fill_geometry(Plan& p, const Geometry& g, double scale, int num_sms) {
   p.B = g.B; p.N1 = g.N1; p.N2 = g.N2; p.G = g.G; p.D = g.D;
   p.bx = g.bx; p.by = g.by; p.rb = kTile / g.bx; p.cb = kTile / g.by;
@@ -499,8 +520,7 @@ bsa_status bsa_grad_workspace_size(
   if (atten_mask != nullptr)
     return fail(BSA_ERR_PARAM_INVALID, "attenMaskOptional is not supported: pass NULL");
   if (mask_type != 0) return fail(BSA_ERR_PARAM_INVALID, "maskType must be 0");
-  if (pre_tokens != 2147483647 || next_tokens != 2147483647)
-    return fail(BSA_ERR_PARAM_INVALID, "preTokens/nextTokens must be 2147483647");
+  if (check_window(pre_tokens, next_tokens) != BSA_OK) return BSA_ERR_PARAM_INVALID;
   Geometry g;
   bsa_status st = check_common(query, key, value, block_sparse_mask, block_shape, block_shape_len,
                                actual_seq_lengths, n_seq, actual_seq_lengths_kv, n_seq_kv,
@@ -531,6 +551,7 @@ bsa_status bsa_grad_workspace_size(
   ex->g = g;
   Plan& p = ex->plan;
   fill_geometry(p, g, scale_value, num_sms);
+  fill_window(p, g, pre_tokens, next_tokens);
   build_info(ex);
   ex->q = query->data; ex->k = key->data; ex->v = value->data; ex->dout = dout->data;
   p.q = query->data; p.k = key->data; p.v = value->data; p.dout = dout->data;
@@ -668,6 +689,7 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.col_slots = p.Mk_t; ca.row_slots = p.Mq_t;
   ca.lq = p.lq; ca.lk = p.lk;
   ca.counts = p.colcnt; ca.ptr = p.colptr; ca.out = p.entries; ca.plain = 0;
+  ca.win = p.win; ca.win_pre = p.win_pre; ca.win_next = p.win_next;
   ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
   // The preprocess (bandwidth-bound) runs on a side stream while the mask
   // compaction and the planner (latency-bound, one block) run on `st`.
@@ -820,8 +842,8 @@ bsa_status bsa_fwd_workspace_size(
     const bsa_tensor* block_sparse_mask, const int64_t* block_shape, int64_t block_shape_len,
     const int64_t* actual_seq_lengths, int64_t n_seq, const int64_t* actual_seq_lengths_kv,
     int64_t n_seq_kv, const char* q_layout, const char* kv_layout, int64_t num_key_value_heads,
-    double scale_value, const bsa_tensor* attention_out, const bsa_tensor* softmax_lse,
-    uint64_t* workspace_size, bsa_executor** executor) {
+    double scale_value, int64_t pre_tokens, int64_t next_tokens, const bsa_tensor* attention_out,
+    const bsa_tensor* softmax_lse, uint64_t* workspace_size, bsa_executor** executor) {
   if (query == nullptr || key == nullptr || value == nullptr || attention_out == nullptr ||
       softmax_lse == nullptr || workspace_size == nullptr || executor == nullptr)
     return fail(BSA_ERR_PARAM_NULLPTR, "query, key, value, attentionOut, softmaxLse, "
@@ -833,6 +855,7 @@ bsa_status bsa_fwd_workspace_size(
   if (block_sparse_mask != nullptr && block_sparse_mask->data == nullptr)
     return fail(BSA_ERR_PARAM_NULLPTR, "blockSparseMask with a NULL data pointer");
   *executor = nullptr;
+  if (check_window(pre_tokens, next_tokens) != BSA_OK) return BSA_ERR_PARAM_INVALID;
   Geometry g;
   bsa_status st = check_common(query, key, value, block_sparse_mask, block_shape, block_shape_len,
                                actual_seq_lengths, n_seq, actual_seq_lengths_kv, n_seq_kv,
@@ -850,6 +873,7 @@ bsa_status bsa_fwd_workspace_size(
   ex->g = g;
   Plan& p = ex->plan;
   fill_geometry(p, g, scale_value, num_sms);
+  fill_window(p, g, pre_tokens, next_tokens);
   build_info(ex);
   ex->q = query->data; ex->k = key->data; ex->v = value->data;
   p.q = query->data; p.k = key->data; p.v = value->data;

@@ -666,13 +666,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Lk = p.lk[ii.b];
       const bool t_ok = (ii.jt * 128 + t) < Lk;
       for (int e = ii.e0; e < ii.e1; ++e) {
-        const int sub = entry_sub(p.entries[e]);
+        const int32_t ent = p.entries[e];
+        const int sub = entry_sub(ent);
         const int s_sub = (p.rb == 2) ? wg : 0;
         const int t_sub = (p.cb == 2) ? (t >> 6) : 0;
         // key row t of this thread takes part (inside the key length, in a
         // selected sub-block); query columns past the query length need no
         // test: their lse rows hold +inf, so P is exactly 0 there
         const uint32_t rmask = (t_ok && ((sub >> (s_sub * 2 + t_sub)) & 1)) ? 0xFFFFFFFFu : 0u;
+        // sliding window: when it cuts this tile (the same answer for the whole
+        // CTA), wm0 / wm1 flag the live query columns of this thread's two
+        // 32-column chunks
+        bool wcut = false;
+        uint32_t wm0 = 0u, wm1 = 0u;
+        if (p.win) {
+          const int64_t s0 = (int64_t)entry_it(ent) * 128, t0 = (int64_t)ii.jt * 128;
+          wcut = !win_covers(s0, s0 + 128, t0, t0 + 128, p.win_pre, p.win_next);
+          if (wcut) {
+            const int2 w = win_span(t0 + t, s0 + 64 * wg, -p.win_next, p.win_pre);
+            wm0 = bit_range(w.x, w.y);
+            wm1 = bit_range(w.x - 32, w.y - 32);
+          }
+        }
         const int st = n & 1;
         if (!mbar_wait(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
         if (!mbar_wait(&bars[kSFull], n & 1, abort_flag)) { where = kErrWaitS; break; }
@@ -696,6 +711,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p3 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 3]), p.scale_log2, -l4.w));
             Ppk[16 * c + 2 * j4] = E::pack(p0, p1) & rmask;
             Ppk[16 * c + 2 * j4 + 1] = E::pack(p2, p3) & rmask;
+          }
+          if (wcut) {  // word j holds columns 2j (low half) and 2j + 1 (high half)
+            const uint32_t wm = c ? wm1 : wm0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              Ppk[16 * c + j] &= ((wm >> (2 * j)) & 1u ? 0x0000FFFFu : 0u) |
+                                 ((wm >> (2 * j + 1)) & 1u ? 0xFFFF0000u : 0u);
           }
           uint32_t pk[16];
 #pragma unroll

@@ -107,7 +107,7 @@ __device__ __forceinline__ QItem decode(const Plan& p, int idx) {
 }
 
 // Sub-block bits of key tile jt for query tile it of (b, h); 0 when the tile
-// has no selected block inside the valid range.
+// has no selected block inside the valid range that meets the sliding window.
 __device__ __forceinline__ int q_tile_bits(const Plan& p, int b, int h, int it, int jt, int Lq, int Lk) {
   int bits = 0;
   for (int ri = 0; ri < p.rb; ++ri) {
@@ -120,6 +120,10 @@ __device__ __forceinline__ int q_tile_bits(const Plan& p, int b, int h, int it, 
       if (p.has_mask)
         on = (i < p.Mq && j < p.Mk) &&
              p.mask[(int64_t)b * p.mask_sb + (int64_t)h * p.mask_sh + (int64_t)i * p.mask_si + j] != 0;
+      if (on && p.win)
+        on = win_meets((int64_t)i * p.bx, min((int64_t)(i + 1) * p.bx, (int64_t)Lq),
+                       (int64_t)j * p.by, min((int64_t)(j + 1) * p.by, (int64_t)Lk), p.win_pre,
+                       p.win_next);
       if (on) bits |= 1 << (ri * 2 + cj);
     }
   }
@@ -442,7 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars[kSFull], m & 1, abort_flag)) { where = kErrWaitS; break; }
         if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
         tc_fence_after();
-        const int t_lim = Lk - jt * 128;
+        // live key columns [t_lo, t_hi): inside the key length and the window
+        int t_lo = 0, t_hi = Lk - jt * 128;
+        if (p.win) {
+          const int2 w = win_span(srow, (int64_t)jt * 128, -p.win_pre, p.win_next);
+          t_lo = w.x;
+          t_hi = min(t_hi, w.y);
+        }
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t x[32], y[32];
@@ -456,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 2; ++u) {
               const int t = 32 * c + 2 * k + u;
               const int t_sub = p.cb == 2 ? (t >> 6) : 0;
-              const bool on = s_ok && t < t_lim && ((bits >> (s_sub * 2 + t_sub)) & 1);
+              const bool on = s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1);
               // P rounded to the operand type, as in the dV/dK kernel
               const float pv =
                   on ? E::round(ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)))

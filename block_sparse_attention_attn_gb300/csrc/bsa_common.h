@@ -62,6 +62,43 @@ __host__ __device__ inline int entry_it(int32_t e) { return e & 0xFFFFF; }
 __host__ __device__ inline int entry_hl(int32_t e) { return (e >> 20) & 0xFF; }
 __host__ __device__ inline int entry_sub(int32_t e) { return (int)(((uint32_t)e) >> 28); }
 
+// Sliding window (preTokens / nextTokens rows of the parameter table; left and
+// right window edges as on the FlashAttentionScore page): query s and key t of
+// one sequence, both counted from that sequence's first token, pair up iff
+// s - pre <= t <= s + next. The host clamps pre and next to +-2^40 (positions
+// stay below 2^31, so the clamp changes no pair and int64 never overflows).
+constexpr int64_t kWinClamp = int64_t(1) << 40;
+
+// The rectangle of positions [s0, s1) x [t0, t1) (both non-empty) holds at
+// least one pair of the window.
+__host__ __device__ inline bool win_meets(int64_t s0, int64_t s1, int64_t t0, int64_t t1,
+                                          int64_t pre, int64_t next) {
+  return t0 - (s1 - 1) <= next && (t1 - 1) - s0 >= -pre;
+}
+// Every pair of the rectangle lies in the window.
+__host__ __device__ inline bool win_covers(int64_t s0, int64_t s1, int64_t t0, int64_t t1,
+                                           int64_t pre, int64_t next) {
+  return (t1 - 1) - s0 <= next && t0 - (s1 - 1) >= -pre;
+}
+// Positions x of the other axis with pos + dlo <= x <= pos + dhi, as the
+// half-open range [lo, hi) of offsets from `base`, clipped to [0, 128]
+// (a query row: dlo = -pre, dhi = next; a key row: dlo = -next, dhi = pre).
+__host__ __device__ inline int2 win_span(int64_t pos, int64_t base, int64_t dlo, int64_t dhi) {
+  int64_t lo = pos + dlo - base, hi = pos + dhi - base + 1;
+  lo = lo < 0 ? 0 : (lo > 128 ? 128 : lo);
+  hi = hi < 0 ? 0 : (hi > 128 ? 128 : hi);
+  return make_int2((int)lo, (int)hi);
+}
+
+// Bits lo .. hi-1 of a 32-bit word (the part of [lo, hi) inside [0, 32)).
+__host__ __device__ inline uint32_t bit_range(int lo, int hi) {
+  lo = lo < 0 ? 0 : lo;
+  hi = hi > 32 ? 32 : hi;
+  if (hi <= lo) return 0u;
+  const uint32_t below_hi = hi == 32 ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  return below_hi & ~((1u << lo) - 1u);
+}
+
 // Everything the kernels need, passed by value.
 struct Plan {
   // problem
@@ -90,6 +127,8 @@ struct Plan {
   int dq_vec, dkv_vec;                  // outputs allow 16-byte row stores
   int dkv_tma;                          // dK / dV written by TMA stores (BwdMaps dk, dv)
   int det;                              // deterministic dQ: separate query-tile pass, no reduce-adds
+  int win;                              // a sliding window cuts some pair of the problem
+  int64_t win_pre, win_next;            // its limits (clamped to +-kWinClamp)
   // per-batch info in the workspace (int32 [B] each)
   const int* lq;
   const int* lk;

@@ -101,7 +101,8 @@ __device__ __forceinline__ FItem decode(const Plan& p, int idx) {
   return r;
 }
 
-// Sub-block bits of key tile jt for query tile `it` of (b, h).
+// Sub-block bits of key tile jt for query tile `it` of (b, h): selected,
+// inside the valid range and meeting the sliding window.
 __device__ __forceinline__ int fwd_tile_bits(const Plan& p, int b, int h, int it, int jt, int Lq,
                                              int Lk) {
   int bits = 0;
@@ -115,6 +116,10 @@ __device__ __forceinline__ int fwd_tile_bits(const Plan& p, int b, int h, int it
       if (p.has_mask)
         on = (i < p.Mq && j < p.Mk) &&
              p.mask[(int64_t)b * p.mask_sb + (int64_t)h * p.mask_sh + (int64_t)i * p.mask_si + j] != 0;
+      if (on && p.win)
+        on = win_meets((int64_t)i * p.bx, min((int64_t)(i + 1) * p.bx, (int64_t)Lq),
+                       (int64_t)j * p.by, min((int64_t)(j + 1) * p.by, (int64_t)Lk), p.win_pre,
+                       p.win_next);
       if (on) bits |= 1 << (ri * 2 + cj);
     }
   }
@@ -387,12 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = sb ? kColS1 : kColS0;
         if (!mbar_wait(&bars[kSFull0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
-        const int t_lim = Lk - jt * 128;
+        // live columns [t_lo, t_hi): inside the key length and the sliding window
+        int t_lo = 0, t_hi = Lk - jt * 128;
+        if (p.win) {
+          const int2 w = win_span((int64_t)fi.it * 128 + s, (int64_t)jt * 128, -p.win_pre, p.win_next);
+          t_lo = w.x;
+          t_hi = min(t_hi, w.y);
+        }
         const int s_sub = p.rb == 2 ? (s >> 6) : 0;
-        // column c is live when t < t_lim and its key sub-block bit is set
+        // column t is live when t_lo <= t < t_hi and its key sub-block bit is set
         auto col_on = [&](int t) -> bool {
           const int t_sub = p.cb == 2 ? (t >> 6) : 0;
-          return s_ok && t < t_lim && ((bits >> (s_sub * 2 + t_sub)) & 1);
+          return s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1);
         };
         float mx = -INFINITY;
 #pragma unroll

@@ -21,7 +21,8 @@ namespace bsa {
 // compaction
 // --------------------------------------------------------------------------
 // Sub-block bits of tile (it, jt) for (b, h): bit (ri*2+cj) set when block
-// (it*rb+ri, jt*cb+cj) lies inside the valid range and is selected.
+// (it*rb+ri, jt*cb+cj) lies inside the valid range, is selected and (with a
+// sliding window) holds at least one pair of the window.
 __device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int it, int jt,
                                          int Lq, int Lk) {
   int bits = 0;
@@ -36,6 +37,10 @@ __device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int
         on = (i < a.Mq && j < a.Mk) &&
              a.mask[(int64_t)b * a.sb + (int64_t)h * a.sh + (int64_t)i * a.si + j] != 0;
       }
+      if (on && a.win)
+        on = win_meets((int64_t)i * a.bx, min((int64_t)(i + 1) * a.bx, (int64_t)Lq),
+                       (int64_t)j * a.by, min((int64_t)(j + 1) * a.by, (int64_t)Lk), a.win_pre,
+                       a.win_next);
       if (on) bits |= 1 << (ri * 2 + cj);
     }
   }

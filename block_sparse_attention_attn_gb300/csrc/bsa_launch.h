@@ -27,6 +27,8 @@ struct CompactArgs {
   const int* ptr;      // fill pass: exclusive scan of counts
   int32_t* out;        // fill pass output
   int plain;           // 1: store the tile index only; 0: packed entry
+  int win;             // drop sub-blocks outside the sliding window (Plan::win)
+  int64_t win_pre, win_next;
   float* zero;            // fill pass: optional fp32 region cleared first (or null)
   const int* zero_count;  // device: number of zero_per-float units to clear
   int zero_per;           // floats per unit, a multiple of 4

@@ -88,7 +88,16 @@ typedef struct bsa_executor bsa_executor; /* opaque, host side */
  *   q_layout, kv_layout        : "BNSD" or "TND"; must be equal.
  *   num_key_value_heads        : N2; N1 % N2 == 0; query head h uses key head
  *                                h / (N1/N2), and dK/dV sum over the group.
- *   mask_type                  : must be 0.   pre_tokens, next_tokens: must be 2147483647.
+ *   mask_type                  : must be 0.
+ *   pre_tokens, next_tokens    : sliding window (parameter table rows preTokens /
+ *                                nextTokens; window edges as on the
+ *                                FlashAttentionScore page, 参数说明): query s and
+ *                                key t of one sequence, both counted from that
+ *                                sequence's first token, take part only if
+ *                                s - pre_tokens <= t <= s + next_tokens (on top of
+ *                                the block mask). 2147483647 for both = no window;
+ *                                next_tokens = 0 = causal (top-left aligned).
+ *                                pre_tokens + next_tokens must be >= 0.
  *   scale_value                : the scale (typically D^-0.5).
  *   dq, dk, dv                 : outputs with the shapes of query/key/value, same
  *                                dtype; any strides (non-contiguous allowed).
@@ -121,15 +130,17 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
  * over the selected blocks) * V and softmaxLse = natural-log logsumexp of the
  * scaled selected scores (page formulas 计算公式, forward part; online-softmax
  * update as in the FlashAttentionScore page, section 实现原理). Arguments as in
- * bsa_grad_workspace_size. Query rows with no selected key (and BNSD padding
- * rows) get Out = 0 and lse = -inf. Out has the dtype of query, lse is F32. */
+ * bsa_grad_workspace_size (pre_tokens / next_tokens: the same sliding window).
+ * Query rows with no selected key inside the window (and BNSD padding rows)
+ * get Out = 0 and lse = -inf. Out has the dtype of query, lse is F32. */
 bsa_status bsa_fwd_workspace_size(
     const bsa_tensor* query, const bsa_tensor* key, const bsa_tensor* value,
     const bsa_tensor* block_sparse_mask, const int64_t* block_shape, int64_t block_shape_len,
     const int64_t* actual_seq_lengths, int64_t n_seq,
     const int64_t* actual_seq_lengths_kv, int64_t n_seq_kv,
     const char* q_layout, const char* kv_layout, int64_t num_key_value_heads,
-    double scale_value, const bsa_tensor* attention_out, const bsa_tensor* softmax_lse,
+    double scale_value, int64_t pre_tokens, int64_t next_tokens,
+    const bsa_tensor* attention_out, const bsa_tensor* softmax_lse,
     uint64_t* workspace_size, bsa_executor** executor);
 
 bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* executor,

@@ -30,10 +30,11 @@ def host_inputs(w, pad_fill=None):
     return ts
 
 
-def oracle_forward(w, q, k, v, blockrows=False):
+def oracle_forward(w, q, k, v, blockrows=False, **window):
+    """The oracle's (out, lse); ``window``: pre_tokens / next_tokens."""
     fn = O.forward_blockrows if blockrows else O.forward
     out, lse = fn(f64(q), f64(k), f64(v), w.mask, (w.bx, w.by), w.seq_q, w.seq_kv, w.layout,
-                  w.N2, w.scale)
+                  w.N2, w.scale, **window)
     return out, lse
 
 

@@ -63,6 +63,13 @@ def test_valid_arguments_reach_the_device_query(lib):
     assert st == (0 if torch.cuda.is_available() else B.BSA_ERR_RUNTIME)
 
 
+@pytest.mark.parametrize("pre,nxt", [(1024, 0), (-3, 5), (7, -7), (2 ** 63 - 1, 2 ** 63 - 1),
+                                     (0, 0)])
+def test_windows_that_overlap_the_diagonal_are_accepted(lib, pre, nxt):
+    st = _status(**_grad_args(), pre_tokens=pre, next_tokens=nxt)
+    assert st == (0 if torch.cuda.is_available() else B.BSA_ERR_RUNTIME)
+
+
 def test_null_required_tensors(lib):
     for name in ("dout", "query", "key", "value", "attention_out"):
         kw = _grad_args()
@@ -77,7 +84,8 @@ def test_tnd_without_lengths_is_nullptr(lib):
 
 @pytest.mark.parametrize("change", [
     dict(q_layout="BSND"), dict(kv_layout="TND"), dict(mask_type=1),
-    dict(pre_tokens=1024), dict(next_tokens=0), dict(block_shape=[128]),
+    dict(pre_tokens=-5, next_tokens=4), dict(pre_tokens=3, next_tokens=-10),
+    dict(pre_tokens=-(2 ** 63), next_tokens=2 ** 63 - 1), dict(block_shape=[128]),
     dict(block_shape=[0, 128]), dict(block_shape=[96, 128]), dict(num_key_value_heads=3),
 ])
 def test_invalid_scalars(lib, change):
