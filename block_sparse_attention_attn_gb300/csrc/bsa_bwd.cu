@@ -179,7 +179,9 @@ __device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
   return it;
 }
 
-template <int D, int DT>
+// WIN: instantiated with the sliding-window code (Plan::win set); the plain
+// instance carries none of it.
+template <int D, int DT, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -679,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 32-column chunks
         bool wcut = false;
         uint32_t wm0 = 0u, wm1 = 0u;
-        if (p.win) {
+        if (WIN) {
           const int64_t s0 = (int64_t)entry_it(ent) * 128, t0 = (int64_t)ii.jt * 128;
           wcut = !win_covers(s0, s0 + 128, t0, t0 + 128, p.win_pre, p.win_next);
           if (wcut) {
@@ -990,17 +992,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DT>
+template <int D, int DT, bool WIN>
 cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
   const size_t smem = Smem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd<D, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_bwd<D, DT, WIN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int grid = p.num_sms;
   if (p.max_items < grid) grid = p.max_items;
   if (grid < 1) grid = 1;
-  k_bwd<D, DT><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, m.dk, m.dv, p);
+  k_bwd<D, DT, WIN><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, m.dk, m.dv, p);
   return cudaGetLastError();
+}
+
+template <bool WIN>
+cudaError_t launch_w(const Plan& p, const BwdMaps& m, cudaStream_t st) {
+  if (p.dtype == kDtBF16)
+    return p.D == 128 ? launch_t<128, kDtBF16, WIN>(p, m, st) : launch_t<64, kDtBF16, WIN>(p, m, st);
+  return p.D == 128 ? launch_t<128, kDtF16, WIN>(p, m, st) : launch_t<64, kDtF16, WIN>(p, m, st);
 }
 
 }  // namespace
@@ -1008,9 +1017,7 @@ cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
 size_t bwd_smem_bytes(int D) { return D == 128 ? Smem<128>::kBytes : Smem<64>::kBytes; }
 
 cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st) {
-  if (p.dtype == kDtBF16)
-    return p.D == 128 ? launch_t<128, kDtBF16>(p, m, st) : launch_t<64, kDtBF16>(p, m, st);
-  return p.D == 128 ? launch_t<128, kDtF16>(p, m, st) : launch_t<64, kDtF16>(p, m, st);
+  return p.win ? launch_w<true>(p, m, st) : launch_w<false>(p, m, st);
 }
 
 }  // namespace bsa
