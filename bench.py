@@ -178,7 +178,7 @@ def make_inputs(w, dev):
     out, lse, fws = bsa.block_sparse_attention_fwd(q, k, v, block_sparse_mask=mask,
                                                  block_shape=[w.bx, w.by], layout=w.layout,
                                                  num_key_value_heads=w.N2, scale_value=w.scale,
-                                                 **seq)
+                                                 **seq, **w.window_kw())
     bsa.bsa_check_status(fws)
     return dict(dout=dout, query=q, key=k, value=v, attention_out=out, softmax_lse=lse,
                 block_sparse_mask=mask), seq
@@ -193,7 +193,7 @@ def grad_executor(w, t, seq, dq, dk, dv):
         t["dout"], t["query"], t["key"], t["value"], t["attention_out"], t["softmax_lse"],
         t["block_sparse_mask"], None, [w.bx, w.by], seq["actual_seq_lengths"],
         seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, 0, w.scale,
-        dq=dq, dk=dk, dv=dv)
+        w.pre_tokens, w.next_tokens, dq=dq, dk=dk, dv=dv)
     if DETERMINISTIC:
         ex.set_deterministic(True)
     return size, ex
@@ -297,7 +297,8 @@ def bench_ours(args, rank, world, local):
                    "active_blocks": summ["active_blocks"], "density": round(summ["density"], 4),
                    "gflop_per_step": round(flops / 1e9, 2), "parallelism": f"replicas x{world}",
                    "l2": "flushed (512 MB write) before every timed step",
-                   "dq_mode": "deterministic (query-tile pass)" if DETERMINISTIC else "fp32 reduce-add"},
+                   "dq_mode": "deterministic (query-tile pass)" if DETERMINISTIC else "fp32 reduce-add",
+                   "window": ([w.pre_tokens, w.next_tokens] if w.windowed() else None)},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -339,14 +340,14 @@ def _oracle_sample(w, heads, S):
             .to(dt).to(torch.float64).numpy()
     q, dout, out = rnd(heads), rnd(heads), rnd(heads) * 0.1
     k, v = rnd(g_heads), rnd(g_heads)
+    from block_sparse_attention_attn_gb300.workloads import Workload
     mask = None if w.mask is None else w.mask[:1, :heads, :-(-S // w.bx), :-(-S // w.by)]
     lse = np.full((1, heads, S, 1), math.log(S) + 2.0)
-    kw = dict(mask=mask, block_shape=(w.bx, w.by), num_kv_heads=g_heads, scale=w.scale)
-    if mask is None:
-        nb = heads * (-(-S // w.bx)) * (-(-S // w.by))
-    else:
-        nb = int(np.count_nonzero(mask))
-    return (dout, q, k, v, out, lse), kw, 10.0 * w.bx * w.by * w.D * nb
+    kw = dict(mask=mask, block_shape=(w.bx, w.by), num_kv_heads=g_heads, scale=w.scale,
+              **w.window_kw())
+    sample = Workload(w.name, "BNSD", w.dtype, 1, heads, g_heads, w.D, w.bx, w.by, [S], [S], S, S,
+                      w.scale, mask, **w.window_kw())
+    return (dout, q, k, v, out, lse), kw, sample.flops()
 
 
 def cpu_baseline(w, target_s=12.0):

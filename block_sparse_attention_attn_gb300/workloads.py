@@ -24,6 +24,10 @@ w4    BNSD bf16 B1 N8 Nkv8 S65536 D128, 128x128, top-k style rows: the
       diagonal, block 0 and 14 uniform picks from the earlier blocks
 ====  ==========================================================================
 
+With a sliding window (preTokens / nextTokens): ``w2causal`` is w2 with
+nextTokens = 0 (token-level causal inside the diagonal blocks), ``w1causal``
+is w1dense with nextTokens = 0 (dense causal attention).
+
 Values are N(0, 1) (w3: standard deviation 0.5), drawn from numpy's PCG64 and
 rounded to the input dtype with round-to-nearest-even.
 """
@@ -35,7 +39,9 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "make_workload", "normal", "random_mask",
-           "ceil_div"]
+           "ceil_div", "NO_WINDOW", "window_pairs"]
+
+NO_WINDOW = 2147483647   # preTokens / nextTokens value of "no sliding window"
 
 
 def ceil_div(a: int, b: int) -> int:
@@ -69,6 +75,14 @@ class Workload:
     mask: Optional[np.ndarray]  # uint8 [B, N1, ceil(Sq/bx), ceil(Skv/by)] or None
     std: float = 1.0
     seed: int = 0
+    pre_tokens: int = NO_WINDOW     # sliding window: query s sees keys
+    next_tokens: int = NO_WINDOW    # s - pre_tokens .. s + next_tokens
+
+    def windowed(self) -> bool:
+        return not (self.pre_tokens >= self.Sq - 1 and self.next_tokens >= self.Skv - 1)
+
+    def window_kw(self) -> dict:
+        return dict(pre_tokens=self.pre_tokens, next_tokens=self.next_tokens)
 
     @property
     def Mq(self) -> int:
@@ -93,21 +107,39 @@ class Workload:
             return (self.B, self.N1, self.Sq, 1)
         return (int(sum(self.seq_q)), self.N1, 1)
 
+    def _selected_per_block(self, b):
+        """[mq, mk] number of query heads selecting each block of batch b."""
+        mq = ceil_div(self.seq_q[b], self.bx)
+        mk = ceil_div(self.seq_kv[b], self.by)
+        if self.mask is None:
+            return np.full((mq, mk), self.N1, dtype=np.int64)
+        return np.count_nonzero(self.mask[b, :, :mq, :mk], axis=0).astype(np.int64)
+
     def active_blocks(self) -> int:
-        """Active blocks inside the valid range, summed over batch and q-heads."""
+        """Active blocks inside the valid range (and meeting the window),
+        summed over batch and q-heads."""
         n = 0
         for b in range(self.B):
-            mq = ceil_div(self.seq_q[b], self.bx)
-            mk = ceil_div(self.seq_kv[b], self.by)
-            if self.mask is None:
-                n += self.N1 * mq * mk
-            else:
-                n += int(np.count_nonzero(self.mask[b, :, :mq, :mk]))
+            sel = self._selected_per_block(b)
+            if self.windowed():
+                sel = sel * (window_pairs(self.seq_q[b], self.seq_kv[b], self.bx, self.by,
+                                          self.pre_tokens, self.next_tokens) > 0)
+            n += int(sel.sum())
         return n
 
     def flops(self) -> float:
-        """Algorithmic backward FLOPs: 10*bx*by*D per active block per q-head."""
-        return 10.0 * self.bx * self.by * self.D * self.active_blocks()
+        """Algorithmic backward FLOPs: 10*D per (query, key) pair that takes
+        part, per q-head (5 products of 2*D each: S, dP, dV, dQ, dK). Without a
+        window a selected block counts as bx*by pairs (tail blocks included);
+        with one only the pairs inside the window and the lengths count."""
+        if not self.windowed():
+            return 10.0 * self.bx * self.by * self.D * self.active_blocks()
+        pairs = 0
+        for b in range(self.B):
+            wp = window_pairs(self.seq_q[b], self.seq_kv[b], self.bx, self.by,
+                              self.pre_tokens, self.next_tokens)
+            pairs += int((self._selected_per_block(b) * wp).sum())
+        return 10.0 * self.D * pairs
 
     def tensors(self, seed: Optional[int] = None):
         """(dout, q, k, v) as float32 numpy arrays of the layout's shapes.
@@ -122,6 +154,21 @@ class Workload:
         v = normal(rng, self.kv_shape(), self.std)
         dout = normal(rng, self.q_shape(), self.std)
         return dout, q, k, v
+
+
+def window_pairs(lq, lk, bx, by, pre, nxt):
+    """[ceil(lq/bx), ceil(lk/by)] int64: per block, the (s, t) pairs with s < lq,
+    t < lk and s - pre <= t <= s + nxt (geometry for FLOP counting)."""
+    mq, mk = ceil_div(lq, bx), ceil_div(lk, by)
+    s = np.arange(lq, dtype=np.int64)[:, None]
+    t0 = (np.arange(mk, dtype=np.int64) * by)[None, :]
+    t1 = np.minimum(t0 + by, lk) - 1
+    lo = np.maximum(t0, s - min(int(pre), 1 << 40))
+    hi = np.minimum(t1, s + min(int(nxt), 1 << 40))
+    per_row = np.maximum(hi - lo + 1, 0)                       # [lq, mk]
+    pad = mq * bx - lq
+    per_row = np.concatenate([per_row, np.zeros((pad, mk), np.int64)])
+    return per_row.reshape(mq, bx, mk).sum(axis=1)
 
 
 def random_mask(rng, B, N, Mq, Mk, p, diag=True):
@@ -205,6 +252,12 @@ def _w4():
                     D ** -0.5, m, seed=2004)
 
 
+def _causal(w, name):
+    w.name = name
+    w.next_tokens = 0
+    return w
+
+
 WORKLOADS = {
     "w0": _w0,
     "w1": _w1,
@@ -212,6 +265,8 @@ WORKLOADS = {
     "w2": _w2,
     "w3": _w3,
     "w4": _w4,
+    "w2causal": lambda: _causal(_w2(), "w2causal"),
+    "w1causal": lambda: _causal(_w1(dense=True), "w1causal"),
 }
 
 
@@ -221,7 +276,8 @@ def make_workload(name: str) -> Workload:
 
 def small_workload(layout="BNSD", dtype="bf16", B=1, N1=2, N2=1, D=64, bx=64, by=64,
                    seq_q=(200,), seq_kv=(200,), Sq=None, Skv=None, p=0.5, seed=7,
-                   scale=None, dense=False, std=1.0, name="small") -> Workload:
+                   scale=None, dense=False, std=1.0, name="small", pre_tokens=NO_WINDOW,
+                   next_tokens=NO_WINDOW) -> Workload:
     """A small seeded case for parity tests (ragged tails, GQA, both layouts)."""
     seq_q, seq_kv = list(seq_q), list(seq_kv)
     assert len(seq_q) == B and len(seq_kv) == B
@@ -231,7 +287,8 @@ def small_workload(layout="BNSD", dtype="bf16", B=1, N1=2, N2=1, D=64, bx=64, by
     Mq, Mk = ceil_div(Sq, bx), ceil_div(Skv, by)
     m = None if dense else random_mask(rng, B, N1, Mq, Mk, p)
     return Workload(name, layout, dtype, B, N1, N2, D, bx, by, seq_q, seq_kv, Sq, Skv,
-                    D ** -0.5 if scale is None else scale, m, std=std, seed=seed + 1)
+                    D ** -0.5 if scale is None else scale, m, std=std, seed=seed + 1,
+                    pre_tokens=pre_tokens, next_tokens=next_tokens)
 
 
 def workload_summary(w: Workload) -> dict:
