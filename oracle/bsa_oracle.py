@@ -33,13 +33,13 @@ R4  Only tokens below the per-batch actual lengths count; mask bits of blocks
     starting at or beyond them are ignored. Output rows at or beyond the actual
     length (BNSD padding) are 0.
 R5  Inside a selected block every token pair takes part unless the sliding
-    window of R8 excludes it (no other token-level mask: attenMaskOptional must
+    window of R18 excludes it (no other token-level mask: attenMaskOptional must
     be null and maskType 0).
 R6  A query row with no selected key has Out = 0 and lse = -inf in the forward
     and contributes nothing in the backward (its dQ row is 0).
 R7  In TND, actualSeqLengths are per-batch counts; batch b starts at the
     exclusive prefix sum of the counts.
-R8  preTokens / nextTokens (parameter table rows preTokens, nextTokens: how
+R18 preTokens / nextTokens (parameter table rows preTokens, nextTokens: how
     many earlier / later tokens a token may attend to; FlashAttentionScore
     page, 参数说明: left / right edge of the sliding window, and 约束说明: the
     two must overlap). Query s and key t of one sequence, both counted from 0
@@ -59,7 +59,7 @@ __all__ = ["token_mask", "token_mask_at", "window_mask", "head_rows", "forward",
            "forward_blockrows", "backward", "backward_dq_rows", "backward_dkdv_rows",
            "compact_mask", "seq_offsets", "NO_WINDOW"]
 
-NO_WINDOW = 2147483647   # preTokens / nextTokens value for "no sliding window" (R8)
+NO_WINDOW = 2147483647   # preTokens / nextTokens value for "no sliding window" (R18)
 
 
 # --------------------------------------------------------------------------
@@ -94,7 +94,7 @@ def _lse_rows(lse, layout, b, h, length, offsets):
 def window_mask(rows, cols, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
     """[len(rows), len(cols)] bool: query position s = rows[i] and key position
     t = cols[j] (both counted from the start of their sequence) satisfy
-    s - preTokens <= t <= s + nextTokens (reading R8)."""
+    s - preTokens <= t <= s + nextTokens (reading R18)."""
     s = np.asarray(rows, dtype=np.int64)[:, None]
     t = np.asarray(cols, dtype=np.int64)[None, :]
     # |t - s| < 2^31, so limits beyond +-2^40 act as no limit; clipping them
@@ -108,7 +108,7 @@ def token_mask(block_mask, bx, by, Lq, Lk, pre_tokens=NO_WINDOW, next_tokens=NO_
     """Token-level [Lq, Lk] bool mask of one (b, h): pair (s, t) takes part iff
     the block (s // bx, t // by) is selected (parameter table,
     blockSparseMaskOptional; ``None`` = every block) and (s, t) lies in the
-    sliding window (R8)."""
+    sliding window (R18)."""
     return token_mask_at(block_mask, bx, by, np.arange(Lq), np.arange(Lk),
                          pre_tokens, next_tokens)
 

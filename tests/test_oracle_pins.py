@@ -425,7 +425,7 @@ def test_token_mask_at_matches_full_expansion():
     np.testing.assert_array_equal(full, ref)
 
 
-# -------------------------------------------- sliding window (reading R8) pins
+# -------------------------------------------- sliding window (reading R18) pins
 def _sdpa_rows(q, k, v, do, tm, scale, G):
     """torch SDPA + autograd (float64, CPU) per (b, h) on the query rows that
     have at least one key in the token mask tm [B, N1, S, Skv]; rows without a
