@@ -33,8 +33,7 @@ R4  Only tokens below the per-batch actual lengths count; mask bits of blocks
     starting at or beyond them are ignored. Output rows at or beyond the actual
     length (BNSD padding) are 0.
 R5  Inside a selected block every token pair takes part unless the sliding
-    window of R18 excludes it (no other token-level mask: attenMaskOptional must
-    be null and maskType 0).
+    window of R18 or the token mask of R19 excludes it.
 R6  A query row with no selected key has Out = 0 and lse = -inf in the forward
     and contributes nothing in the backward (its dQ row is 0).
 R7  In TND, actualSeqLengths are per-batch counts; batch b starts at the
@@ -50,6 +49,14 @@ R18 preTokens / nextTokens (parameter table rows preTokens, nextTokens: how
     value the page's own build accepts) is no window for any sequence shorter
     than 2^31. nextTokens = 0 with preTokens = 2147483647 is the causal
     (lower-triangular, top-left aligned) mask.
+R19 attenMaskOptional (parameter table: the atten_mask of the formula
+    S = Mask(scale*Q*K^T, atten_mask), BOOL, 2 dimensions; FlashAttentionScore
+    page, 参数说明 and 实现原理: a true entry masks the position out, a false one
+    keeps it). A 2-D [maxSq, maxSkv] matrix shared by every batch and head,
+    indexed like the window by the positions s, t counted from each
+    sequence's start; pair (s, t) takes part iff atten_mask[s, t] == 0, on top
+    of the block mask and the window. maskType 0 = no token mask (attenMask
+    absent), maskType 1 = the given attenMask.
 """
 from __future__ import annotations
 
@@ -104,16 +111,18 @@ def window_mask(rows, cols, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
     return (t >= s - pre) & (t <= s + nxt)
 
 
-def token_mask(block_mask, bx, by, Lq, Lk, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+def token_mask(block_mask, bx, by, Lq, Lk, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW,
+               atten_mask=None):
     """Token-level [Lq, Lk] bool mask of one (b, h): pair (s, t) takes part iff
     the block (s // bx, t // by) is selected (parameter table,
-    blockSparseMaskOptional; ``None`` = every block) and (s, t) lies in the
-    sliding window (R18)."""
+    blockSparseMaskOptional; ``None`` = every block), (s, t) lies in the
+    sliding window (R18) and atten_mask[s, t] is 0 (R19; ``None`` = no mask)."""
     return token_mask_at(block_mask, bx, by, np.arange(Lq), np.arange(Lk),
-                         pre_tokens, next_tokens)
+                         pre_tokens, next_tokens, atten_mask)
 
 
-def token_mask_at(block_mask, bx, by, rows, cols, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+def token_mask_at(block_mask, bx, by, rows, cols, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW,
+                  atten_mask=None):
     """The entries [rows x cols] of :func:`token_mask` only (same definition,
     evaluated on the requested query rows and key columns)."""
     rows, cols = np.asarray(rows), np.asarray(cols)
@@ -122,7 +131,10 @@ def token_mask_at(block_mask, bx, by, rows, cols, pre_tokens=NO_WINDOW, next_tok
     else:
         bm = np.asarray(block_mask) != 0
         sel = bm[(rows // bx)[:, None], (cols // by)[None, :]]
-    return sel & window_mask(rows, cols, pre_tokens, next_tokens)
+    sel = sel & window_mask(rows, cols, pre_tokens, next_tokens)
+    if atten_mask is not None:
+        sel = sel & (np.asarray(atten_mask)[rows[:, None], cols[None, :]] == 0)
+    return sel
 
 
 def _dims(q, k, layout):
@@ -165,7 +177,7 @@ def _head_forward(Qm, Km, Vm, M, scale):
 
 def forward(q, k, v, mask=None, block_shape=(128, 128), seq_q=None, seq_kv=None,
             layout="BNSD", num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
-            next_tokens=NO_WINDOW):
+            next_tokens=NO_WINDOW, atten_mask=None):
     """Plain dense-with-mask forward. Returns (out, lse) in the layout's shapes
     (lse with the trailing 1), fp64. Padding rows: out 0, lse -inf (R4, R6)."""
     bx, by = int(block_shape[0]), int(block_shape[1])
@@ -185,7 +197,7 @@ def forward(q, k, v, mask=None, block_shape=(128, 128), seq_q=None, seq_kv=None,
             Km = head_rows(k, layout, b, g, lk[b], okv)
             Vm = head_rows(v, layout, b, g, lk[b], okv)
             M = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b],
-                           pre_tokens, next_tokens)
+                           pre_tokens, next_tokens, atten_mask)
             o, l = _head_forward(Qm, Km, Vm, M, scale)
             if layout == "BNSD":
                 out[b, h, :lq[b]] = o
@@ -198,7 +210,7 @@ def forward(q, k, v, mask=None, block_shape=(128, 128), seq_q=None, seq_kv=None,
 
 def forward_blockrows(q, k, v, mask=None, block_shape=(128, 128), seq_q=None,
                       seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0,
-                      pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+                      pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
     """The same forward, evaluated per query block row over that row's selected
     key set K(s) only (every query row of a block row has the same K(s)). Used
     where the dense [Lq, Lk] score matrix would not fit in host memory; pinned
@@ -232,6 +244,8 @@ def forward_blockrows(q, k, v, mask=None, block_shape=(128, 128), seq_q=None,
                 keys = np.concatenate([np.arange(j * by, min(lk[b], (j + 1) * by))
                                        for j in sel])
                 M = window_mask(np.arange(s0, s1), keys, pre_tokens, next_tokens)
+                if atten_mask is not None:
+                    M = M & (np.asarray(atten_mask)[s0:s1][:, keys] == 0)
                 o, l = _head_forward(Qh[s0:s1], Kh[keys], Vh[keys], M, scale)
                 if layout == "BNSD":
                     out[b, h, s0:s1] = o
@@ -262,7 +276,7 @@ def _head_backward(Qm, Km, Vm, dOm, Om, lse, M, scale):
 
 def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=None,
              seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
-             next_tokens=NO_WINDOW):
+             next_tokens=NO_WINDOW, atten_mask=None):
     """Full dQ, dK, dV (fp64, the layout's shapes) from the given Out and lse."""
     bx, by = int(block_shape[0]), int(block_shape[1])
     B, lq, lk = _lengths(q, k, layout, seq_q, seq_kv)
@@ -282,7 +296,7 @@ def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=N
             Om = head_rows(out, layout, b, h, lq[b], oq)
             L = _lse_rows(lse, layout, b, h, lq[b], oq)
             M = token_mask(None if mask is None else mask[b, h], bx, by, lq[b], lk[b],
-                           pre_tokens, next_tokens)
+                           pre_tokens, next_tokens, atten_mask)
             dQ, dK, dV = _head_backward(Qm, Km, Vm, dOm, Om, L, M, scale)
             if layout == "BNSD":
                 dq[b, h, :lq[b]] = dQ
@@ -298,7 +312,7 @@ def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=N
 def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
                      block_shape=(128, 128), seq_q=None, seq_kv=None, layout="BNSD",
                      num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
-                     next_tokens=NO_WINDOW):
+                     next_tokens=NO_WINDOW, atten_mask=None):
     """dQ[b, h, rows] only (fp64 [len(rows), D]); each row needs only its own
     query, dOut, Out, lse and the keys it selects. Rows at or beyond the actual
     length are 0 (R4)."""
@@ -320,7 +334,7 @@ def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
     Km = head_rows(k, layout, b, g, lk[b], okv)
     Vm = head_rows(v, layout, b, g, lk[b], okv)
     M = token_mask_at(None if mask is None else mask[b, h], bx, by, r, np.arange(lk[b]),
-                      pre_tokens, next_tokens)
+                      pre_tokens, next_tokens, atten_mask)
     dQ, _, _ = _head_backward(Qh, Km, Vm, dOh, Oh, L, M, scale)
     res[ok] = dQ
     return res
@@ -329,7 +343,7 @@ def backward_dq_rows(dout, q, k, v, out, lse, b, h, rows, mask=None,
 def backward_dkdv_rows(dout, q, k, v, out, lse, b, g, rows, mask=None,
                        block_shape=(128, 128), seq_q=None, seq_kv=None, layout="BNSD",
                        num_kv_heads=None, scale=1.0, pre_tokens=NO_WINDOW,
-                       next_tokens=NO_WINDOW):
+                       next_tokens=NO_WINDOW, atten_mask=None):
     """dK[b, g, rows], dV[b, g, rows] only (fp64), summed over the query heads of
     group g (R3). Each key row needs all query rows that select it."""
     bx, by = int(block_shape[0]), int(block_shape[1])
@@ -352,7 +366,7 @@ def backward_dkdv_rows(dout, q, k, v, out, lse, b, g, rows, mask=None,
         Om = head_rows(out, layout, b, h, lq[b], oq)
         L = _lse_rows(lse, layout, b, h, lq[b], oq)
         M = token_mask_at(None if mask is None else mask[b, h], bx, by, np.arange(lq[b]), t,
-                          pre_tokens, next_tokens)
+                          pre_tokens, next_tokens, atten_mask)
         _, dK, dV = _head_backward(Qm, Kt, Vt, dOm, Om, L, M, scale)
         dk[ok] += dK
         dv[ok] += dV

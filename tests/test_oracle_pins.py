@@ -573,3 +573,107 @@ def test_planted_window_mistakes_are_caught(kind, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught >= 1, kind
+
+
+# ----------------------------------------- token mask attenMask (reading R19) pins
+def _am(S, Skv, p, seed):
+    return (np.random.Generator(np.random.PCG64(seed)).random((S, Skv)) < p).astype(np.uint8)
+
+
+@pytest.mark.parametrize("pre,nxt", [(O.NO_WINDOW, O.NO_WINDOW), (20, 3)])
+def test_atten_mask_with_blocks_matches_sdpa(pre, nxt):
+    """attenMask (1 = masked) x window x block mask against SDPA with the
+    combined token mask built here from np.repeat, torch.tril/triu and the
+    inverted attenMask."""
+    S, Skv, bx, by = 40, 45, 8, 16
+    q, k, v, do, m = _case(N1=4, N2=2, S=S, Skv=Skv, D=8, bx=bx, by=by, seed=161, p=0.7)
+    am = _am(S, Skv, 0.3, 162)
+    blocks = np.repeat(np.repeat(m != 0, bx, axis=2), by, axis=3)[:, :, :S, :Skv]
+    band = torch.ones(S, Skv, dtype=torch.bool).tril(min(nxt, Skv)).triu(-min(pre, S)).numpy()
+    tm = blocks & band[None, None] & (am == 0)[None, None]
+    kw = dict(num_kv_heads=2, scale=0.5, pre_tokens=pre, next_tokens=nxt, atten_mask=am)
+    out, lse = O.forward(q, k, v, m, (bx, by), **kw)
+    grads = O.backward(do, q, k, v, out, lse, m, (bx, by), **kw)
+    ref, *rg = _sdpa_rows(q, k, v, do, tm, 0.5, 2)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+    for a, b in zip(grads, rg):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+    bo = O.forward_blockrows(q, k, v, m, (bx, by), **kw)
+    np.testing.assert_allclose(bo[0], out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(np.isneginf(bo[1]), np.isneginf(lse))
+
+
+def test_atten_mask_upper_triangle_is_causal_and_zero_mask_is_none():
+    """attenMask = np.triu(ones, 1) reproduces nextTokens = 0 bit for bit, a
+    band written as a mask reproduces the window, and an all-zero attenMask
+    changes nothing."""
+    S, Skv = 33, 41
+    q, k, v, do, m = _case(N1=2, N2=1, S=S, Skv=Skv, D=8, bx=8, by=8, seed=171)
+    kw = dict(num_kv_heads=1, scale=0.4)
+
+    def run(**extra):
+        o, l = O.forward(q, k, v, m, (8, 8), **kw, **extra)
+        return (o, l) + O.backward(do, q, k, v, o, l, m, (8, 8), **kw, **extra)
+    base, causal, band = run(), run(next_tokens=0), run(pre_tokens=6, next_tokens=2)
+    as_causal = run(atten_mask=np.triu(np.ones((S, Skv), np.uint8), 1))
+    keep = np.tril(np.ones((S, Skv), bool), 2) & np.triu(np.ones((S, Skv), bool), -6)
+    as_band = run(atten_mask=(~keep).astype(np.uint8))
+    zero = run(atten_mask=np.zeros((S, Skv), np.uint8))
+    for x, y in zip(causal, as_causal):
+        np.testing.assert_array_equal(x, y)
+    for x, y in zip(band, as_band):
+        np.testing.assert_array_equal(x, y)
+    for x, y in zip(base, zero):
+        np.testing.assert_array_equal(x, y)
+    full = run(atten_mask=np.ones((S, Skv), np.uint8))   # every pair masked: R6 everywhere
+    assert np.all(full[0] == 0) and np.all(np.isneginf(full[1]))
+    assert all(np.all(g == 0) for g in full[2:])
+
+
+def test_tnd_atten_mask_is_per_sequence_top_left():
+    lens_q, lens_k = [13, 30, 7], [21, 9, 30]
+    N1, N2, D, bx, by = 4, 2, 8, 8, 8
+    rng = np.random.Generator(np.random.PCG64(181))
+    m = (rng.random((3, N1, 4, 4)) < 0.8).astype(np.uint8)
+    am = _am(30, 30, 0.35, 182)
+    qt = _rand((sum(lens_q), N1, D), 183)
+    kt = _rand((sum(lens_k), N2, D), 184)
+    vt = _rand((sum(lens_k), N2, D), 185)
+    dot = _rand((sum(lens_q), N1, D), 186)
+    w = dict(atten_mask=am, pre_tokens=9, next_tokens=4)
+    out, lse = O.forward(qt, kt, vt, m, (bx, by), lens_q, lens_k, "TND", N2, 0.3, **w)
+    dq, dk, dv = O.backward(dot, qt, kt, vt, out, lse, m, (bx, by), lens_q, lens_k, "TND", N2,
+                            0.3, **w)
+    oq, ok = O.seq_offsets(lens_q), O.seq_offsets(lens_k)
+    to_bnsd = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2))[None]
+    for b in range(3):
+        sl_q, sl_k = slice(oq[b], oq[b + 1]), slice(ok[b], ok[b + 1])
+        o1, l1 = O.forward(to_bnsd(qt[sl_q]), to_bnsd(kt[sl_k]), to_bnsd(vt[sl_k]),
+                           m[b:b + 1], (bx, by), num_kv_heads=N2, scale=0.3, **w)
+        np.testing.assert_allclose(o1[0].transpose(1, 0, 2), out[sl_q], rtol=1e-13, atol=1e-14)
+        g1 = O.backward(to_bnsd(dot[sl_q]), to_bnsd(qt[sl_q]), to_bnsd(kt[sl_k]),
+                        to_bnsd(vt[sl_k]), o1, l1, m[b:b + 1], (bx, by), num_kv_heads=N2,
+                        scale=0.3, **w)
+        for x, y, sl in zip(g1, (dq, dk, dv), (sl_q, sl_k, sl_k)):
+            np.testing.assert_allclose(x[0].transpose(1, 0, 2), y[sl], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("kind", ["keep_polarity", "transposed"])
+def test_planted_atten_mask_mistakes_are_caught(kind, monkeypatch):
+    """attenMask read as a keep-mask, or indexed [t, s]: the SDPA pin fails."""
+    real = O.token_mask_at
+
+    def wrong(bm, bx, by, rows, cols, pre=O.NO_WINDOW, nxt=O.NO_WINDOW, am=None):
+        if am is not None:
+            am = np.asarray(am)
+            if kind == "keep_polarity":
+                am = (am == 0).astype(np.uint8)
+            else:
+                sq = max(am.shape)
+                pad = np.zeros((sq, sq), np.uint8)
+                pad[:am.shape[0], :am.shape[1]] = am
+                am = pad.T
+        return real(bm, bx, by, rows, cols, pre, nxt, am)
+    monkeypatch.setattr(O, "token_mask_at", wrong)
+    with pytest.raises(AssertionError):
+        test_atten_mask_with_blocks_matches_sdpa(O.NO_WINDOW, O.NO_WINDOW)
