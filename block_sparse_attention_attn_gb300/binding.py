@@ -59,8 +59,8 @@ def load_library():
         ctypes.c_char_p, i64, i64, ctypes.c_double, i64, i64, T, T, T, P(u64), P(vp)]
     lib.bsa_grad.argtypes = [vp, u64, vp, vp]
     lib.bsa_fwd_workspace_size.argtypes = [
-        T, T, T, T, P(i64), i64, P(i64), i64, P(i64), i64, ctypes.c_char_p, ctypes.c_char_p,
-        i64, ctypes.c_double, i64, i64, T, T, P(u64), P(vp)]
+        T, T, T, T, T, P(i64), i64, P(i64), i64, P(i64), i64, ctypes.c_char_p, ctypes.c_char_p,
+        i64, i64, ctypes.c_double, i64, i64, T, T, P(u64), P(vp)]
     lib.bsa_fwd.argtypes = [vp, u64, vp, vp]
     lib.bsa_executor_destroy.argtypes = [vp]
     lib.bsa_executor_set_timing_events.argtypes = [vp, vp, vp]
@@ -193,22 +193,26 @@ def bsa_fwd_workspace_size(query, key, value, block_sparse_mask=None, block_shap
                            actual_seq_lengths=None, actual_seq_lengths_kv=None,
                            q_layout="BNSD", kv_layout=None, num_key_value_heads=None,
                            scale_value=1.0, pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW,
-                           attention_out=None, softmax_lse=None):
+                           attention_out=None, softmax_lse=None, atten_mask=None,
+                           mask_type=None):
     lib = load_library()
     kv_layout = q_layout if kv_layout is None else kv_layout
     if num_key_value_heads is None:
         num_key_value_heads = key.shape[1]
-    ds = [_desc(t) for t in (query, key, value, block_sparse_mask, attention_out, softmax_lse)]
+    if mask_type is None:
+        mask_type = 0 if atten_mask is None else 1
+    ds = [_desc(t) for t in (query, key, value, block_sparse_mask, attention_out, softmax_lse,
+                             atten_mask)]
     bs, nbs = _i64_array(block_shape)
     sq, nsq = _i64_array(actual_seq_lengths)
     sk, nsk = _i64_array(actual_seq_lengths_kv)
     ws = ctypes.c_uint64(0)
     ex = ctypes.c_void_p(None)
     _check(lib.bsa_fwd_workspace_size(
-        _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ds[3]), bs, nbs, sq, nsq, sk, nsk,
-        q_layout.encode(), kv_layout.encode(), int(num_key_value_heads), float(scale_value),
-        int(pre_tokens), int(next_tokens), _ptr(ds[4]), _ptr(ds[5]), ctypes.byref(ws),
-        ctypes.byref(ex)))
+        _ptr(ds[0]), _ptr(ds[1]), _ptr(ds[2]), _ptr(ds[3]), _ptr(ds[6]), bs, nbs, sq, nsq, sk,
+        nsk, q_layout.encode(), kv_layout.encode(), int(num_key_value_heads), int(mask_type),
+        float(scale_value), int(pre_tokens), int(next_tokens), _ptr(ds[4]), _ptr(ds[5]),
+        ctypes.byref(ws), ctypes.byref(ex)))
     return ws.value, Executor(ex.value, ds)
 
 
@@ -269,20 +273,22 @@ def block_sparse_attention_grad(dout, query, key, value, attention_out, softmax_
                                 layout="BNSD", num_key_value_heads=None, scale_value=None,
                                 dq=None, dk=None, dv=None, workspace=None, stream=None,
                                 deterministic=False, pre_tokens=NO_WINDOW,
-                                next_tokens=NO_WINDOW):
+                                next_tokens=NO_WINDOW, atten_mask=None):
     """Both stages; allocates outputs/workspace with torch when not given.
     pre_tokens / next_tokens: sliding window (query s and key t of a sequence
     pair up iff s - pre_tokens <= t <= s + next_tokens; next_tokens=0 is
-    causal). Returns (dq, dk, dv, workspace)."""
+    causal). atten_mask: optional 2-D bool/uint8 [>= maxSq, >= maxSkv] token
+    mask, True = masked (maskType 1). Returns (dq, dk, dv, workspace)."""
     if scale_value is None:
         scale_value = query.shape[-1] ** -0.5
     dq = torch.empty_like(query) if dq is None else dq
     dk = torch.empty_like(key) if dk is None else dk
     dv = torch.empty_like(value) if dv is None else dv
     size, ex = bsa_grad_workspace_size(
-        dout, query, key, value, attention_out, softmax_lse, block_sparse_mask, None,
+        dout, query, key, value, attention_out, softmax_lse, block_sparse_mask, atten_mask,
         block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
-        num_key_value_heads, 0, scale_value, pre_tokens, next_tokens, dq=dq, dk=dk, dv=dv)
+        num_key_value_heads, 0 if atten_mask is None else 1, scale_value, pre_tokens,
+        next_tokens, dq=dq, dk=dk, dv=dv)
     if deterministic:
         ex.set_deterministic(True)
     if workspace is None or workspace.numel() < size:
@@ -295,7 +301,7 @@ def block_sparse_attention_fwd(query, key, value, block_sparse_mask=None, block_
                                actual_seq_lengths=None, actual_seq_lengths_kv=None,
                                layout="BNSD", num_key_value_heads=None, scale_value=None,
                                out=None, lse=None, workspace=None, stream=None,
-                               pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+                               pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
     """Companion forward (same sliding window arguments as the backward);
     returns (out, lse [..., 1] fp32, workspace)."""
     if scale_value is None:
@@ -306,7 +312,7 @@ def block_sparse_attention_fwd(query, key, value, block_sparse_mask=None, block_
     size, ex = bsa_fwd_workspace_size(query, key, value, block_sparse_mask, block_shape,
                                       actual_seq_lengths, actual_seq_lengths_kv, layout, layout,
                                       num_key_value_heads, scale_value, pre_tokens,
-                                      next_tokens, out, lse)
+                                      next_tokens, out, lse, atten_mask)
     if workspace is None or workspace.numel() < size:
         workspace = torch.empty(max(size, 256), dtype=torch.uint8, device=query.device)
     bsa_fwd(workspace, size, ex, stream)
@@ -322,16 +328,17 @@ class BlockSparseAttentionFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
                 actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic,
-                pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+                pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
         if scale_value is None:
             scale_value = query.shape[-1] ** -0.5
         query, key, value = query.contiguous(), key.contiguous(), value.contiguous()
         out, lse, _ = block_sparse_attention_fwd(
             query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
             actual_seq_lengths_kv, layout, num_key_value_heads, scale_value,
-            pre_tokens=pre_tokens, next_tokens=next_tokens)
+            pre_tokens=pre_tokens, next_tokens=next_tokens, atten_mask=atten_mask)
         ctx.save_for_backward(query, key, value, out, lse)
         ctx.mask = block_sparse_mask
+        ctx.atten_mask = atten_mask
         ctx.args = (block_shape, actual_seq_lengths, actual_seq_lengths_kv, layout,
                     num_key_value_heads, scale_value, deterministic, pre_tokens, next_tokens)
         return out
@@ -344,19 +351,20 @@ class BlockSparseAttentionFunction(torch.autograd.Function):
         dq, dk, dv, ws = block_sparse_attention_grad(
             dout.contiguous(), query, key, value, out, lse, ctx.mask, block_shape,
             actual_seq_lengths, actual_seq_lengths_kv, layout, num_key_value_heads, scale_value,
-            deterministic=deterministic, pre_tokens=pre_tokens, next_tokens=next_tokens)
+            deterministic=deterministic, pre_tokens=pre_tokens, next_tokens=next_tokens,
+            atten_mask=ctx.atten_mask)
         bsa_check_status(ws)
-        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None
+        return dq, dk, dv, None, None, None, None, None, None, None, None, None, None, None
 
 
 def block_sparse_attention(query, key, value, block_sparse_mask=None, block_shape=None,
                            actual_seq_lengths=None, actual_seq_lengths_kv=None, layout="BNSD",
                            num_key_value_heads=None, scale_value=None, deterministic=False,
-                           pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW):
+                           pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
     """Differentiable block-sparse attention: Out = softmax(scale*Q K^T over the
     selected blocks, inside the sliding window) V; gradients for Q, K and V come
     from the backward kernels."""
     return BlockSparseAttentionFunction.apply(
         query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
         actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic,
-        pre_tokens, next_tokens)
+        pre_tokens, next_tokens, atten_mask)

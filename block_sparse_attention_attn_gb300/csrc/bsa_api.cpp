@@ -367,6 +367,11 @@ struct bsa_executor {
   uint64_t off_info = 0, off_lse2 = 0, off_dvec = 0, off_dqacc = 0, off_colcnt = 0,
            off_colptr = 0, off_entries = 0, off_items = 0, off_colinfo = 0, off_fin = 0,
            off_slots = 0;
+  // token mask attenMask (maskType 1): the caller's matrix and its packed form
+  const uint8_t* am_ptr = nullptr;
+  int64_t am_st0 = 0, am_st1 = 0;
+  int am_rows = 0, am_cols = 0;
+  uint64_t off_am_row = 0, off_am_col = 0, off_am_sub = 0;
   uint64_t ws_size = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;      // owned: side-stream preprocess
@@ -404,6 +409,69 @@ void build_info(bsa_executor* ex) {
   Plan& p = ex->plan;
   p.Rq = rq;
   p.n_qtiles = rq / kTile;
+}
+
+// maskType / attenMaskOptional: 0 with no mask, or 1 with a 2-D BOOL/UINT8
+// [rows >= maxSq, cols >= maxSkv] matrix (any positive strides; nonzero =
+// the pair is masked out).
+bsa_status check_amask(const bsa_tensor* am, int64_t mask_type, const Geometry& g) {
+  if (am == nullptr) {
+    if (mask_type != 0)
+      return fail(BSA_ERR_PARAM_INVALID, "maskType %lld needs attenMaskOptional",
+                  (long long)mask_type);
+    return BSA_OK;
+  }
+  if (mask_type != 1)
+    return fail(BSA_ERR_PARAM_INVALID, "attenMaskOptional needs maskType 1 (got %lld)",
+                (long long)mask_type);
+  if (am->data == nullptr) return fail(BSA_ERR_PARAM_NULLPTR, "attenMask with a NULL data pointer");
+  if (am->dtype != BSA_U8 || am->ndim != 2)
+    return fail(BSA_ERR_PARAM_INVALID, "attenMask must be a 2-D BOOL/UINT8 tensor");
+  if (am->shape[0] < g.Sq || am->shape[1] < g.Skv)
+    return fail(BSA_ERR_PARAM_INVALID, "attenMask must cover [%d, %d] (maxSq, maxSkv)", g.Sq,
+                g.Skv);
+  if (am->stride[0] <= 0 || am->stride[1] <= 0)
+    return fail(BSA_ERR_PARAM_INVALID, "attenMask strides must be positive");
+  return BSA_OK;
+}
+
+// Records the token mask in the executor and reserves its packed form at `off`.
+uint64_t reserve_amask(bsa_executor* ex, const bsa_tensor* am, uint64_t off) {
+  Plan& p = ex->plan;
+  if (am == nullptr) {
+    p.am = 0;
+    return off;
+  }
+  p.am = 1;
+  ex->am_ptr = static_cast<const uint8_t*>(am->data);
+  ex->am_st0 = am->stride[0];
+  ex->am_st1 = am->stride[1];
+  ex->am_rows = (int)std::min<int64_t>(am->shape[0], (int64_t)p.Mq_t * kTile);
+  ex->am_cols = (int)std::min<int64_t>(am->shape[1], (int64_t)p.Mk_t * kTile);
+  p.am_wk = p.Mk_t * 4;
+  p.am_wq = p.Mq_t * 4;
+  p.am_sk = p.Mk_t * 2;
+  ex->off_am_row = off; off = align256(off + (uint64_t)p.Mq_t * kTile * p.am_wk * 4);
+  ex->off_am_col = off; off = align256(off + (uint64_t)p.Mk_t * kTile * p.am_wq * 4);
+  ex->off_am_sub = off; off = align256(off + (uint64_t)p.Mq_t * 2 * p.am_sk);
+  return off;
+}
+
+// Points the plan at the packed token mask in `ws` and queues its packing.
+cudaError_t launch_amask_for(const bsa_executor* ex, Plan& p, uint8_t* ws, cudaStream_t st) {
+  if (!p.am) return cudaSuccess;
+  p.am_row = reinterpret_cast<const uint32_t*>(ws + ex->off_am_row);
+  p.am_col = reinterpret_cast<const uint32_t*>(ws + ex->off_am_col);
+  p.am_sub = ws + ex->off_am_sub;
+  AmaskArgs a{};
+  a.m = ex->am_ptr; a.st0 = ex->am_st0; a.st1 = ex->am_st1;
+  a.rows = ex->am_rows; a.cols = ex->am_cols;
+  a.row_bits = reinterpret_cast<uint32_t*>(ws + ex->off_am_row);
+  a.col_bits = reinterpret_cast<uint32_t*>(ws + ex->off_am_col);
+  a.sub = ws + ex->off_am_sub;
+  a.nsub_q = p.Mq_t * 2; a.nsub_k = p.Mk_t * 2;
+  a.wk = p.am_wk; a.wq = p.am_wq;
+  return launch_amask(a, st);
 }
 
 // preTokens / nextTokens: any int64 pair whose window overlaps the diagonal
@@ -517,15 +585,17 @@ bsa_status bsa_grad_workspace_size(
   if (block_sparse_mask != nullptr && block_sparse_mask->data == nullptr)
     return fail(BSA_ERR_PARAM_NULLPTR, "blockSparseMask with a NULL data pointer");
   *executor = nullptr;
-  if (atten_mask != nullptr)
-    return fail(BSA_ERR_PARAM_INVALID, "attenMaskOptional is not supported: pass NULL");
-  if (mask_type != 0) return fail(BSA_ERR_PARAM_INVALID, "maskType must be 0");
+  if (atten_mask == nullptr && mask_type != 0)
+    return fail(BSA_ERR_PARAM_INVALID, "maskType %lld needs attenMaskOptional", (long long)mask_type);
+  if (atten_mask != nullptr && mask_type != 1)
+    return fail(BSA_ERR_PARAM_INVALID, "attenMaskOptional needs maskType 1");
   if (check_window(pre_tokens, next_tokens) != BSA_OK) return BSA_ERR_PARAM_INVALID;
   Geometry g;
   bsa_status st = check_common(query, key, value, block_sparse_mask, block_shape, block_shape_len,
                                actual_seq_lengths, n_seq, actual_seq_lengths_kv, n_seq_kv,
                                q_layout, kv_layout, num_key_value_heads, scale_value, &g);
   if (st != BSA_OK) return st;
+  if ((st = check_amask(atten_mask, mask_type, g)) != BSA_OK) return st;
   if (dout->dtype != query->dtype || attention_out->dtype != query->dtype)
     return fail(BSA_ERR_PARAM_INVALID, "dout/attentionOut dtype must equal query dtype");
   if (!same_shape(dout, query) || !same_shape(attention_out, query))
@@ -618,6 +688,7 @@ bsa_status bsa_grad_workspace_size(
   ex->off_colinfo = off; off = align256(off + (uint64_t)p.NGC * 4);
   ex->off_fin = off; off = align256(off + (uint64_t)p.NGC * 4);
   ex->off_slots = off; off = align256(off + (uint64_t)p.max_slots * 2 * kTile * g.D * 4);
+  off = reserve_amask(ex, atten_mask, off);
   ex->ws_size = off;
   // events of the side-stream preprocess (without them everything runs on
   // the caller's stream)
@@ -680,6 +751,8 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
                                 reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "copy of sequence info: %s", cudaGetErrorString(e));
+  if ((e = launch_amask_for(ex, p, ws, st)) != cudaSuccess)
+    return fail(BSA_ERR_RUNTIME, "token mask packing launch failed: %s", cudaGetErrorString(e));
   CompactArgs ca{};
   ca.mask = p.mask; ca.sb = p.mask_sb; ca.sh = p.mask_sh; ca.si = p.mask_si;
   ca.has_mask = p.has_mask;
@@ -690,6 +763,7 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.lq = p.lq; ca.lk = p.lk;
   ca.counts = p.colcnt; ca.ptr = p.colptr; ca.out = p.entries; ca.plain = 0;
   ca.win = p.win; ca.win_pre = p.win_pre; ca.win_next = p.win_next;
+  ca.am_sub = p.am ? p.am_sub : nullptr; ca.am_sk = p.am_sk;
   ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
   // The preprocess (bandwidth-bound) runs on a side stream while the mask
   // compaction and the planner (latency-bound, one block) run on `st`.
@@ -839,10 +913,11 @@ bsa_status bsa_mask_compact(const bsa_tensor* mask, int64_t bx, int64_t by,
 // ---------------------------------------------------------------------------
 bsa_status bsa_fwd_workspace_size(
     const bsa_tensor* query, const bsa_tensor* key, const bsa_tensor* value,
-    const bsa_tensor* block_sparse_mask, const int64_t* block_shape, int64_t block_shape_len,
-    const int64_t* actual_seq_lengths, int64_t n_seq, const int64_t* actual_seq_lengths_kv,
-    int64_t n_seq_kv, const char* q_layout, const char* kv_layout, int64_t num_key_value_heads,
-    double scale_value, int64_t pre_tokens, int64_t next_tokens, const bsa_tensor* attention_out,
+    const bsa_tensor* block_sparse_mask, const bsa_tensor* atten_mask, const int64_t* block_shape,
+    int64_t block_shape_len, const int64_t* actual_seq_lengths, int64_t n_seq,
+    const int64_t* actual_seq_lengths_kv, int64_t n_seq_kv, const char* q_layout,
+    const char* kv_layout, int64_t num_key_value_heads, int64_t mask_type, double scale_value,
+    int64_t pre_tokens, int64_t next_tokens, const bsa_tensor* attention_out,
     const bsa_tensor* softmax_lse, uint64_t* workspace_size, bsa_executor** executor) {
   if (query == nullptr || key == nullptr || value == nullptr || attention_out == nullptr ||
       softmax_lse == nullptr || workspace_size == nullptr || executor == nullptr)
@@ -861,6 +936,7 @@ bsa_status bsa_fwd_workspace_size(
                                actual_seq_lengths, n_seq, actual_seq_lengths_kv, n_seq_kv,
                                q_layout, kv_layout, num_key_value_heads, scale_value, &g);
   if (st != BSA_OK) return st;
+  if ((st = check_amask(atten_mask, mask_type, g)) != BSA_OK) return st;
   if (attention_out->dtype != query->dtype || !same_shape(attention_out, query) ||
       !out_strides_ok(attention_out))
     return fail(BSA_ERR_PARAM_INVALID, "attentionOut must match query's dtype and shape");
@@ -891,6 +967,7 @@ bsa_status bsa_fwd_workspace_size(
   f.n_rows_items = g.B * g.N1 * p.Mq_t;
   uint64_t off = align256(kHdrWords * 4);
   ex->off_info = off; off = align256(off + ex->info.size() * 4);
+  off = reserve_amask(ex, atten_mask, off);
   ex->ws_size = off;
   *workspace_size = off;
   *executor = ex;
@@ -928,6 +1005,7 @@ bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* execu
   cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
                                 reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, kHdrWords * 4, st);
+  if (e == cudaSuccess) e = launch_amask_for(ex, f.p, ws, st);
   if (e == cudaSuccess && ex->ev_before) e = cudaEventRecord(ex->ev_before, st);
   if (e == cudaSuccess) e = launch_fwd(f, maps, st);
   if (e == cudaSuccess && ex->ev_after) e = cudaEventRecord(ex->ev_after, st);

@@ -179,9 +179,9 @@ __device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
   return it;
 }
 
-// WIN: instantiated with the sliding-window code (Plan::win set); the plain
-// instance carries none of it.
-template <int D, int DT, bool WIN>
+// EM: instantiated with the element-mask code (sliding window, Plan::win, and
+// token mask, Plan::am); the plain instance carries none of it.
+template <int D, int DT, bool EM>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -676,18 +676,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // selected sub-block); query columns past the query length need no
         // test: their lse rows hold +inf, so P is exactly 0 there
         const uint32_t rmask = (t_ok && ((sub >> (s_sub * 2 + t_sub)) & 1)) ? 0xFFFFFFFFu : 0u;
-        // sliding window: when it cuts this tile (the same answer for the whole
-        // CTA), wm0 / wm1 flag the live query columns of this thread's two
-        // 32-column chunks
+        // element masks: when the sliding window or the token mask cuts this
+        // tile (the same answer for the whole CTA), wm0 / wm1 flag the live
+        // query columns of this thread's two 32-column chunks
         bool wcut = false;
-        uint32_t wm0 = 0u, wm1 = 0u;
-        if (WIN) {
-          const int64_t s0 = (int64_t)entry_it(ent) * 128, t0 = (int64_t)ii.jt * 128;
-          wcut = !win_covers(s0, s0 + 128, t0, t0 + 128, p.win_pre, p.win_next);
-          if (wcut) {
+        uint32_t wm0 = 0xFFFFFFFFu, wm1 = 0xFFFFFFFFu;
+        if (EM) {
+          const int it = entry_it(ent);
+          const int64_t s0 = (int64_t)it * 128, t0 = (int64_t)ii.jt * 128;
+          if (p.win && !win_covers(s0, s0 + 128, t0, t0 + 128, p.win_pre, p.win_next)) {
+            wcut = true;
             const int2 w = win_span(t0 + t, s0 + 64 * wg, -p.win_next, p.win_pre);
             wm0 = bit_range(w.x, w.y);
             wm1 = bit_range(w.x - 32, w.y - 32);
+          }
+          if (p.am) {
+            const uint8_t* sc = p.am_sub + (int64_t)(2 * it) * p.am_sk + 2 * ii.jt;
+            if ((sc[0] & sc[1] & sc[p.am_sk] & sc[p.am_sk + 1]) != kAmNone) {
+              wcut = true;
+              const uint2 a = *reinterpret_cast<const uint2*>(
+                  p.am_col + (int64_t)(t0 + t) * p.am_wq + 4 * it + 2 * wg);
+              wm0 &= ~a.x;
+              wm1 &= ~a.y;
+            }
           }
         }
         const int st = n & 1;
@@ -992,24 +1003,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DT, bool WIN>
+template <int D, int DT, bool EM>
 cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
   const size_t smem = Smem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd<D, DT, WIN>,
+  cudaError_t e = cudaFuncSetAttribute(k_bwd<D, DT, EM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int grid = p.num_sms;
   if (p.max_items < grid) grid = p.max_items;
   if (grid < 1) grid = 1;
-  k_bwd<D, DT, WIN><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, m.dk, m.dv, p);
+  k_bwd<D, DT, EM><<<grid, kThreads, smem, st>>>(m.q, m.k, m.v, m.dout, m.dqacc, m.dk, m.dv, p);
   return cudaGetLastError();
 }
 
-template <bool WIN>
+template <bool EM>
 cudaError_t launch_w(const Plan& p, const BwdMaps& m, cudaStream_t st) {
   if (p.dtype == kDtBF16)
-    return p.D == 128 ? launch_t<128, kDtBF16, WIN>(p, m, st) : launch_t<64, kDtBF16, WIN>(p, m, st);
-  return p.D == 128 ? launch_t<128, kDtF16, WIN>(p, m, st) : launch_t<64, kDtF16, WIN>(p, m, st);
+    return p.D == 128 ? launch_t<128, kDtBF16, EM>(p, m, st) : launch_t<64, kDtBF16, EM>(p, m, st);
+  return p.D == 128 ? launch_t<128, kDtF16, EM>(p, m, st) : launch_t<64, kDtF16, EM>(p, m, st);
 }
 
 }  // namespace
@@ -1017,7 +1028,7 @@ cudaError_t launch_w(const Plan& p, const BwdMaps& m, cudaStream_t st) {
 size_t bwd_smem_bytes(int D) { return D == 128 ? Smem<128>::kBytes : Smem<64>::kBytes; }
 
 cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st) {
-  return p.win ? launch_w<true>(p, m, st) : launch_w<false>(p, m, st);
+  return (p.win || p.am) ? launch_w<true>(p, m, st) : launch_w<false>(p, m, st);
 }
 
 }  // namespace bsa

@@ -124,6 +124,7 @@ __device__ __forceinline__ int q_tile_bits(const Plan& p, int b, int h, int it, 
         on = win_meets((int64_t)i * p.bx, min((int64_t)(i + 1) * p.bx, (int64_t)Lq),
                        (int64_t)j * p.by, min((int64_t)(j + 1) * p.by, (int64_t)Lk), p.win_pre,
                        p.win_next);
+      if (on && p.am) on = am_block_meets(p.am_sub, p.am_sk, i, j, p.bx, p.by);
       if (on) bits |= 1 << (ri * 2 + cj);
     }
   }
@@ -446,18 +447,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars[kSFull], m & 1, abort_flag)) { where = kErrWaitS; break; }
         if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
         tc_fence_after();
-        // live key columns [t_lo, t_hi): inside the key length and the window
+        // live key columns [t_lo, t_hi): inside the key length and the window;
+        // amw: token mask bits of this row's 128 keys (bit set = masked)
         int t_lo = 0, t_hi = Lk - jt * 128;
         if (p.win) {
           const int2 w = win_span(srow, (int64_t)jt * 128, -p.win_pre, p.win_next);
           t_lo = w.x;
           t_hi = min(t_hi, w.y);
         }
+        uint4 amw = make_uint4(0u, 0u, 0u, 0u);
+        if (p.am)
+          amw = *reinterpret_cast<const uint4*>(p.am_row + (int64_t)srow * p.am_wk + 4 * jt);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t x[32], y[32];
           tmem_ld32(tmem + lane_off + kColS + 32 * c, x);
           tmem_ld32(tmem + lane_off + kColP + 32 * c, y);
+          const uint32_t aw = c == 0 ? amw.x : c == 1 ? amw.y : c == 2 ? amw.z : amw.w;
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -466,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 2; ++u) {
               const int t = 32 * c + 2 * k + u;
               const int t_sub = p.cb == 2 ? (t >> 6) : 0;
-              const bool on = s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1);
+              const bool on = s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1) &&
+                              !((aw >> (2 * k + u)) & 1u);
               // P rounded to the operand type, as in the dV/dK kernel
               const float pv =
                   on ? E::round(ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)))

@@ -90,6 +90,24 @@ __host__ __device__ inline int2 win_span(int64_t pos, int64_t base, int64_t dlo,
   return make_int2((int)lo, (int)hi);
 }
 
+// Token mask attenMask (parameter table row attenMaskOptional: the atten_mask
+// of S = Mask(scale*Q*K^T, atten_mask); a true entry masks the pair out, as
+// on the FlashAttentionScore page): one [maxSq, maxSkv] matrix for every
+// batch and head, indexed by per-sequence positions. The preprocess packs it
+// into bit rows (query-major and key-major) and classifies each 64x64
+// sub-block: 0 every pair masked, 1 some, 2 none (positions outside the
+// matrix count as masked; they lie past every sequence length).
+constexpr int kAmAll = 0, kAmSome = 1, kAmNone = 2;
+
+// A block (i, j) of bx x by tokens has a pair the token mask keeps.
+__host__ __device__ inline bool am_block_meets(const uint8_t* sub, int sk, int i, int j, int bx,
+                                               int by) {
+  for (int qi = i * bx / 64; qi < (i + 1) * bx / 64; ++qi)
+    for (int qj = j * by / 64; qj < (j + 1) * by / 64; ++qj)
+      if (sub[qi * sk + qj] != kAmAll) return true;
+  return false;
+}
+
 // Bits lo .. hi-1 of a 32-bit word (the part of [lo, hi) inside [0, 32)).
 __host__ __device__ inline uint32_t bit_range(int lo, int hi) {
   lo = lo < 0 ? 0 : lo;
@@ -129,6 +147,11 @@ struct Plan {
   int det;                              // deterministic dQ: separate query-tile pass, no reduce-adds
   int win;                              // a sliding window cuts some pair of the problem
   int64_t win_pre, win_next;            // its limits (clamped to +-kWinClamp)
+  int am;                               // the token mask attenMask applies (maskType 1)
+  const uint32_t* am_row;               // [Mq_t*128][am_wk]: bit k of word w = pair (s, 32w+k) masked
+  const uint32_t* am_col;               // [Mk_t*128][am_wq]: bit k of word w = pair (32w+k, t) masked
+  const uint8_t* am_sub;                // [Mq_t*2][am_sk] class of each 64x64 sub-block
+  int am_wk, am_wq, am_sk;              // row strides (words, words, bytes)
   // per-batch info in the workspace (int32 [B] each)
   const int* lq;
   const int* lk;

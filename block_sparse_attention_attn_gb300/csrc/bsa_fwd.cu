@@ -120,6 +120,7 @@ __device__ __forceinline__ int fwd_tile_bits(const Plan& p, int b, int h, int it
         on = win_meets((int64_t)i * p.bx, min((int64_t)(i + 1) * p.bx, (int64_t)Lq),
                        (int64_t)j * p.by, min((int64_t)(j + 1) * p.by, (int64_t)Lk), p.win_pre,
                        p.win_next);
+      if (on && p.am) on = am_block_meets(p.am_sub, p.am_sk, i, j, p.bx, p.by);
       if (on) bits |= 1 << (ri * 2 + cj);
     }
   }
@@ -399,11 +400,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           t_lo = w.x;
           t_hi = min(t_hi, w.y);
         }
+        // token mask bits of this row's 128 keys (bit set = masked)
+        uint4 amw = make_uint4(0u, 0u, 0u, 0u);
+        if (p.am)
+          amw = *reinterpret_cast<const uint4*>(p.am_row + (int64_t)(fi.it * 128 + s) * p.am_wk +
+                                                4 * jt);
         const int s_sub = p.rb == 2 ? (s >> 6) : 0;
-        // column t is live when t_lo <= t < t_hi and its key sub-block bit is set
+        // column t is live when t_lo <= t < t_hi, its key sub-block bit is set
+        // and the token mask keeps it
         auto col_on = [&](int t) -> bool {
           const int t_sub = p.cb == 2 ? (t >> 6) : 0;
-          return s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1);
+          const uint32_t aw = (t >> 5) == 0 ? amw.x : (t >> 5) == 1 ? amw.y : (t >> 5) == 2 ? amw.z : amw.w;
+          return s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1) &&
+                 !((aw >> (t & 31)) & 1u);
         };
         float mx = -INFINITY;
 #pragma unroll

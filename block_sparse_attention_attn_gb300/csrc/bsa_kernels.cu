@@ -3,6 +3,7 @@
 //     page "aclnnBlockSparseAttentionGrad", parameter table, row
 //     blockSparseMaskOptional (1 = the block takes part);
 //   * the backward work planner (column lists -> balanced work items);
+//   * the packing of the token mask attenMask into bit rows;
 //   * the preprocess D = rowsum(dOut * attentionOut) (formulas, softmax_grad)
 //     and lse*log2(e), plus zeroing of the fp32 dQ accumulator;
 //   * the finalize kernels: fp32 dQ (and split-column dK/dV) -> output dtype,
@@ -21,8 +22,8 @@ namespace bsa {
 // compaction
 // --------------------------------------------------------------------------
 // Sub-block bits of tile (it, jt) for (b, h): bit (ri*2+cj) set when block
-// (it*rb+ri, jt*cb+cj) lies inside the valid range, is selected and (with a
-// sliding window) holds at least one pair of the window.
+// (it*rb+ri, jt*cb+cj) lies inside the valid range, is selected and holds at
+// least one pair that the sliding window and the token mask keep.
 __device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int it, int jt,
                                          int Lq, int Lk) {
   int bits = 0;
@@ -41,6 +42,7 @@ __device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int
         on = win_meets((int64_t)i * a.bx, min((int64_t)(i + 1) * a.bx, (int64_t)Lq),
                        (int64_t)j * a.by, min((int64_t)(j + 1) * a.by, (int64_t)Lk), a.win_pre,
                        a.win_next);
+      if (on && a.am_sub != nullptr) on = am_block_meets(a.am_sub, a.am_sk, i, j, a.bx, a.by);
       if (on) bits |= 1 << (ri * 2 + cj);
     }
   }
@@ -118,6 +120,42 @@ __global__ void k_rows(CompactArgs a, int fill) {
     }
   }
   if (!fill && lane == 0) a.counts[row] = count;
+}
+
+// --------------------------------------------------------------------------
+// token mask packing (attenMaskOptional; 1 = the pair is masked out)
+// --------------------------------------------------------------------------
+// One 256-thread block per 64x64 sub-block (i, j): the bytes go through shared
+// memory once and come out as two 32-bit words per query row (keys
+// 64j .. 64j+63), two per key row (queries 64i .. 64i+63) and the sub-block's
+// class. Positions outside the matrix count as masked.
+__global__ void __launch_bounds__(256) k_amask(AmaskArgs a) {
+  __shared__ uint8_t tile[64][65];
+  const int i = blockIdx.y, j = blockIdx.x, tid = threadIdx.x;
+  for (int e = tid; e < 64 * 64; e += 256) {
+    const int r = e >> 6, c = e & 63;
+    const int s = i * 64 + r, t = j * 64 + c;
+    uint8_t v = 1;
+    if (s < a.rows && t < a.cols) v = a.m[(int64_t)s * a.st0 + (int64_t)t * a.st1] != 0;
+    tile[r][c] = v;
+  }
+  __syncthreads();
+  const int r = tid >> 2, q = tid & 3;  // row / column r, 16-wide quarter q
+  uint32_t rb = 0, cb = 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    rb |= (uint32_t)tile[r][16 * q + k] << k;
+    cb |= (uint32_t)tile[16 * q + k][r] << k;
+  }
+  const uint32_t rb_hi = __shfl_down_sync(0xffffffffu, rb, 1);
+  const uint32_t cb_hi = __shfl_down_sync(0xffffffffu, cb, 1);
+  if ((q & 1) == 0) {
+    a.row_bits[(int64_t)(i * 64 + r) * a.wk + 2 * j + (q >> 1)] = rb | (rb_hi << 16);
+    a.col_bits[(int64_t)(j * 64 + r) * a.wq + 2 * i + (q >> 1)] = cb | (cb_hi << 16);
+  }
+  const int all = __syncthreads_and(rb == 0xFFFFu);
+  const int any = __syncthreads_or(rb != 0u);
+  if (tid == 0) a.sub[(int64_t)i * a.nsub_k + j] = all ? kAmAll : (any ? kAmSome : kAmNone);
 }
 
 // Block-wide exclusive scan of one value per thread (1024 threads).
@@ -525,6 +563,12 @@ cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st) {
   const int ncols = a.B * a.N2 * a.col_slots * a.G;
   if (ncols == 0) return cudaSuccess;
   k_columns<<<(ncols + 7) / 8, 256, 0, st>>>(a, fill);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amask(const AmaskArgs& a, cudaStream_t st) {
+  if (a.nsub_q == 0 || a.nsub_k == 0) return cudaSuccess;
+  k_amask<<<dim3(a.nsub_k, a.nsub_q), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,8 @@ struct CompactArgs {
   int plain;           // 1: store the tile index only; 0: packed entry
   int win;             // drop sub-blocks outside the sliding window (Plan::win)
   int64_t win_pre, win_next;
+  const uint8_t* am_sub;  // drop blocks the token mask masks entirely (or null)
+  int am_sk;
   float* zero;            // fill pass: optional fp32 region cleared first (or null)
   const int* zero_count;  // device: number of zero_per-float units to clear
   int zero_per;           // floats per unit, a multiple of 4
@@ -41,6 +43,20 @@ void set_last_error(const char* msg);
 // one cudaMemcpyAsync.
 cudaError_t launch_upload(const int* host, int n, int* dst, cudaStream_t st);
 cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st);
+
+// Packing of the token mask attenMask [rows, cols] (element strides st0, st1;
+// nonzero = masked) into the bit rows and sub-block classes of Plan::am_*.
+struct AmaskArgs {
+  const uint8_t* m;
+  int64_t st0, st1;
+  int rows, cols;
+  uint32_t* row_bits;  // [nsub_q*64][wk]
+  uint32_t* col_bits;  // [nsub_k*64][wq]
+  uint8_t* sub;        // [nsub_q][nsub_k]
+  int nsub_q, nsub_k;  // 64x64 sub-blocks (2 * tiles each way)
+  int wk, wq;          // words per bit row (2*nsub_k, 2*nsub_q)
+};
+cudaError_t launch_amask(const AmaskArgs& a, cudaStream_t st);
 cudaError_t launch_rows(const CompactArgs& a, int fill, cudaStream_t st);
 cudaError_t launch_scan(const int* in, int* out, int n, cudaStream_t st);
 cudaError_t launch_plan(const Plan& p, cudaStream_t st);

@@ -77,7 +77,15 @@ typedef struct bsa_executor bsa_executor; /* opaque, host side */
  *                                the block shape is then ignored. Bits of blocks
  *                                that start at or beyond a sequence's actual
  *                                length are ignored.
- *   atten_mask                 : must be NULL (not supported, as on the page).
+ *   atten_mask                 : token mask, the atten_mask of the formula
+ *                                S = Mask(scale*Q*K^T, atten_mask) (parameter table
+ *                                row attenMaskOptional; polarity as on the
+ *                                FlashAttentionScore page: nonzero = the pair is
+ *                                masked out). NULL = none. Otherwise a 2-D
+ *                                BOOL/UINT8 device matrix of at least [maxSq, maxSkv]
+ *                                rows x columns, any positive strides, shared by
+ *                                every batch and head and indexed by the query /
+ *                                key positions counted from each sequence's start.
  *   block_shape, block_shape_len : host int64 [bx, by, ...]; NULL or len 0 =
  *                                {128, 128}; at least 2 entries, extra entries are
  *                                ignored. This build supports bx, by in {64, 128}.
@@ -88,7 +96,8 @@ typedef struct bsa_executor bsa_executor; /* opaque, host side */
  *   q_layout, kv_layout        : "BNSD" or "TND"; must be equal.
  *   num_key_value_heads        : N2; N1 % N2 == 0; query head h uses key head
  *                                h / (N1/N2), and dK/dV sum over the group.
- *   mask_type                  : must be 0.
+ *   mask_type                  : 0 = no token mask (atten_mask NULL); 1 = apply
+ *                                atten_mask. Other values are rejected.
  *   pre_tokens, next_tokens    : sliding window (parameter table rows preTokens /
  *                                nextTokens; window edges as on the
  *                                FlashAttentionScore page, 参数说明): query s and
@@ -130,16 +139,18 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
  * over the selected blocks) * V and softmaxLse = natural-log logsumexp of the
  * scaled selected scores (page formulas 计算公式, forward part; online-softmax
  * update as in the FlashAttentionScore page, section 实现原理). Arguments as in
- * bsa_grad_workspace_size (pre_tokens / next_tokens: the same sliding window).
- * Query rows with no selected key inside the window (and BNSD padding rows)
+ * bsa_grad_workspace_size (atten_mask / mask_type and pre_tokens / next_tokens:
+ * the same token mask and sliding window). Query rows with no selected key that
+ * the window and the token mask keep (and BNSD padding rows)
  * get Out = 0 and lse = -inf. Out has the dtype of query, lse is F32. */
 bsa_status bsa_fwd_workspace_size(
     const bsa_tensor* query, const bsa_tensor* key, const bsa_tensor* value,
-    const bsa_tensor* block_sparse_mask, const int64_t* block_shape, int64_t block_shape_len,
+    const bsa_tensor* block_sparse_mask, const bsa_tensor* atten_mask,
+    const int64_t* block_shape, int64_t block_shape_len,
     const int64_t* actual_seq_lengths, int64_t n_seq,
     const int64_t* actual_seq_lengths_kv, int64_t n_seq_kv,
     const char* q_layout, const char* kv_layout, int64_t num_key_value_heads,
-    double scale_value, int64_t pre_tokens, int64_t next_tokens,
+    int64_t mask_type, double scale_value, int64_t pre_tokens, int64_t next_tokens,
     const bsa_tensor* attention_out, const bsa_tensor* softmax_lse,
     uint64_t* workspace_size, bsa_executor** executor);
 

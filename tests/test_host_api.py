@@ -70,6 +70,26 @@ def test_windows_that_overlap_the_diagonal_are_accepted(lib, pre, nxt):
     assert st == (0 if torch.cuda.is_available() else B.BSA_ERR_RUNTIME)
 
 
+def test_atten_mask_with_mask_type_1_is_accepted(lib):
+    kw = _grad_args()
+    kw.update(atten_mask=torch.zeros(300, 260, dtype=torch.bool), mask_type=1)
+    assert _status(**kw) == (0 if torch.cuda.is_available() else B.BSA_ERR_RUNTIME)
+
+
+@pytest.mark.parametrize("am,mt", [
+    (torch.zeros(256, 256, dtype=torch.uint8), 0),        # a mask needs maskType 1
+    (None, 1),                                            # maskType 1 needs a mask
+    (torch.zeros(256, 256, dtype=torch.uint8), 2),        # unknown maskType
+    (torch.zeros(1, 256, 256, dtype=torch.uint8), 1),     # not 2-D
+    (torch.zeros(255, 256, dtype=torch.uint8), 1),        # smaller than [maxSq, maxSkv]
+    (torch.zeros(256, 256, dtype=torch.float16), 1),      # not BOOL/UINT8
+])
+def test_invalid_atten_mask(lib, am, mt):
+    kw = _grad_args()
+    kw.update(atten_mask=am, mask_type=mt)
+    assert _status(**kw) == B.BSA_ERR_PARAM_INVALID
+
+
 def test_null_required_tensors(lib):
     for name in ("dout", "query", "key", "value", "attention_out"):
         kw = _grad_args()
