@@ -174,14 +174,15 @@ def make_inputs(w, dev):
     dt = torch_dtype(w.dtype)
     dout, q, k, v = (torch.from_numpy(x).to(dt).to(dev) for x in w.tensors())
     mask = None if w.mask is None else torch.from_numpy(w.mask).to(dev)
+    am = None if w.atten_mask is None else torch.from_numpy(w.atten_mask).to(dev)
     seq = dict(actual_seq_lengths=w.seq_q, actual_seq_lengths_kv=w.seq_kv)
     out, lse, fws = bsa.block_sparse_attention_fwd(q, k, v, block_sparse_mask=mask,
                                                  block_shape=[w.bx, w.by], layout=w.layout,
                                                  num_key_value_heads=w.N2, scale_value=w.scale,
-                                                 **seq, **w.window_kw())
+                                                 atten_mask=am, **seq, **w.window_kw())
     bsa.bsa_check_status(fws)
     return dict(dout=dout, query=q, key=k, value=v, attention_out=out, softmax_lse=lse,
-                block_sparse_mask=mask), seq
+                block_sparse_mask=mask, atten_mask=am), seq
 
 
 DETERMINISTIC = False  # set from --deterministic
@@ -191,9 +192,10 @@ def grad_executor(w, t, seq, dq, dk, dv):
     import block_sparse_attention_attn_gb300 as bsa
     size, ex = bsa.bsa_grad_workspace_size(
         t["dout"], t["query"], t["key"], t["value"], t["attention_out"], t["softmax_lse"],
-        t["block_sparse_mask"], None, [w.bx, w.by], seq["actual_seq_lengths"],
-        seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, 0, w.scale,
-        w.pre_tokens, w.next_tokens, dq=dq, dk=dk, dv=dv)
+        t["block_sparse_mask"], t["atten_mask"], [w.bx, w.by], seq["actual_seq_lengths"],
+        seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2,
+        0 if t["atten_mask"] is None else 1, w.scale, w.pre_tokens, w.next_tokens,
+        dq=dq, dk=dk, dv=dv)
     if DETERMINISTIC:
         ex.set_deterministic(True)
     return size, ex
@@ -298,7 +300,8 @@ def bench_ours(args, rank, world, local):
                    "gflop_per_step": round(flops / 1e9, 2), "parallelism": f"replicas x{world}",
                    "l2": "flushed (512 MB write) before every timed step",
                    "dq_mode": "deterministic (query-tile pass)" if DETERMINISTIC else "fp32 reduce-add",
-                   "window": ([w.pre_tokens, w.next_tokens] if w.windowed() else None)},
+                   "window": ([w.pre_tokens, w.next_tokens] if w.windowed() else None),
+                   "atten_mask": (w.atten_mask_desc or None)},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -343,10 +346,11 @@ def _oracle_sample(w, heads, S):
     from block_sparse_attention_attn_gb300.workloads import Workload
     mask = None if w.mask is None else w.mask[:1, :heads, :-(-S // w.bx), :-(-S // w.by)]
     lse = np.full((1, heads, S, 1), math.log(S) + 2.0)
+    am = None if w.atten_mask is None else w.atten_mask[:S, :S]
     kw = dict(mask=mask, block_shape=(w.bx, w.by), num_kv_heads=g_heads, scale=w.scale,
-              **w.window_kw())
+              atten_mask=am, **w.window_kw())
     sample = Workload(w.name, "BNSD", w.dtype, 1, heads, g_heads, w.D, w.bx, w.by, [S], [S], S, S,
-                      w.scale, mask, **w.window_kw())
+                      w.scale, mask, atten_mask=am, **w.window_kw())
     return (dout, q, k, v, out, lse), kw, sample.flops()
 
 

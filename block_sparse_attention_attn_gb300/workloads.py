@@ -26,7 +26,10 @@ w4    BNSD bf16 B1 N8 Nkv8 S65536 D128, 128x128, top-k style rows: the
 
 With a sliding window (preTokens / nextTokens): ``w2causal`` is w2 with
 nextTokens = 0 (token-level causal inside the diagonal blocks), ``w1causal``
-is w1dense with nextTokens = 0 (dense causal attention).
+is w1dense with nextTokens = 0 (dense causal attention). With a token mask
+(attenMask, 1 = masked): ``w1doc`` is w1dense with causal documents of
+200-1500 tokens (a pair is masked across documents and above the diagonal:
+packed-document training).
 
 Values are N(0, 1) (w3: standard deviation 0.5), drawn from numpy's PCG64 and
 rounded to the input dtype with round-to-nearest-even.
@@ -39,7 +42,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["Workload", "WORKLOADS", "make_workload", "normal", "random_mask",
-           "ceil_div", "NO_WINDOW", "window_pairs"]
+           "ceil_div", "NO_WINDOW", "window_pairs", "document_mask"]
 
 NO_WINDOW = 2147483647   # preTokens / nextTokens value of "no sliding window"
 
@@ -77,9 +80,14 @@ class Workload:
     seed: int = 0
     pre_tokens: int = NO_WINDOW     # sliding window: query s sees keys
     next_tokens: int = NO_WINDOW    # s - pre_tokens .. s + next_tokens
+    atten_mask: Optional[np.ndarray] = None   # uint8 [Sq, Skv], 1 = masked (maskType 1)
+    atten_mask_desc: str = ""
 
     def windowed(self) -> bool:
         return not (self.pre_tokens >= self.Sq - 1 and self.next_tokens >= self.Skv - 1)
+
+    def token_masked(self) -> bool:
+        return self.windowed() or self.atten_mask is not None
 
     def window_kw(self) -> dict:
         return dict(pre_tokens=self.pre_tokens, next_tokens=self.next_tokens)
@@ -121,23 +129,25 @@ class Workload:
         n = 0
         for b in range(self.B):
             sel = self._selected_per_block(b)
-            if self.windowed():
+            if self.token_masked():
                 sel = sel * (window_pairs(self.seq_q[b], self.seq_kv[b], self.bx, self.by,
-                                          self.pre_tokens, self.next_tokens) > 0)
+                                          self.pre_tokens, self.next_tokens,
+                                          self.atten_mask) > 0)
             n += int(sel.sum())
         return n
 
     def flops(self) -> float:
         """Algorithmic backward FLOPs: 10*D per (query, key) pair that takes
         part, per q-head (5 products of 2*D each: S, dP, dV, dQ, dK). Without a
-        window a selected block counts as bx*by pairs (tail blocks included);
-        with one only the pairs inside the window and the lengths count."""
-        if not self.windowed():
+        window or token mask a selected block counts as bx*by pairs (tail
+        blocks included); with one only the pairs they keep inside the lengths
+        count."""
+        if not self.token_masked():
             return 10.0 * self.bx * self.by * self.D * self.active_blocks()
         pairs = 0
         for b in range(self.B):
             wp = window_pairs(self.seq_q[b], self.seq_kv[b], self.bx, self.by,
-                              self.pre_tokens, self.next_tokens)
+                              self.pre_tokens, self.next_tokens, self.atten_mask)
             pairs += int((self._selected_per_block(b) * wp).sum())
         return 10.0 * self.D * pairs
 
@@ -156,10 +166,18 @@ class Workload:
         return dout, q, k, v
 
 
-def window_pairs(lq, lk, bx, by, pre, nxt):
+def window_pairs(lq, lk, bx, by, pre, nxt, atten_mask=None):
     """[ceil(lq/bx), ceil(lk/by)] int64: per block, the (s, t) pairs with s < lq,
-    t < lk and s - pre <= t <= s + nxt (geometry for FLOP counting)."""
+    t < lk, s - pre <= t <= s + nxt and (with a token mask) atten_mask[s, t] == 0
+    (geometry for FLOP counting)."""
     mq, mk = ceil_div(lq, bx), ceil_div(lk, by)
+    if atten_mask is not None:
+        s = np.arange(lq, dtype=np.int64)[:, None]
+        t = np.arange(lk, dtype=np.int64)[None, :]
+        keep = (t >= s - min(int(pre), 1 << 40)) & (t <= s + min(int(nxt), 1 << 40))
+        keep &= np.asarray(atten_mask)[:lq, :lk] == 0
+        keep = np.pad(keep, ((0, mq * bx - lq), (0, mk * by - lk)))
+        return keep.reshape(mq, bx, mk, by).sum(axis=(1, 3)).astype(np.int64)
     s = np.arange(lq, dtype=np.int64)[:, None]
     t0 = (np.arange(mk, dtype=np.int64) * by)[None, :]
     t1 = np.minimum(t0 + by, lk) - 1
@@ -169,6 +187,20 @@ def window_pairs(lq, lk, bx, by, pre, nxt):
     pad = mq * bx - lq
     per_row = np.concatenate([per_row, np.zeros((pad, mk), np.int64)])
     return per_row.reshape(mq, bx, mk).sum(axis=1)
+
+
+def document_mask(S, Skv, seed, lo=40, hi=300, causal=True):
+    """uint8 [S, Skv] token mask (1 = masked) of documents with lengths drawn
+    uniformly from [lo, hi): a pair is masked when query and key lie in
+    different documents and, with ``causal``, when the key comes later."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = max(S, Skv)
+    cuts = np.cumsum(rng.integers(lo, hi, size=n // lo + 2))
+    doc = np.searchsorted(cuts, np.arange(n), side="right")
+    am = doc[:S, None] != doc[None, :Skv]
+    if causal:
+        am |= np.arange(Skv)[None, :] > np.arange(S)[:, None]
+    return am.astype(np.uint8)
 
 
 def random_mask(rng, B, N, Mq, Mk, p, diag=True):
@@ -252,6 +284,13 @@ def _w4():
                     D ** -0.5, m, seed=2004)
 
 
+def _documents(w, name):
+    w.name = name
+    w.atten_mask = document_mask(w.Sq, w.Skv, 1601, lo=200, hi=1500)
+    w.atten_mask_desc = "causal documents of U[200,1500) tokens (seed 1601), 1 = masked"
+    return w
+
+
 def _causal(w, name):
     w.name = name
     w.next_tokens = 0
@@ -267,6 +306,7 @@ WORKLOADS = {
     "w4": _w4,
     "w2causal": lambda: _causal(_w2(), "w2causal"),
     "w1causal": lambda: _causal(_w1(dense=True), "w1causal"),
+    "w1doc": lambda: _documents(_w1(dense=True), "w1doc"),
 }
 
 
