@@ -8,16 +8,22 @@
 // other CTAs finish: no fp32 reduce-adds, the same bits on every run. The
 // key-tile-stationary kernel then computes dK and dV only.
 //
-// One persistent CTA per SM, 192 threads:
-//   warp 4      producer: Q and dO of the query tile, then K/V tiles of the
+// One persistent CTA per SM, 320 threads:
+//   warp 8      producer: Q and dO of the query tile, then K/V tiles of the
 //               selected key tiles (found by scanning the mask row) through a
 //               2-stage TMA ring;
-//   warp 5      MMA issuer and TMEM owner: S = Q K^T, dP = dO V^T (shared-
-//               memory operands), dQ += dS K (dS read from TMEM);
-//   warps 0-3   TMEM lane s = query row s: P and dS (lse and D are per-thread
-//               values here), then the dQ epilogue.
-// TMEM columns: [0,128) S, then dS packed in place; [128,256) dP;
-// [256,256+D) dQ.
+//   warp 9      MMA issuer and TMEM owner. Per key tile m it issues S(m) =
+//               Q K^T into one of two S buffers, dP(m) = dO V^T once the
+//               softmax warps have read dP(m-1), then dQ += dS(m-1) K(m-1)
+//               (dS read from TMEM): the tensor cores compute tile m while
+//               the softmax warps work on tile m-1;
+//   warps 0-7   two warpgroups, TMEM lane s = query row s, warpgroup wg owns
+//               keys [64 wg, 64 wg + 64): P and dS (lse and D are per-thread
+//               values here), then the dQ epilogue (columns split by wg).
+// TMEM columns: [0,128) and [128,256) S, with dS packed in place (keys 0-63
+// at the buffer's columns [0,32), keys 64-127 at [96,128), so neither
+// warpgroup overwrites S values the other still reads); [256,384) dP;
+// [384,384+D) dQ.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -28,16 +34,20 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kProdWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kPanel = 128 * 128;
-constexpr uint32_t kColS = 0, kColP = 128, kColQ = 256;
+constexpr uint32_t kColS0 = 0, kColP = 256, kColQ = 384;
+
+// TMEM column of the packed dS of keys [16 kk, 16 kk + 16) inside an S buffer.
+__host__ __device__ constexpr uint32_t ds_col(int kk) { return (kk >> 2) * 96 + (kk & 3) * 8; }
 
 enum Bar {
   kQFull = 0, kQAux, kQEmpty,
   kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kKvAux0, kKvAux1,
-  kSFull, kDpFull, kDsReady, kDqStep, kDqFull, kDqEmpty,
+  kSFull0, kSFull1, kSFree0, kSFree1, kDpFull, kDpFree, kDsReady, kDqFull, kDqEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
   kDrain,
   kNumBars
@@ -66,7 +76,9 @@ struct Elem<kDtBF16> {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
-  __device__ static float round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+  __device__ static float2 unpack(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+  }
 };
 template <>
 struct Elem<kDtF16> {
@@ -76,7 +88,9 @@ struct Elem<kDtF16> {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
   }
-  __device__ static float round(float x) { return __half2float(__float2half_rn(x)); }
+  __device__ static float2 unpack(uint32_t u) {
+    return __half22float2(*reinterpret_cast<__half2*>(&u));
+  }
 };
 
 __device__ __forceinline__ void record_error(int* header, int where) {
@@ -163,17 +177,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kQEmpty], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kKvFull0 + i], 1);
-      mbar_init(&bars[kKvEmpty0 + i], 5);  // MMA (commit or arrive) + 4 softmax warps
+      mbar_init(&bars[kKvEmpty0 + i], 1 + kSoftmaxWarps);  // MMA (commit or arrive) + softmax warps
       mbar_init(&bars[kKvAux0 + i], 1);
       mbar_init(&bars[kItemFull0 + i], 1);
-      mbar_init(&bars[kItemEmpty0 + i], 5);
+      mbar_init(&bars[kItemEmpty0 + i], 1 + kSoftmaxWarps);
+      mbar_init(&bars[kSFull0 + i], 1);   // S MMA commit
+      mbar_init(&bars[kSFree0 + i], 1);   // dQ MMA commit: the buffer's dS was read
     }
-    mbar_init(&bars[kSFull], 1);
     mbar_init(&bars[kDpFull], 1);
-    mbar_init(&bars[kDsReady], 4);
-    mbar_init(&bars[kDqStep], 1);
+    mbar_init(&bars[kDpFree], kSoftmaxWarps);   // dP read out of TMEM
+    mbar_init(&bars[kDsReady], kSoftmaxWarps);
     mbar_init(&bars[kDqFull], 1);
-    mbar_init(&bars[kDqEmpty], 4);
+    mbar_init(&bars[kDqEmpty], kSoftmaxWarps);
     mbar_init(&bars[kDrain], 1);
     mbar_fence_init();
   }
@@ -330,9 +345,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     uint32_t n = 0, itc = 0;  // n: K/V stages (end markers included)
-    uint32_t m = 0;           // m: computed key tiles
+    uint32_t m = 0;           // m: computed key tiles (S buffer m & 1)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO);
+    // dQ += dS(mm) K: A = dS in S buffer mm & 1 (TMEM), B = K of stage kst
+    // (MN-major); `first` starts the item's accumulator
+    auto issue_dq = [&](uint32_t mm, int kst, bool first) {
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t dKmn = sdesc_sw128(smem_u32(sK0 + kst * S::kTileBytes), kPanel, 1024);
+        const uint32_t sb = kColS0 + 128 * (mm & 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + kColQ, tmem + sb + ds_col(k), dKmn + (uint64_t)((k * 2048) >> 4), kIdQ,
+                 (first && k == 0) ? 0u : 1u);
+        tc_commit(&bars[kSFree0 + (mm & 1)]);
+        tc_commit(&bars[kKvEmpty0 + kst]);
+      }
+      __syncwarp();
+    };
     while (true) {
       const int slot = itc & 1;
       if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
@@ -341,32 +372,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
       if (idx < 0) break;
       if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
-      int j = 0;
+      int j = 0, st_prev = 0;
       while (true) {
         const int st = n & 1;
         if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         if (mt < 0) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+          if (lane == 0) {
+            mbar_arrive(&bars[kKvEmpty0 + st]);
+            tc_commit(&bars[kQEmpty]);  // Q and dO: their last readers are issued
+          }
+          __syncwarp();
           ++n;
           break;
         }
-        // the S columns hold dS of the previous key tile until its dQ MMA
-        // has read them
-        if (m > 0 && !mbar_wait(&bars[kDqStep], (m - 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        const uint32_t sb = kColS0 + 128 * (m & 1);
+        // the S buffer is free once the dQ MMA of tile m-2 has read its dS
+        if (!mbar_wait(&bars[kSFree0 + (m & 1)], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
         const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
         if (lane == 0) {
           const uint64_t dQk = sdesc_sw128(aQ, 16, 1024), dKk = sdesc_sw128(aK, 16, 1024);
-          const uint64_t dOk = sdesc_sw128(adO, 16, 1024), dVk = sdesc_sw128(aV, 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint64_t off = (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
-            mma_ss(tmem + kColS, dQk + off, dKk + off, kIdS, k > 0);
+            mma_ss(tmem + sb, dQk + off, dKk + off, kIdS, k > 0);
           }
-          tc_commit(&bars[kSFull]);
+          tc_commit(&bars[kSFull0 + (m & 1)]);
+        }
+        __syncwarp();
+        // dP has one buffer: the softmax warps must have read dP(m-1)
+        if (!mbar_wait(&bars[kDpFree], (m & 1) ^ 1, abort_flag)) { where = kErrWaitDP; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t dOk = sdesc_sw128(adO, 16, 1024), dVk = sdesc_sw128(aV, 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint64_t off = (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
@@ -375,32 +416,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&bars[kDpFull]);
         }
         __syncwarp();
-        if (!mbar_wait(&bars[kDsReady], m & 1, abort_flag)) { where = kErrWaitDS; break; }
-        // the first dQ MMA of an item overwrites the accumulator: the previous
-        // item's epilogue must have read it
-        if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
-        tc_fence_after();
-        if (lane == 0) {  // dQ += dS K: A = dS (TMEM, packed in the S columns), B = K (MN-major)
-          const uint64_t dKmn = sdesc_sw128(aK, kPanel, 1024);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColQ, tmem + kColS + 8 * k, dKmn + (uint64_t)((k * 2048) >> 4), kIdQ,
-                   (j == 0 && k == 0) ? 0u : 1u);
-          tc_commit(&bars[kDqStep]);
-          tc_commit(&bars[kKvEmpty0 + st]);
+        if (j > 0) {  // dQ of the previous key tile, while the softmax works on this one
+          if (!mbar_wait(&bars[kDsReady], (m - 1) & 1, abort_flag)) { where = kErrWaitDS; break; }
+          // the first dQ MMA of an item overwrites the accumulator: the
+          // previous item's epilogue must have read it
+          if (j == 1 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+          issue_dq(m - 1, st_prev, j == 1);
         }
-        __syncwarp();
+        st_prev = st;
         ++j;
         ++n;
         ++m;
       }
       if (where) break;
-      // every item waits for the previous epilogue exactly once
-      if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
-      if (lane == 0) {
-        tc_commit(&bars[kDqFull]);
-        tc_commit(&bars[kQEmpty]);
+      if (j > 0) {  // the item's last key tile
+        if (!mbar_wait(&bars[kDsReady], (m - 1) & 1, abort_flag)) { where = kErrWaitDS; break; }
+        if (j == 1 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        issue_dq(m - 1, st_prev, j == 1);
+      } else if (!mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) {  // once per item
+        where = kErrWaitAcc;
+        break;
       }
+      if (lane == 0) tc_commit(&bars[kDqFull]);
       __syncwarp();
       ++itc;
     }
@@ -412,8 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ----------------------------------------------------- P, dS, epilogue
-    const int s = warp * 32 + lane;  // query row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int qd = warp & 3, wg = warp >> 2;
+    const int s = qd * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     uint32_t n = 0, itc = 0, m = 0;
     int where = 0;
     while (true) {
@@ -432,70 +470,85 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse2 = s_ok ? p.lse2[prow] : 0.f;
       const float dsum = s_ok ? p.dvec[prow] : 0.f;
       const int s_sub = p.rb == 2 ? (s >> 6) : 0;
+      const int t_sub = p.cb == 2 ? wg : 0;  // this warpgroup's keys lie in one key block
       int j = 0;
       while (true) {
         const int st = n & 1;
         if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
         if (mt < 0) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
           ++n;
           break;
         }
         const int jt = mt & 0xFFFFFF, bits = mt >> 24;
-        if (!mbar_wait(&bars[kSFull], m & 1, abort_flag)) { where = kErrWaitS; break; }
-        if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
-        tc_fence_after();
-        // live key columns [t_lo, t_hi): inside the key length and the window;
-        // amw: token mask bits of this row's 128 keys (bit set = masked)
+        // live key columns [t_lo, t_hi) of the tile (key length and window),
+        // restricted to this warpgroup's 64; amw: token mask bits (set = masked)
         int t_lo = 0, t_hi = Lk - jt * 128;
         if (p.win) {
           const int2 w = win_span(srow, (int64_t)jt * 128, -p.win_pre, p.win_next);
           t_lo = w.x;
           t_hi = min(t_hi, w.y);
         }
-        uint4 amw = make_uint4(0u, 0u, 0u, 0u);
+        uint2 amw = make_uint2(0u, 0u);
         if (p.am)
-          amw = *reinterpret_cast<const uint4*>(p.am_row + (int64_t)srow * p.am_wk + 4 * jt);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t x[32], y[32];
-          tmem_ld32(tmem + lane_off + kColS + 32 * c, x);
-          tmem_ld32(tmem + lane_off + kColP + 32 * c, y);
-          const uint32_t aw = c == 0 ? amw.x : c == 1 ? amw.y : c == 2 ? amw.z : amw.w;
+          amw = *reinterpret_cast<const uint2*>(p.am_row + (int64_t)srow * p.am_wk + 4 * jt + 2 * wg);
+        const bool row_on = s_ok && ((bits >> (s_sub * 2 + t_sub)) & 1);
+        const uint32_t live0 = row_on ? bit_range(t_lo - 64 * wg, t_hi - 64 * wg) & ~amw.x : 0u;
+        const uint32_t live1 = row_on ? bit_range(t_lo - 64 * wg - 32, t_hi - 64 * wg - 32) & ~amw.y : 0u;
+        const uint32_t sb = kColS0 + 128 * (m & 1);
+        if (!mbar_wait(&bars[kSFull0 + (m & 1)], (m >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
+        tc_fence_after();
+        // P of this warpgroup's 64 keys, rounded to the operand type as in the
+        // dV/dK kernel, kept packed in registers
+        uint32_t Ppk[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t x[32];
+          tmem_ld32(tmem + lane_off + sb + 64 * wg + 32 * c, x);
+          const uint32_t live = c ? live1 : live0;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float pv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const bool on = (live >> (2 * k + u)) & 1u;
+              pv[u] = on ? ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)) : 0.f;
+            }
+            Ppk[16 * c + k] = E::pack(pv[0], pv[1]);
+          }
+        }
+        if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
+        tc_fence_after();
+        uint32_t y[2][32];
+        tmem_ld32(tmem + lane_off + kColP + 64 * wg, y[0]);
+        tmem_ld32(tmem + lane_off + kColP + 64 * wg + 32, y[1]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kDpFree]);  // the MMA may write dP(m+1)
+        // dS = P o (dP - D), packed in place over this warpgroup's S columns
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            float ds[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int t = 32 * c + 2 * k + u;
-              const int t_sub = p.cb == 2 ? (t >> 6) : 0;
-              const bool on = s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1) &&
-                              !((aw >> (2 * k + u)) & 1u);
-              // P rounded to the operand type, as in the dV/dK kernel
-              const float pv =
-                  on ? E::round(ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)))
-                     : 0.f;
-              ds[u] = on ? pv * (__uint_as_float(y[2 * k + u]) - dsum) : 0.f;
-            }
-            pk[k] = E::pack(ds[0], ds[1]);
+            const float2 pp = E::unpack(Ppk[16 * c + k]);
+            pk[k] = E::pack(pp.x * (__uint_as_float(y[c][2 * k]) - dsum),
+                            pp.y * (__uint_as_float(y[c][2 * k + 1]) - dsum));
           }
-          tmem_st16(tmem + lane_off + kColS + 16 * c, pk);
+          tmem_st16(tmem + lane_off + sb + 96 * wg + 16 * c, pk);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars[kDsReady]);
-          mbar_arrive(&bars[kKvEmpty0 + st]);
-        }
+        if (lane == 0) mbar_arrive(&bars[kDsReady]);
         ++j;
         ++n;
         ++m;
       }
       if (where) break;
-      // epilogue: dQ = scale * accumulator (zeros when no key tile was selected)
+      // epilogue: dQ = scale * accumulator (zeros when no key tile was
+      // selected); warpgroup wg writes the columns [wg D/2, wg D/2 + D/2)
       if (!mbar_wait(&bars[kDqFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const bool write_row = p.layout == kLayoutBNSD ? (srow < p.Sq) : s_ok;
@@ -510,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       T* out = static_cast<T*>(p.dq) + ooff;
       const float mul = (s_ok && j > 0) ? p.scale : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         uint32_t o[32];
         if (j > 0) {
           tmem_ld32(tmem + lane_off + kColQ + 32 * c, o);
