@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic dQ mode (separate query-tile pass)")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the companion forward (bsa_fwd) instead of the backward")
     return ap.parse_args()
 
 
@@ -329,6 +331,121 @@ def bench_ours(args, rank, world, local):
     return line
 
 
+# ------------------------------------------------- companion forward arm
+FWD_METRIC = "block-sparse attn fwd TFLOP/s (companion forward, active blocks)"
+
+
+def bench_forward(args, rank, world, local):
+    """The same protocol for bsa_fwd: Out and lse of one workload per step;
+    4*D FLOP per (query, key) pair per query head (S = QK^T and O = PV)."""
+    import torch
+
+    import block_sparse_attention_attn_gb300 as bsa
+    from block_sparse_attention_attn_gb300.workloads import make_workload
+    dev = torch.device("cuda", local)
+    w = make_workload(args.workload)
+    flops = 0.4 * w.flops()
+    t, seq = make_inputs(w, dev)
+    q, k, v = t["query"], t["key"], t["value"]
+    out, lse = torch.empty_like(t["attention_out"]), torch.empty_like(t["softmax_lse"])
+
+    def fwd_executor():
+        return bsa.bsa_fwd_workspace_size(
+            q, k, v, t["block_sparse_mask"], [w.bx, w.by], seq["actual_seq_lengths"],
+            seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, w.scale, w.pre_tokens,
+            w.next_tokens, out, lse, t["atten_mask"])
+
+    size, _ = fwd_executor()
+    ws = torch.empty(size, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        bsa.bsa_fwd(ws, size, fwd_executor()[1], stream)
+    torch.cuda.synchronize()
+    bsa.bsa_check_status(ws)
+    n = args.steps
+    exs = [fwd_executor()[1] for _ in range(n)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    for e in ev:
+        e[1].record(stream)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        exs[i].set_timing_events(ev[i][1], ev[i][2])
+        bsa.bsa_fwd(ws, size, exs[i], stream)
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    bsa.bsa_check_status(ws)
+    ms_step = max_over_ranks(float(np.mean([e[0].elapsed_time(e[3]) for e in ev])), world)
+    ms_kern = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
+    # end to end: pinned host Q, K, V (and masks) -> H2D -> both stages -> D2H of Out, lse
+    host = {k_: t[k_].cpu().pin_memory() for k_ in ("query", "key", "value", "block_sparse_mask",
+                                                   "atten_mask") if t[k_] is not None}
+    h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (out, lse)]
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    times = []
+    for i in range(max(3, min(n, 20)) + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k_, x in host.items():
+            t[k_].copy_(x, non_blocking=True)
+        bsa.bsa_fwd(ws, size, fwd_executor()[1], stream)
+        for hd, dd in zip(h_out, (out, lse)):
+            hd.copy_(dd, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i > 0:
+            times.append(a.elapsed_time(b))
+    e2e_ms = max_over_ranks(float(np.mean(times)), world)
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
+    achieved = flops / (ms_kern * 1e-3) / 1e12
+    line = {
+        "metric": FWD_METRIC, "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
+        "unit": UNIT, "n_gpus": world, "steps": n, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded PCG64 N(0,1) inputs)",
+        "config": {"workload": w.name, "pass": "forward", "gflop_per_step": round(flops / 1e9, 2),
+                   "parallelism": f"replicas x{world}",
+                   "l2": "flushed (512 MB write) before every timed step",
+                   "window": ([w.pre_tokens, w.next_tokens] if w.windowed() else None),
+                   "atten_mask": (w.atten_mask_desc or None)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "k_fwd (tcgen05 forward)", "kernel_ms": round(ms_kern, 4),
+                     "peak_source": f"{src}: MEASURED_PEAKS.json bf16_tflops (burst)"
+                     if src == "measured" else "fallback 1.9 PFLOP/s bf16"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": (3 if w.atten_mask is not None else 2) * n,  # info upload, [mask packing,] forward
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and rank == 0:
+        from oracle import bsa_oracle as O
+        S = min(w.Sq, 2048)
+        a, kw, fl = _oracle_sample(w, 1, S)
+        t0 = time.perf_counter()
+        O.forward(a[1], a[2], a[3], **kw)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(0.4 * fl / dt / 1e12, 6), "unit": UNIT,
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{w.name} batch 0, 1 query head, first {S} tokens "
+                                          f"({0.4 * fl / 1e9:.2f} GFLOP, {dt:.1f} s)"}
+    return line
+
+
 # ------------------------------------------------------- CPU oracle timings
 def _oracle_sample(w, heads, S):
     """The workload restricted to batch 0, the first `heads` query heads (and
@@ -413,7 +530,7 @@ def main():
     global DETERMINISTIC
     DETERMINISTIC = args.deterministic
     rank, world, local = dist_setup(args.gpus)
-    line = bench_ours(args, rank, world, local)
+    line = (bench_forward if args.forward else bench_ours)(args, rank, world, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -10,8 +10,12 @@
 //   warp 4      producer: scans the mask row(s) of its query tile for selected
 //               key tiles and streams K/V tiles through a 2-stage TMA ring;
 //   warp 5      MMA issuer (S = Q K^T into one of two TMEM buffers, O += P V
-//               with P read from TMEM) and TMEM owner;
-//   warps 0-3   softmax: TMEM lane s = query row s.
+//               with P read from TMEM) and TMEM owner; O += P(m-1) V(m-1) is
+//               issued after S(m), so the softmax of tile m overlaps both;
+//   warps 0-3   softmax: TMEM lane s = query row s; the live keys of a tile
+//               (length, window, sub-block, token mask) are one bit word per
+//               32 columns, and the 32-column chunks run in a rolled loop to
+//               keep the code small.
 // The rescale is lazy: O is only rescaled when a row max grows by more than
 // 8 (log2 units), so P stays below 2^8 and most tiles skip the TMEM round trip.
 #include <cuda_bf16.h>
@@ -295,6 +299,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t m = 0;           // m: computed key tiles (S/P buffers, PV commits)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ);
+    // O += P(mm) V: A = P (TMEM, packed in S buffer mm & 1), B = V of stage vst
+    // (MN-major); `first` starts the item's accumulator. false = a wait gave up.
+    auto issue_pv = [&](uint32_t mm, int vst, bool first) -> bool {
+      if (!mbar_wait(&bars[kPReady0 + (mm & 1)], (mm >> 1) & 1, abort_flag)) { where = kErrWaitP; return false; }
+      if (first && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; return false; }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t colS = (mm & 1) ? kColS1 : kColS0;
+        const uint32_t aV = smem_u32(sV0 + vst * S::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tmem + kColO, tmem + colS + 8 * k, sdesc_sw128(aV + k * 2048, kPanel, 1024), kIdO,
+                 (first && k == 0) ? 0u : 1u);
+        tc_commit(&bars[kPvDone0 + (mm & 1)]);
+        tc_commit(&bars[kKvEmpty0 + vst]);
+      }
+      __syncwarp();
+      return true;
+    };
     while (true) {
       const int slot = itc & 1;
       if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
@@ -304,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
       tc_fence_after();
-      int j = 0;
+      int j = 0, st_prev = 0;
       while (true) {
         const int st = n & 1;
         if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
@@ -315,11 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
           break;
         }
+        // S(m) into buffer m & 1 once the PV of tile m-2 has read its P
         const uint32_t sb = m & 1;
         if (!mbar_wait(&bars[kPvDone0 + sb], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
-        const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
         const uint32_t colS = sb ? kColS1 : kColS0;
         if (lane == 0) {
 #pragma unroll
@@ -330,26 +353,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&bars[kSFull0 + sb]);
         }
         __syncwarp();
-        if (!mbar_wait(&bars[kPReady0 + sb], (m >> 1) & 1, abort_flag)) { where = kErrWaitP; break; }
-        if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
-        tc_fence_after();
-        if (lane == 0) {  // O += P V: A = P (TMEM, packed in the S buffer), B = V (MN-major)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + kColO, tmem + colS + 8 * k, sdesc_sw128(aV + k * 2048, kPanel, 1024), kIdO,
-                   (j == 0 && k == 0) ? 0u : 1u);
-          tc_commit(&bars[kPvDone0 + sb]);
-          tc_commit(&bars[kKvEmpty0 + st]);
-        }
-        __syncwarp();
+        // O += P(m-1) V(m-1) after S(m) is queued, so the softmax of tile m
+        // overlaps with the tensor cores
+        if (j > 0 && !issue_pv(m - 1, st_prev, j == 1)) break;
+        st_prev = st;
         ++j;
         ++n;
         ++m;
       }
       if (where) break;
-      // every item waits for the previous epilogue exactly once (a parity wait
-      // cannot tell phase c from phase c-2, so no item may skip it)
-      if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+      if (j > 0) {
+        if (!issue_pv(m - 1, st_prev, j == 1)) break;
+      } else if (!mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
+        // every item waits for the previous epilogue exactly once (a parity
+        // wait cannot tell phase c from phase c-2, so no item may skip it)
+        where = kErrWaitAcc;
+        break;
+      }
       if (lane == 0) {
         tc_commit(&bars[kOFull]);
         tc_commit(&bars[kQEmpty]);
@@ -393,35 +413,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = sb ? kColS1 : kColS0;
         if (!mbar_wait(&bars[kSFull0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
-        // live columns [t_lo, t_hi): inside the key length and the sliding window
+        // live columns: inside the key length and the sliding window ([t_lo,
+        // t_hi)), in a selected key sub-block, kept by the token mask;
+        // live_bits(c) has bit k set when key 32c + k of the tile takes part
         int t_lo = 0, t_hi = Lk - jt * 128;
         if (p.win) {
           const int2 w = win_span((int64_t)fi.it * 128 + s, (int64_t)jt * 128, -p.win_pre, p.win_next);
           t_lo = w.x;
           t_hi = min(t_hi, w.y);
         }
-        // token mask bits of this row's 128 keys (bit set = masked)
-        uint4 amw = make_uint4(0u, 0u, 0u, 0u);
-        if (p.am)
-          amw = *reinterpret_cast<const uint4*>(p.am_row + (int64_t)(fi.it * 128 + s) * p.am_wk +
-                                                4 * jt);
+        const uint32_t* amr = p.am ? p.am_row + (int64_t)(fi.it * 128 + s) * p.am_wk + 4 * jt : nullptr;
         const int s_sub = p.rb == 2 ? (s >> 6) : 0;
-        // column t is live when t_lo <= t < t_hi, its key sub-block bit is set
-        // and the token mask keeps it
-        auto col_on = [&](int t) -> bool {
-          const int t_sub = p.cb == 2 ? (t >> 6) : 0;
-          const uint32_t aw = (t >> 5) == 0 ? amw.x : (t >> 5) == 1 ? amw.y : (t >> 5) == 2 ? amw.z : amw.w;
-          return s_ok && t >= t_lo && t < t_hi && ((bits >> (s_sub * 2 + t_sub)) & 1) &&
-                 !((aw >> (t & 31)) & 1u);
+        auto live_bits = [&](int c) -> uint32_t {
+          const int t_sub = p.cb == 2 ? (c >> 1) : 0;
+          if (!(s_ok && ((bits >> (s_sub * 2 + t_sub)) & 1))) return 0u;
+          const uint32_t b = bit_range(t_lo - 32 * c, t_hi - 32 * c);
+          return amr != nullptr ? b & ~amr[c] : b;
         };
         float mx = -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t x[32];
           tmem_ld32(tmem + lane_off + colS + 32 * c, x);
+          const uint32_t live = live_bits(c);
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            if (col_on(32 * c + k)) mx = fmaxf(mx, __uint_as_float(x[k]) * p.scale_log2);
+            mx = fmaxf(mx, ((live >> k) & 1u) ? __uint_as_float(x[k]) * p.scale_log2 : -INFINITY);
         }
         float m_use = m;
         const bool grow = mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY);
@@ -452,16 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
         }
         float rs = 0.f;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t x[32];
           tmem_ld32(tmem + lane_off + colS + 32 * c, x);
+          const uint32_t live = live_bits(c);
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            float p0 = 0.f, p1 = 0.f;
-            if (col_on(32 * c + 2 * k)) p0 = ex2_approx(__uint_as_float(x[2 * k]) * p.scale_log2 - m_use);
-            if (col_on(32 * c + 2 * k + 1)) p1 = ex2_approx(__uint_as_float(x[2 * k + 1]) * p.scale_log2 - m_use);
+            const float e0 = ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -m_use));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -m_use));
+            const float p0 = ((live >> (2 * k)) & 1u) ? e0 : 0.f;
+            const float p1 = ((live >> (2 * k + 1)) & 1u) ? e1 : 0.f;
             rs += p0 + p1;
             pk[k] = E::pack(p0, p1);
           }
