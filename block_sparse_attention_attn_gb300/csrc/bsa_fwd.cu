@@ -6,16 +6,18 @@
 // running row max m and sum l are updated per key tile and the partial PV
 // product is rescaled by exp(m_old - m_new) when the max grows.
 //
-// One persistent CTA per SM, 192 threads:
-//   warp 4      producer: scans the mask row(s) of its query tile for selected
+// One persistent CTA per SM, 320 threads:
+//   warp 8      producer: scans the mask row(s) of its query tile for selected
 //               key tiles and streams K/V tiles through a 2-stage TMA ring;
-//   warp 5      MMA issuer (S = Q K^T into one of two TMEM buffers, O += P V
+//   warp 9      MMA issuer (S = Q K^T into one of two TMEM buffers, O += P V
 //               with P read from TMEM) and TMEM owner; O += P(m-1) V(m-1) is
 //               issued after S(m), so the softmax of tile m overlaps both;
-//   warps 0-3   softmax: TMEM lane s = query row s; the live keys of a tile
-//               (length, window, sub-block, token mask) are one bit word per
-//               32 columns, and the 32-column chunks run in a rolled loop to
-//               keep the code small.
+//   warps 0-7   softmax, two warpgroups: TMEM lane s = query row s, warpgroup
+//               wg owns keys [64 wg, 64 wg + 64) of every tile and columns
+//               [wg D/2, wg D/2 + D/2) of O. The two halves of a row swap their
+//               partial maxima (and at the end their partial sums) through
+//               shared memory. The live keys of a tile (length, window,
+//               sub-block, token mask) are one bit word per 32 columns.
 // The rescale is lazy: O is only rescaled when a row max grows by more than
 // 8 (log2 units), so P stays below 2^8 and most tiles skip the TMEM round trip.
 #include <cuda_bf16.h>
@@ -28,9 +30,10 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kProdWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr float kRescaleThreshold = 8.f;
@@ -39,7 +42,7 @@ enum Bar {
   kQFull = 0, kQEmpty,
   kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kKvAux0, kKvAux1,
   kSFull0, kSFull1, kPReady0, kPReady1, kPvDone0, kPvDone1,
-  kOFull, kOEmpty,
+  kOFull, kOEmpty, kXch0, kXch1, kLx,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
   kDrain,
   kNumBars
@@ -51,7 +54,9 @@ struct Smem {
   static constexpr int oQ = 0;
   static constexpr int oK = oQ + kTileBytes;       // [2]
   static constexpr int oV = oK + 2 * kTileBytes;   // [2]
-  static constexpr int oBar = oV + 2 * kTileBytes;
+  static constexpr int oXch = oV + 2 * kTileBytes;  // float [2][2][128] partial row maxima
+  static constexpr int oLx = oXch + 2048;           // float [2][2][128] partial row sums
+  static constexpr int oBar = oLx + 2048;
   static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;  // int4 slots need 16 B
   static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
   static constexpr int kBytes = oMisc + 128;
@@ -162,16 +167,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kQEmpty], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kKvFull0 + i], 1);
-      mbar_init(&bars[kKvEmpty0 + i], 5);  // MMA + 4 softmax warps
+      mbar_init(&bars[kKvEmpty0 + i], 1 + kSoftmaxWarps);  // MMA + softmax warps
       mbar_init(&bars[kKvAux0 + i], 1);
       mbar_init(&bars[kSFull0 + i], 1);
-      mbar_init(&bars[kPReady0 + i], 4);
+      mbar_init(&bars[kPReady0 + i], kSoftmaxWarps);
+      mbar_init(&bars[kXch0 + i], 32 * kSoftmaxWarps);  // every softmax thread posts its max
       mbar_init(&bars[kPvDone0 + i], 1);
       mbar_init(&bars[kItemFull0 + i], 1);
-      mbar_init(&bars[kItemEmpty0 + i], 5);
+      mbar_init(&bars[kItemEmpty0 + i], 1 + kSoftmaxWarps);
     }
     mbar_init(&bars[kOFull], 1);
-    mbar_init(&bars[kOEmpty], 4);
+    mbar_init(&bars[kOEmpty], kSoftmaxWarps);
+    mbar_init(&bars[kLx], 32 * kSoftmaxWarps);
     mbar_init(&bars[kDrain], 1);
     mbar_fence_init();
   }
@@ -310,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aV = smem_u32(sV0 + vst * S::kTileBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColO, tmem + colS + 8 * k, sdesc_sw128(aV + k * 2048, kPanel, 1024), kIdO,
-                 (first && k == 0) ? 0u : 1u);
+          mma_ts(tmem + kColO, tmem + colS + (k >> 2) * 64 + (k & 3) * 8,
+                 sdesc_sw128(aV + k * 2048, kPanel, 1024), kIdO, (first && k == 0) ? 0u : 1u);
         tc_commit(&bars[kPvDone0 + (mm & 1)]);
         tc_commit(&bars[kKvEmpty0 + vst]);
       }
@@ -385,8 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int s = warp * 32 + lane;  // query row within the tile
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int qd = warp & 3, wg = warp >> 2;
+    const int s = qd * 32 + lane;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    float* xch = reinterpret_cast<float*>(smem + S::oXch);
+    float* lxch = reinterpret_cast<float*>(smem + S::oLx);
     uint32_t n = 0, itc = 0, m_step = 0;  // stages / computed key tiles (as in the MMA warp)
     int where = 0;
     while (true) {
@@ -399,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const FItem fi = decode(p, idx);
       const int Lq = p.lq[fi.b], Lk = p.lk[fi.b];
       const bool s_ok = fi.it * 128 + s < Lq;
-      float m = -INFINITY, l = 0.f;  // running max (log2 units) and sum
+      float m = -INFINITY, l = 0.f;  // running max (log2 units) and this warpgroup's sum
       int j = 0;
       while (true) {
         const int st = n & 1;
@@ -432,13 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
           uint32_t x[32];
           tmem_ld32(tmem + lane_off + colS + 32 * c, x);
           const uint32_t live = live_bits(c);
 #pragma unroll
           for (int k = 0; k < 32; ++k)
             mx = fmaxf(mx, ((live >> k) & 1u) ? __uint_as_float(x[k]) * p.scale_log2 : -INFINITY);
+        }
+        {  // the row's maximum over both halves
+          float* xb = xch + sb * 256;
+          xb[wg * 128 + s] = mx;
+          mbar_arrive(&bars[kXch0 + sb]);
+          if (!mbar_wait(&bars[kXch0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+          mx = fmaxf(mx, xb[(wg ^ 1) * 128 + s]);
         }
         float m_use = m;
         const bool grow = mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY);
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const float alpha = grow ? ex2_approx(m - mx) : 1.f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
             if (grow) {
@@ -470,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float rs = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
           uint32_t x[32];
           tmem_ld32(tmem + lane_off + colS + 32 * c, x);
           const uint32_t live = live_bits(c);
@@ -484,7 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs += p0 + p1;
             pk[k] = E::pack(p0, p1);
           }
-          tmem_st16(tmem + lane_off + colS + 16 * c, pk);
+          // P packed in place over this warpgroup's own S columns: keys
+          // 64 wg + 32 (c & 1) .. +31 at columns 64 wg + 16 (c & 1)
+          tmem_st16(tmem + lane_off + colS + 64 * wg + 16 * (c & 1), pk);
         }
         l += rs;
         tc_fence_before();
@@ -495,7 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++m_step;
       }
       if (where) break;
-      // epilogue: Out = O / l, lse = (m + log2 l) * ln 2
+      // epilogue: Out = O / l, lse = (m + log2 l) * ln 2, l summed over both halves
+      {
+        float* lb = lxch + (itc & 1) * 256;
+        lb[wg * 128 + s] = l;
+        mbar_arrive(&bars[kLx]);
+        if (!mbar_wait(&bars[kLx], itc & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        l += lb[(wg ^ 1) * 128 + s];
+      }
       if (!mbar_wait(&bars[kOFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const int srow = fi.it * 128 + s;
@@ -512,8 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sd = f.out_st[2];
       }
       T* out = static_cast<T*>(f.out) + ooff;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         uint32_t o[32];
         if (j > 0) tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
         if (write_row) {
@@ -537,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (write_row) {
+      if (write_row && wg == 0) {
         int64_t li;
         if (p.layout == kLayoutBNSD)
           li = ((int64_t)fi.b * p.N1 + fi.h) * p.Sq + srow;
