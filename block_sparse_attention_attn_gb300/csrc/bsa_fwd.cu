@@ -8,7 +8,7 @@
 //
 // One persistent CTA per SM, 320 threads:
 //   warp 8      producer: scans the mask row(s) of its query tile for selected
-//               key tiles and streams K/V tiles through a 2-stage TMA ring;
+//               key tiles and streams K/V tiles through a 3-stage TMA ring;
 //   warp 9      MMA issuer (S = Q K^T into one of two TMEM buffers, O += P V
 //               with P read from TMEM) and TMEM owner; O += P(m-1) V(m-1) is
 //               issued after S(m), so the softmax of tile m overlaps both;
@@ -37,12 +37,13 @@ constexpr int kMmaWarp = 9;
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr float kRescaleThreshold = 8.f;
+constexpr int kStages = 3;  // K/V ring depth
 
 enum Bar {
   kQFull = 0, kQEmpty,
-  kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kKvAux0, kKvAux1,
+  kKvFull0, kKvFull1, kKvFull2, kKvEmpty0, kKvEmpty1, kKvEmpty2, kKvAux0, kKvAux1, kKvAux2,
   kSFull0, kSFull1, kPReady0, kPReady1, kPvDone0, kPvDone1,
-  kOFull, kOEmpty, kXch0, kXch1, kLx,
+  kOFull, kOEmpty, kXch0, kXch1,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
   kDrain,
   kNumBars
@@ -52,11 +53,10 @@ template <int D>
 struct Smem {
   static constexpr int kTileBytes = (D / 64) * kPanel;
   static constexpr int oQ = 0;
-  static constexpr int oK = oQ + kTileBytes;       // [2]
-  static constexpr int oV = oK + 2 * kTileBytes;   // [2]
-  static constexpr int oXch = oV + 2 * kTileBytes;  // float [2][2][128] partial row maxima
-  static constexpr int oLx = oXch + 2048;           // float [2][2][128] partial row sums
-  static constexpr int oBar = oLx + 2048;
+  static constexpr int oK = oQ + kTileBytes;             // [kStages]
+  static constexpr int oV = oK + kStages * kTileBytes;   // [kStages]
+  static constexpr int oXch = oV + kStages * kTileBytes;  // float [2][2][128] partial row maxima / sums
+  static constexpr int oBar = oXch + 2048;
   static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;  // int4 slots need 16 B
   static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
   static constexpr int kBytes = oMisc + 128;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = misc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 1);
   int* item_slot = misc + 2;   // [2]
-  int* meta = misc + 4;        // [2] per stage: jt | bits << 24, -1 = end of item
+  int* meta = misc + 4;        // [kStages] per stage: jt | bits << 24, -1 = end of item
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -165,10 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_init(&bars[kQFull], 1);
     mbar_init(&bars[kQEmpty], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars[kKvFull0 + i], 1);
       mbar_init(&bars[kKvEmpty0 + i], 1 + kSoftmaxWarps);  // MMA + softmax warps
       mbar_init(&bars[kKvAux0 + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kSFull0 + i], 1);
       mbar_init(&bars[kPReady0 + i], kSoftmaxWarps);
       mbar_init(&bars[kXch0 + i], 32 * kSoftmaxWarps);  // every softmax thread posts its max
@@ -178,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars[kOFull], 1);
     mbar_init(&bars[kOEmpty], kSoftmaxWarps);
-    mbar_init(&bars[kLx], 32 * kSoftmaxWarps);
     mbar_init(&bars[kDrain], 1);
     mbar_fence_init();
   }
@@ -196,10 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t n = 0, itc = 0, aux[2] = {0u, 0u};
+    uint32_t n = 0, itc = 0, aux[kStages] = {0u, 0u, 0u};
     bool ok = true;
-    int pend_q = 0, pend_kv[2] = {0, 0}, pend_aux[2] = {0, 0};
-    uint32_t par_kv[2] = {0u, 0u};
+    int pend_q = 0, pend_kv[kStages] = {0, 0, 0}, pend_aux[kStages] = {0, 0, 0};
+    uint32_t par_kv[kStages] = {0u, 0u, 0u};
     while (ok) {
       const int slot = itc & 1;
       if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
@@ -239,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ball &= ball - 1;
           const int jsel = jt0 + src;
           const int bsel = __shfl_sync(0xffffffffu, bits, src);
-          const int st = n & 1;
-          if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+          const int st = n % kStages;
+          if (!mbar_wait(&bars[kKvEmpty0 + st], ((n / kStages) & 1) ^ 1, abort_flag)) {
             record_error(p.header, kErrWaitKV);
             ok = false;
             break;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           pend_kv[st] = tail ? 0 : 1;
-          par_kv[st] = (n >> 1) & 1;
+          par_kv[st] = (n / kStages) & 1;
           if (tail) {
             pend_aux[st] = 1;
             if (!mbar_wait(&bars[kKvAux0 + st], aux[st] & 1, abort_flag)) {
@@ -280,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // end-of-item marker
-      const int st = n & 1;
-      if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+      const int st = n % kStages;
+      if (!mbar_wait(&bars[kKvEmpty0 + st], ((n / kStages) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitKV);
         break;
       }
@@ -295,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (*abort_flag) {
       if (pend_q) mbar_wait_drain(&bars[kQFull], (itc & 1));
-      for (int st = 0; st < 2; ++st) {
+      for (int st = 0; st < kStages; ++st) {
         if (pend_kv[st]) mbar_wait_drain(&bars[kKvFull0 + st], par_kv[st]);
         if (pend_aux[st]) mbar_wait_drain(&bars[kKvAux0 + st], aux[st] & 1);
       }
@@ -336,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       int j = 0, st_prev = 0;
       while (true) {
-        const int st = n & 1;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int st = n % kStages;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         if (mt < 0) {
           __syncwarp();
@@ -396,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = qd * 32 + lane;  // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     float* xch = reinterpret_cast<float*>(smem + S::oXch);
-    float* lxch = reinterpret_cast<float*>(smem + S::oLx);
     uint32_t n = 0, itc = 0, m_step = 0;  // stages / computed key tiles (as in the MMA warp)
+    uint32_t xs = 0;                       // exchanges through xch (maxima per tile, sums per item)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
@@ -412,8 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f;  // running max (log2 units) and this warpgroup's sum
       int j = 0;
       while (true) {
-        const int st = n & 1;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int st = n % kStages;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
@@ -451,11 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = fmaxf(mx, ((live >> k) & 1u) ? __uint_as_float(x[k]) * p.scale_log2 : -INFINITY);
         }
         {  // the row's maximum over both halves
-          float* xb = xch + sb * 256;
+          float* xb = xch + (xs & 1) * 256;
           xb[wg * 128 + s] = mx;
-          mbar_arrive(&bars[kXch0 + sb]);
-          if (!mbar_wait(&bars[kXch0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+          mbar_arrive(&bars[kXch0 + (xs & 1)]);
+          if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
           mx = fmaxf(mx, xb[(wg ^ 1) * 128 + s]);
+          ++xs;
         }
         float m_use = m;
         const bool grow = mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY);
@@ -516,11 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (where) break;
       // epilogue: Out = O / l, lse = (m + log2 l) * ln 2, l summed over both halves
       {
-        float* lb = lxch + (itc & 1) * 256;
+        float* lb = xch + (xs & 1) * 256;
         lb[wg * 128 + s] = l;
-        mbar_arrive(&bars[kLx]);
-        if (!mbar_wait(&bars[kLx], itc & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        mbar_arrive(&bars[kXch0 + (xs & 1)]);
+        if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
         l += lb[(wg ^ 1) * 128 + s];
+        ++xs;
       }
       if (!mbar_wait(&bars[kOFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
