@@ -9,9 +9,10 @@
 // key-tile-stationary kernel then computes dK and dV only.
 //
 // One persistent CTA per SM, 320 threads:
-//   warp 8      producer: Q and dO of the query tile, then K/V tiles of the
-//               selected key tiles (found by scanning the mask row) through a
-//               2-stage TMA ring;
+//   warp 8      producer: Q and dO of the query tile, then K and V tiles of
+//               the selected key tiles (found by scanning the mask row)
+//               through TMA rings of 3 (K: read by S and the later dQ) and
+//               2 (V: read by dP only) stages;
 //   warp 9      MMA issuer and TMEM owner. Per key tile m it issues S(m) =
 //               Q K^T into one of two S buffers, dP(m) = dO V^T once the
 //               softmax warps have read dP(m-1), then dQ += dS(m-1) K(m-1)
@@ -40,13 +41,15 @@ constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColP = 256, kColQ = 384;
+constexpr int kKStages = 3, kVStages = 2;
 
 // TMEM column of the packed dS of keys [16 kk, 16 kk + 16) inside an S buffer.
 __host__ __device__ constexpr uint32_t ds_col(int kk) { return (kk >> 2) * 96 + (kk & 3) * 8; }
 
 enum Bar {
   kQFull = 0, kQAux, kQEmpty,
-  kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kKvAux0, kKvAux1,
+  kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kKAux0, kKAux1, kKAux2,
+  kVFull0, kVFull1, kVEmpty0, kVEmpty1, kVAux0, kVAux1,
   kSFull0, kSFull1, kSFree0, kSFree1, kDpFull, kDpFree, kDsReady, kDqFull, kDqEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
   kDrain,
@@ -58,9 +61,9 @@ struct Smem {
   static constexpr int kTileBytes = (D / 64) * kPanel;
   static constexpr int oQ = 0;
   static constexpr int odO = oQ + kTileBytes;
-  static constexpr int oK = odO + kTileBytes;      // [2]
-  static constexpr int oV = oK + 2 * kTileBytes;   // [2]
-  static constexpr int oBar = oV + 2 * kTileBytes;
+  static constexpr int oK = odO + kTileBytes;             // [kKStages]
+  static constexpr int oV = oK + kKStages * kTileBytes;   // [kVStages]
+  static constexpr int oBar = oV + kVStages * kTileBytes;
   static constexpr int oMisc = (oBar + kNumBars * 8 + 63) / 64 * 64;
   static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
   static constexpr int kBytes = oMisc + 128;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = misc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 1);
   int* item_slot = misc + 2;  // [2]
-  int* meta = misc + 4;       // [2] per stage: jt | bits << 24, -1 = end of item
+  int* meta = misc + 4;       // [kKStages] per K stage: jt | bits << 24, -1 = end of item
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -175,10 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kQFull], 1);
     mbar_init(&bars[kQAux], 1);
     mbar_init(&bars[kQEmpty], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bars[kKFull0 + i], 1);
+      mbar_init(&bars[kKEmpty0 + i], 1 + kSoftmaxWarps);  // MMA (commit or arrive) + softmax warps
+      mbar_init(&bars[kKAux0 + i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bars[kVFull0 + i], 1);
+      mbar_init(&bars[kVEmpty0 + i], 1);  // dP MMA commit
+      mbar_init(&bars[kVAux0 + i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kKvFull0 + i], 1);
-      mbar_init(&bars[kKvEmpty0 + i], 1 + kSoftmaxWarps);  // MMA (commit or arrive) + softmax warps
-      mbar_init(&bars[kKvAux0 + i], 1);
       mbar_init(&bars[kItemFull0 + i], 1);
       mbar_init(&bars[kItemEmpty0 + i], 1 + kSoftmaxWarps);
       mbar_init(&bars[kSFull0 + i], 1);   // S MMA commit
@@ -214,10 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
-    uint32_t n = 0, itc = 0, aux[2] = {0u, 0u}, qaux = 0;
+    uint32_t nk = 0, nv = 0, itc = 0, qaux = 0;  // K stages (end markers included), V stages
+    uint32_t kaux[kKStages] = {0u, 0u, 0u}, vaux[kVStages] = {0u, 0u};
     bool ok = true;
-    int pend_q = 0, pend_qaux = 0, pend_kv[2] = {0, 0}, pend_aux[2] = {0, 0};
-    uint32_t par_kv[2] = {0u, 0u};
+    int pend_q = 0, pend_qaux = 0;
+    int pend_k[kKStages] = {0, 0, 0}, pend_kaux[kKStages] = {0, 0, 0};
+    int pend_v[kVStages] = {0, 0}, pend_vaux[kVStages] = {0, 0};
+    uint32_t par_k[kKStages] = {0u, 0u, 0u}, par_v[kVStages] = {0u, 0u};
     while (ok) {
       const int slot = itc & 1;
       if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
@@ -279,73 +292,90 @@ __global__ void __launch_bounds__(kThreads, 1)
           ball &= ball - 1;
           const int jsel = jt0 + src;
           const int bsel = __shfl_sync(0xffffffffu, bits, src);
-          const int st = n & 1;
-          if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+          const int kst = nk % kKStages, vst = nv % kVStages;
+          if (!mbar_wait(&bars[kKEmpty0 + kst], ((nk / kKStages) & 1) ^ 1, abort_flag) ||
+              !mbar_wait(&bars[kVEmpty0 + vst], ((nv / kVStages) & 1) ^ 1, abort_flag)) {
             record_error(p.header, kErrWaitKV);
             ok = false;
             break;
           }
           const bool tail = (Lk - jsel * 128) < 128;
-          uint8_t* sK = sK0 + st * S::kTileBytes;
-          uint8_t* sV = sV0 + st * S::kTileBytes;
+          uint8_t* sK = sK0 + kst * S::kTileBytes;
+          uint8_t* sV = sV0 + vst * S::kTileBytes;
           if (lane == 0) {
-            meta[st] = jsel | (bsel << 24);
-            uint64_t* tb = tail ? &bars[kKvAux0 + st] : &bars[kKvFull0 + st];
-            mbar_arrive_expect_tx(tb, 2 * S::kTileBytes);
+            meta[kst] = jsel | (bsel << 24);
+            uint64_t* tk = tail ? &bars[kKAux0 + kst] : &bars[kKFull0 + kst];
+            uint64_t* tv = tail ? &bars[kVAux0 + vst] : &bars[kVFull0 + vst];
+            mbar_arrive_expect_tx(tk, S::kTileBytes);
+            mbar_arrive_expect_tx(tv, S::kTileBytes);
             const int c1 = p.layout == kLayoutBNSD ? jsel * 128 : g;
             const int c2 = p.layout == kLayoutBNSD ? qi.b * p.N2 + g : p.cu_k[qi.b] + jsel * 128;
             for (int pn = 0; pn < kPanels; ++pn) {
-              tma_load_3d(sK + pn * kPanel, &tm_k, tb, pn * 64, c1, c2);
-              tma_load_3d(sV + pn * kPanel, &tm_v, tb, pn * 64, c1, c2);
+              tma_load_3d(sK + pn * kPanel, &tm_k, tk, pn * 64, c1, c2);
+              tma_load_3d(sV + pn * kPanel, &tm_v, tv, pn * 64, c1, c2);
             }
           }
-          pend_kv[st] = tail ? 0 : 1;
-          par_kv[st] = (n >> 1) & 1;
+          pend_k[kst] = tail ? 0 : 1;
+          par_k[kst] = (nk / kKStages) & 1;
+          pend_v[vst] = tail ? 0 : 1;
+          par_v[vst] = (nv / kVStages) & 1;
           if (tail) {  // K and V rows past the key length must be finite zeros
-            pend_aux[st] = 1;
-            if (!mbar_wait(&bars[kKvAux0 + st], aux[st] & 1, abort_flag)) {
+            pend_kaux[kst] = 1;
+            pend_vaux[vst] = 1;
+            if (!mbar_wait(&bars[kKAux0 + kst], kaux[kst] & 1, abort_flag) ||
+                !mbar_wait(&bars[kVAux0 + vst], vaux[vst] & 1, abort_flag)) {
               record_error(p.header, kErrWaitKV);
               ok = false;
               break;
             }
-            aux[st]++;
-            pend_aux[st] = 0;
+            kaux[kst]++;
+            vaux[vst]++;
+            pend_kaux[kst] = 0;
+            pend_vaux[vst] = 0;
             zero_rows(sK, kPanels, Lk - jsel * 128, lane);
             zero_rows(sV, kPanels, Lk - jsel * 128, lane);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kKvFull0 + st]);
+            if (lane == 0) {
+              mbar_arrive(&bars[kKFull0 + kst]);
+              mbar_arrive(&bars[kVFull0 + vst]);
+            }
           }
-          ++n;
+          ++nk;
+          ++nv;
         }
       }
       if (!ok) break;
-      // end-of-item marker
-      const int st = n & 1;
-      if (!mbar_wait(&bars[kKvEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+      // end-of-item marker (a K stage without a copy)
+      const int kst = nk % kKStages;
+      if (!mbar_wait(&bars[kKEmpty0 + kst], ((nk / kKStages) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitKV);
         break;
       }
       if (lane == 0) {
-        meta[st] = -1;
-        mbar_arrive(&bars[kKvFull0 + st]);
+        meta[kst] = -1;
+        mbar_arrive(&bars[kKFull0 + kst]);
       }
       __syncwarp();
-      ++n;
+      ++nk;
       ++itc;
     }
     if (*abort_flag) {  // let copies still in flight land before the CTA exits
       if (pend_q) mbar_wait_drain(&bars[kQFull], itc & 1);
       if (pend_qaux) mbar_wait_drain(&bars[kQAux], qaux & 1);
-      for (int st = 0; st < 2; ++st) {
-        if (pend_kv[st]) mbar_wait_drain(&bars[kKvFull0 + st], par_kv[st]);
-        if (pend_aux[st]) mbar_wait_drain(&bars[kKvAux0 + st], aux[st] & 1);
+      for (int st = 0; st < kKStages; ++st) {
+        if (pend_k[st]) mbar_wait_drain(&bars[kKFull0 + st], par_k[st]);
+        if (pend_kaux[st]) mbar_wait_drain(&bars[kKAux0 + st], kaux[st] & 1);
+      }
+      for (int st = 0; st < kVStages; ++st) {
+        if (pend_v[st]) mbar_wait_drain(&bars[kVFull0 + st], par_v[st]);
+        if (pend_vaux[st]) mbar_wait_drain(&bars[kVAux0 + st], vaux[st] & 1);
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    uint32_t n = 0, itc = 0;  // n: K/V stages (end markers included)
-    uint32_t m = 0;           // m: computed key tiles (S buffer m & 1)
+    uint32_t nk = 0, nv = 0, itc = 0;  // K stages (end markers included), V stages
+    uint32_t m = 0;                    // m: computed key tiles (S buffer m & 1)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO);
     // dQ += dS(mm) K: A = dS in S buffer mm & 1 (TMEM), B = K of stage kst
@@ -360,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + kColQ, tmem + sb + ds_col(k), dKmn + (uint64_t)((k * 2048) >> 4), kIdQ,
                  (first && k == 0) ? 0u : 1u);
         tc_commit(&bars[kSFree0 + (mm & 1)]);
-        tc_commit(&bars[kKvEmpty0 + kst]);
+        tc_commit(&bars[kKEmpty0 + kst]);  // K read for the last time
       }
       __syncwarp();
     };
@@ -374,17 +404,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
       int j = 0, st_prev = 0;
       while (true) {
-        const int st = n & 1;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int st = nk % kKStages;
+        if (!mbar_wait(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         if (mt < 0) {
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&bars[kKvEmpty0 + st]);
+            mbar_arrive(&bars[kKEmpty0 + st]);
             tc_commit(&bars[kQEmpty]);  // Q and dO: their last readers are issued
           }
           __syncwarp();
-          ++n;
+          ++nk;
           break;
         }
         const uint32_t sb = kColS0 + 128 * (m & 1);
@@ -392,7 +422,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars[kSFree0 + (m & 1)], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
-        const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
         if (lane == 0) {
           const uint64_t dQk = sdesc_sw128(aQ, 16, 1024), dKk = sdesc_sw128(aK, 16, 1024);
 #pragma unroll
@@ -404,18 +433,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // dP has one buffer: the softmax warps must have read dP(m-1)
+        const int vst = nv % kVStages;
         if (!mbar_wait(&bars[kDpFree], (m & 1) ^ 1, abort_flag)) { where = kErrWaitDP; break; }
+        if (!mbar_wait(&bars[kVFull0 + vst], (nv / kVStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         tc_fence_after();
         if (lane == 0) {
-          const uint64_t dOk = sdesc_sw128(adO, 16, 1024), dVk = sdesc_sw128(aV, 16, 1024);
+          const uint64_t dOk = sdesc_sw128(adO, 16, 1024);
+          const uint64_t dVk = sdesc_sw128(smem_u32(sV0 + vst * S::kTileBytes), 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint64_t off = (uint64_t)(((k >> 2) * kPanel + (k & 3) * 32) >> 4);
             mma_ss(tmem + kColP, dOk + off, dVk + off, kIdS, k > 0);
           }
           tc_commit(&bars[kDpFull]);
+          tc_commit(&bars[kVEmpty0 + vst]);  // V is read by dP only
         }
         __syncwarp();
+        ++nv;
         if (j > 0) {  // dQ of the previous key tile, while the softmax works on this one
           if (!mbar_wait(&bars[kDsReady], (m - 1) & 1, abort_flag)) { where = kErrWaitDS; break; }
           // the first dQ MMA of an item overwrites the accumulator: the
@@ -425,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         st_prev = st;
         ++j;
-        ++n;
+        ++nk;
         ++m;
       }
       if (where) break;
@@ -473,11 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t_sub = p.cb == 2 ? wg : 0;  // this warpgroup's keys lie in one key block
       int j = 0;
       while (true) {
-        const int st = n & 1;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int st = n % kKStages;
+        if (!mbar_wait(&bars[kKFull0 + st], (n / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+        if (lane == 0) mbar_arrive(&bars[kKEmpty0 + st]);
         if (mt < 0) {
           ++n;
           break;
