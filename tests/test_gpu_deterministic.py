@@ -132,3 +132,45 @@ def test_autograd_function(deterministic):
     for name, g, r in zip(("dq", "dk", "dv"), (qd.grad, kd.grad, vd.grad), ref):
         assert g.dtype == TORCH_DT[w.dtype]
         check(f"autograd:{name}", f64(g), r)
+
+
+def test_deterministic_large_token_masked():
+    """w1doc (dense B2 N16 S4096 with causal documents as attenMask) in the
+    deterministic mode: two runs give identical bytes, and sampled rows match
+    the oracle."""
+    w = make_workload("w1doc")
+    dout, q, k, v = host_inputs(w)
+    win = dict(atten_mask=w.atten_mask)
+    out, lse = oracle_forward(w, q, k, v, blockrows=True, **win)
+    tout, tlse = rounded_out_lse(w, out, lse)
+    del out, lse
+    am = torch.from_numpy(w.atten_mask).to(DEV)
+
+    def grad():
+        res = bsa.block_sparse_attention_grad(
+            dout.to(DEV), q.to(DEV), k.to(DEV), v.to(DEV), tout.to(DEV), tlse.to(DEV),
+            block_shape=[w.bx, w.by], num_key_value_heads=w.N2, scale_value=w.scale,
+            deterministic=True, atten_mask=am)
+        bsa.bsa_check_status(res[3])
+        return res[:3]
+    first, second = grad(), grad()
+    for a, b in zip(first, second):
+        assert torch.equal(a, b)
+    dq, dk, dv = (f64(t) for t in first)
+    args = (f64(dout), f64(q), f64(k), f64(v), f64(tout), f64(tlse))
+    kw = dict(mask=None, block_shape=(w.bx, w.by), seq_q=w.seq_q, seq_kv=w.seq_kv,
+              layout=w.layout, num_kv_heads=w.N2, scale=w.scale, **win)
+    got_q, ref_q = [], []
+    for (b, h, s) in sampled_rows(w):
+        ref_q.append(O.backward_dq_rows(*args, b, h, np.array([s]), **kw)[0])
+        got_q.append(dq[b, h, s])
+    check("w1doc:det:dq", np.array(got_q), np.array(ref_q))
+    got_k, ref_k, got_v, ref_v = [], [], [], []
+    for (b, g, t) in sampled_cols(w):
+        rk, rv = O.backward_dkdv_rows(*args, b, g, np.array([t]), **kw)
+        ref_k.append(rk[0])
+        ref_v.append(rv[0])
+        got_k.append(dk[b, g, t])
+        got_v.append(dv[b, g, t])
+    check("w1doc:det:dk", np.array(got_k), np.array(ref_k))
+    check("w1doc:det:dv", np.array(got_v), np.array(ref_v))
