@@ -20,7 +20,8 @@ The sources it follows (all from the ``aclnnBlockSparseAttentionGrad`` page,
   default [128, 128] (same table);
 * numKeyValueHeads: N1 % N2 == 0 (section 约束说明, constraints).
 
-Readings of points the page leaves open (each also listed in the design doc):
+Readings of points the pages leave open (numbered; the same numbers are used
+wherever the project refers to them):
 
 R1  softmaxGrad(dOut, attentionOut) is the row vector D_s = sum_d dOut_sd*Out_sd
     (the softmax Jacobian-vector product that makes dS = P*(dP - D) exact).
