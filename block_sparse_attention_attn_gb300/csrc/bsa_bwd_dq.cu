@@ -30,6 +30,7 @@
 
 #include "bsa_common.h"
 #include "bsa_launch.h"
+#include "bsa_device.cuh"
 #include "sm103_ptx.cuh"
 
 namespace bsa {
@@ -68,39 +69,6 @@ struct Smem {
   static_assert(oMisc % 16 == 0, "misc area must be 16-byte aligned");
   static constexpr int kBytes = oMisc + 128;
 };
-
-template <int DT>
-struct Elem;
-template <>
-struct Elem<kDtBF16> {
-  using T = __nv_bfloat16;
-  static constexpr int kAB = 1;
-  __device__ static uint32_t pack(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __device__ static float2 unpack(uint32_t u) {
-    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
-  }
-};
-template <>
-struct Elem<kDtF16> {
-  using T = __half;
-  static constexpr int kAB = 0;
-  __device__ static uint32_t pack(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
-  __device__ static float2 unpack(uint32_t u) {
-    return __half22float2(*reinterpret_cast<__half2*>(&u));
-  }
-};
-
-__device__ __forceinline__ void record_error(int* header, int where) {
-  atomicCAS(&header[kHdrErrorWhere], 0, where);
-  atomicExch(&header[kHdrError], 1);
-  atomicAdd(&header[kHdrErrorCounts + (where & 15)], 1);
-}
 
 __device__ __noinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
   const int n16 = (128 - r0) * 8;
