@@ -677,3 +677,30 @@ def test_planted_atten_mask_mistakes_are_caught(kind, monkeypatch):
     monkeypatch.setattr(O, "token_mask_at", wrong)
     with pytest.raises(AssertionError):
         test_atten_mask_with_blocks_matches_sdpa(O.NO_WINDOW, O.NO_WINDOW)
+
+
+@pytest.mark.parametrize("how", ["blocks", "window", "atten_mask"])
+def test_single_key_per_row_closed_form(how):
+    """Each query sees only the key at its own position (an identity mask of
+    1x1 blocks, the window pre = next = 0, or an attenMask that masks all but
+    the diagonal): P = 1, so Out_s = V_s and lse_s = scale q_s.k_s, and
+    dS = P (dP - D) = 0 since D_s = dOut_s.Out_s = dOut_s.V_s = dP_ss: dQ = dK = 0
+    and dV_t = dOut_t."""
+    S, D = 12, 8
+    q, k, v, do, _ = _case(N1=1, N2=1, S=S, D=D, seed=191)
+    kw = dict(num_kv_heads=1, scale=0.3)
+    if how == "blocks":
+        mask, bs = np.eye(S, dtype=np.uint8)[None, None], (1, 1)
+    elif how == "window":
+        mask, bs = None, (4, 4)
+        kw.update(pre_tokens=0, next_tokens=0)
+    else:
+        mask, bs = None, (4, 4)
+        kw.update(atten_mask=(1 - np.eye(S, dtype=np.uint8)))
+    out, lse = O.forward(q, k, v, mask, bs, **kw)
+    np.testing.assert_allclose(out, v, rtol=1e-14, atol=1e-14)
+    expect_lse = 0.3 * np.einsum("bhsd,bhsd->bhs", q, k)[..., None]
+    np.testing.assert_allclose(lse, expect_lse, rtol=1e-13, atol=1e-13)
+    dq, dk, dv = O.backward(do, q, k, v, out, lse, mask, bs, **kw)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+    np.testing.assert_allclose(dv, do, rtol=1e-13, atol=1e-14)
