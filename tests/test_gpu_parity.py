@@ -295,3 +295,23 @@ def test_bounded_wait_reports_error_and_context_survives():
     hdr = ws[:128].view(torch.int32).cpu().tolist()
     assert hdr[6] == 12 or hdr[16 + 12] > 0       # the test wait is among the recorded codes
     full_case(w)                                   # the context still computes correctly
+
+
+def test_zero_length_sequences():
+    """TND batches with no queries, no keys or neither, between non-empty ones:
+    nothing is read or written for them, rows without keys get dQ = 0, and the
+    forward gives Out = 0 and lse = -inf there."""
+    w = small_workload(layout="TND", dtype="bf16", B=5, N1=4, N2=2, D=128, bx=128, by=64,
+                       seq_q=(0, 150, 70, 0, 200), seq_kv=(90, 0, 130, 0, 260), p=0.8, seed=29)
+    full_case(w)
+    dout, q, k, v = host_inputs(w)
+    ref_out, ref_lse = oracle_forward(w, q, k, v)
+    mask = torch.from_numpy(w.mask).to(DEV)
+    out, lse, ws = bsa.block_sparse_attention_fwd(
+        q.to(DEV), k.to(DEV), v.to(DEV), block_sparse_mask=mask, block_shape=[w.bx, w.by],
+        actual_seq_lengths=w.seq_q, actual_seq_lengths_kv=w.seq_kv, layout="TND",
+        num_key_value_heads=w.N2, scale_value=w.scale)
+    bsa.bsa_check_status(ws)
+    check("zero-len:fwd_out", f64(out), ref_out)
+    np.testing.assert_array_equal(np.isneginf(f64(lse)), np.isneginf(ref_lse))
+    assert np.all(np.isneginf(f64(lse)[0:150]))        # batch 1: 150 queries, no keys
