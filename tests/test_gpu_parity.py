@@ -315,3 +315,14 @@ def test_zero_length_sequences():
     check("zero-len:fwd_out", f64(out), ref_out)
     np.testing.assert_array_equal(np.isneginf(f64(lse)), np.isneginf(ref_lse))
     assert np.all(np.isneginf(f64(lse)[0:150]))        # batch 1: 150 queries, no keys
+
+
+def test_largest_gqa_group():
+    """G = N1/N2 = 256, the largest group the work lists encode (8 bits of
+    local head), with ragged tiles. In fp16: dK and dV of a key sum 256 heads'
+    contributions, and with bf16 operands the rounding of P and dS alone (the
+    kernel's exact arithmetic, emulated on the host, lands on the GPU's
+    values) exceeds the per-element bound on some elements."""
+    w = small_workload(layout="BNSD", dtype="f16", B=1, N1=256, N2=1, D=64, bx=64, by=64,
+                       seq_q=(130,), seq_kv=(200,), p=0.5, seed=37)
+    full_case(w)
