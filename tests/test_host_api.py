@@ -148,3 +148,38 @@ def test_wait_test_switch_needs_an_executor(lib):
 
 def test_deterministic_switch_needs_a_backward_executor(lib):
     assert lib.bsa_executor_set_deterministic(None, 1) == B.BSA_ERR_PARAM_NULLPTR
+
+
+def _fwd_status(**kw):
+    try:
+        bsa.bsa_fwd_workspace_size(**kw)
+    except B.BsaError as e:
+        return e.status
+    return 0
+
+
+def _fwd_args():
+    g = _grad_args()
+    return dict(query=g["query"], key=g["key"], value=g["value"],
+                block_sparse_mask=g["block_sparse_mask"], block_shape=[128, 128],
+                num_key_value_heads=1, scale_value=g["scale_value"],
+                attention_out=g["attention_out"], softmax_lse=g["softmax_lse"])
+
+
+def test_forward_first_stage_validation(lib):
+    ok = 0 if torch.cuda.is_available() else B.BSA_ERR_RUNTIME
+    assert _fwd_status(**_fwd_args()) == ok
+    assert _fwd_status(**_fwd_args(), pre_tokens=100, next_tokens=0) == ok
+    assert _fwd_status(**_fwd_args(), atten_mask=torch.zeros(256, 256, dtype=torch.bool)) == ok
+    bad = [dict(pre_tokens=-3, next_tokens=2),
+           dict(atten_mask=torch.zeros(256, 256, dtype=torch.uint8), mask_type=0),
+           dict(mask_type=1),
+           dict(atten_mask=torch.zeros(200, 256, dtype=torch.uint8)),
+           dict(block_shape=[32, 128])]
+    for extra in bad:
+        kw = _fwd_args()
+        kw.update(extra)
+        assert _fwd_status(**kw) == B.BSA_ERR_PARAM_INVALID, extra
+    kw = _fwd_args()
+    kw["softmax_lse"] = None
+    assert _fwd_status(**kw) == B.BSA_ERR_PARAM_NULLPTR
