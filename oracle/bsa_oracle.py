@@ -64,8 +64,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = ["token_mask", "token_mask_at", "window_mask", "head_rows", "forward",
-           "forward_blockrows", "backward", "backward_dq_rows", "backward_dkdv_rows",
-           "compact_mask", "seq_offsets", "NO_WINDOW"]
+           "forward_blockrows", "backward", "backward_blockrows", "backward_dq_rows",
+           "backward_dkdv_rows", "compact_mask", "seq_offsets", "NO_WINDOW"]
 
 NO_WINDOW = 2147483647   # preTokens / nextTokens value for "no sliding window" (R18)
 
@@ -307,6 +307,69 @@ def backward(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=N
                 dq[oq[b]:oq[b] + lq[b], h] = dQ
                 dk[okv[b]:okv[b] + lk[b], g] += dK
                 dv[okv[b]:okv[b] + lk[b], g] += dV
+    return dq, dk, dv
+
+
+def backward_blockrows(dout, q, k, v, out, lse, mask=None, block_shape=(128, 128), seq_q=None,
+                       seq_kv=None, layout="BNSD", num_kv_heads=None, scale=1.0,
+                       pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
+    """The same full dQ, dK, dV as :func:`backward`, evaluated per query block
+    row over that row's selected key set only (every query row of a block row
+    has the same K(s)): the row's dQ comes out whole, and its contributions to
+    dK / dV of the selected keys are added to those keys' rows (the sums over s
+    of the formulas, taken block row by block row). Used where the dense
+    [Lq, Lk] matrices would not fit in host memory; pinned to
+    :func:`backward` by the tests."""
+    bx, by = int(block_shape[0]), int(block_shape[1])
+    B, lq, lk = _lengths(q, k, layout, seq_q, seq_kv)
+    _, N1, N2, D = _dims(q, k, layout)
+    G = N1 // N2
+    oq, okv = seq_offsets(lq), seq_offsets(lk)
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    for b in range(B):
+        mq = -(-lq[b] // bx)
+        mk = -(-lk[b] // by)
+        for g in range(N2):
+            Kh = head_rows(k, layout, b, g, lk[b], okv)
+            Vh = head_rows(v, layout, b, g, lk[b], okv)
+            dKh = np.zeros((lk[b], D))
+            dVh = np.zeros((lk[b], D))
+            for h in range(g * G, (g + 1) * G):                          # R3
+                Qh = head_rows(q, layout, b, h, lq[b], oq)
+                dOh = head_rows(dout, layout, b, h, lq[b], oq)
+                Oh = head_rows(out, layout, b, h, lq[b], oq)
+                Lh = _lse_rows(lse, layout, b, h, lq[b], oq)
+                dQh = np.zeros((lq[b], D))
+                for i in range(mq):
+                    s0, s1 = i * bx, min(lq[b], (i + 1) * bx)
+                    if mask is None:
+                        sel = np.arange(mk)
+                    else:
+                        sel = np.nonzero(np.asarray(mask[b, h, i, :mk]) != 0)[0]
+                    if len(sel) == 0:
+                        continue                                          # R6
+                    keys = np.concatenate([np.arange(j * by, min(lk[b], (j + 1) * by))
+                                           for j in sel])
+                    M = window_mask(np.arange(s0, s1), keys, pre_tokens, next_tokens)
+                    if atten_mask is not None:
+                        M = M & (np.asarray(atten_mask)[s0:s1][:, keys] == 0)
+                    a, c, e = _head_backward(Qh[s0:s1], Kh[keys], Vh[keys], dOh[s0:s1],
+                                             Oh[s0:s1], Lh[s0:s1], M, scale)
+                    dQh[s0:s1] = a
+                    dKh[keys] += c          # keys are distinct within one block row
+                    dVh[keys] += e
+                if layout == "BNSD":
+                    dq[b, h, :lq[b]] = dQh
+                else:
+                    dq[oq[b]:oq[b] + lq[b], h] = dQh
+            if layout == "BNSD":
+                dk[b, g, :lk[b]] = dKh
+                dv[b, g, :lk[b]] = dVh
+            else:
+                dk[okv[b]:okv[b] + lk[b], g] = dKh
+                dv[okv[b]:okv[b] + lk[b], g] = dVh
     return dq, dk, dv
 
 

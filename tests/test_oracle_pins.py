@@ -704,3 +704,89 @@ def test_single_key_per_row_closed_form(how):
     dq, dk, dv = O.backward(do, q, k, v, out, lse, mask, bs, **kw)
     assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
     np.testing.assert_allclose(dv, do, rtol=1e-13, atol=1e-14)
+
+
+# -------------------------------------------- block-row backward (whole tensors)
+def _blockrows_cases():
+    """(args, kwargs) cases: BNSD GQA with non-square blocks, an empty block
+    row and ragged tails; TND with a zero-length sequence; a window; a token
+    mask; no block mask; garbage bits past the lengths."""
+    cases = []
+    q, k, v, do, m = _case(N1=4, N2=2, S=70, Skv=90, D=8, bx=16, by=32, seed=201, diag=False)
+    m[0, 1, 2, :] = 0
+    out, lse = O.forward(q, k, v, m, (16, 32), num_kv_heads=2, scale=0.5)
+    cases.append(((do, q, k, v, out, lse, m, (16, 32)), dict(num_kv_heads=2, scale=0.5)))
+    lens_q, lens_k = [13, 0, 30, 7], [21, 9, 30, 0]
+    rng = np.random.Generator(np.random.PCG64(202))
+    mt = (rng.random((4, 4, 4, 4)) < 0.6).astype(np.uint8)
+    qt, kt, vt, dot = (_rand((sum(lens_q), 4, 8), 203), _rand((sum(lens_k), 2, 8), 204),
+                       _rand((sum(lens_k), 2, 8), 205), _rand((sum(lens_q), 4, 8), 206))
+    kwt = dict(seq_q=lens_q, seq_kv=lens_k, layout="TND", num_kv_heads=2, scale=0.3)
+    ot, lt = O.forward(qt, kt, vt, mt, (8, 8), **kwt)
+    cases.append(((dot, qt, kt, vt, ot, lt, mt, (8, 8)), kwt))
+    q, k, v, do, m = _case(N1=2, N2=1, S=40, Skv=45, D=8, bx=8, by=16, seed=207, p=0.6)
+    for extra in (dict(pre_tokens=9, next_tokens=-3), dict(atten_mask=_am(40, 45, 0.3, 208))):
+        kw = dict(num_kv_heads=1, scale=0.5, **extra)
+        o, l = O.forward(q, k, v, m, (8, 16), **kw)
+        cases.append(((do, q, k, v, o, l, m, (8, 16)), kw))
+    o, l = O.forward(q, k, v, None, (8, 16), num_kv_heads=1, scale=0.5)
+    cases.append(((do, q, k, v, o, l, None, (8, 16)), dict(num_kv_heads=1, scale=0.5)))
+    g = (rng.random(m.shape) < 0.5).astype(np.uint8)
+    g[:, :, :2, :2] = m[:, :, :2, :2]
+    kwl = dict(seq_q=[23], seq_kv=[30], num_kv_heads=1, scale=0.5)   # blocks past 23 / 30 are garbage
+    o, l = O.forward(q, k, v, g, (8, 16), **kwl)
+    cases.append(((do, q, k, v, o, l, g, (8, 16)), kwl))
+    return cases
+
+
+def test_backward_blockrows_matches_backward():
+    for args, kw in _blockrows_cases():
+        ref = O.backward(*args, **kw)
+        got = O.backward_blockrows(*args, **kw)
+        for a, b in zip(got, ref):
+            np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+def test_backward_blockrows_matches_sdpa_autograd():
+    """Independently of the dense oracle: autograd of the fp64 SDPA with the
+    block mask expanded by np.repeat (GQA, non-square blocks, tails)."""
+    q, k, v, do, m = _case(N1=4, N2=2, S=37, Skv=52, D=16, bx=8, by=16, seed=211)
+    out, lse = O.forward(q, k, v, m, (8, 16), num_kv_heads=2, scale=0.25)
+    got = O.backward_blockrows(do, q, k, v, out, lse, m, (8, 16), num_kv_heads=2, scale=0.25)
+    _, gq, gk, gv = _sdpa_fwd_bwd(q, k, v, do, m, 8, 16, 0.25, 2)
+    for a, b in zip(got, (gq, gk, gv)):
+        np.testing.assert_allclose(a, b, rtol=1e-10, atol=1e-11)
+
+
+_BLOCKROWS_MUTATIONS = {
+    "dk_assigned": ("dKh[keys] += c", "dKh[keys] = c"),          # later block rows overwrite
+    "dv_assigned": ("dVh[keys] += e", "dVh[keys] = e"),
+    "no_group_sum": ("for h in range(g * G, (g + 1) * G):", "for h in range(g * G, g * G + 1):"),
+    "mask_of_kv_head": ("mask[b, h, i, :mk]", "mask[b, g, i, :mk]"),
+    "window_rows_shifted": ("window_mask(np.arange(s0, s1), keys,",
+                            "window_mask(np.arange(s0, s1) + 1, keys,"),
+    "key_block_by_bx": ("np.arange(j * by, min(lk[b], (j + 1) * by))",
+                        "np.arange(j * bx, min(lk[b], j * bx + by))"),
+}
+
+
+@pytest.mark.parametrize("kind", sorted(_BLOCKROWS_MUTATIONS))
+def test_planted_blockrows_mistakes_are_caught(kind, monkeypatch):
+    """Each mutation of the block-row backward's source (a plausible slip)
+    fails one of its pins."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(O.backward_blockrows))
+    old, new = _BLOCKROWS_MUTATIONS[kind]
+    assert src.count(old) == 1, kind
+    ns = dict(vars(O))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(O, "backward_blockrows", ns["backward_blockrows"])
+    caught = 0
+    for pin in (test_backward_blockrows_matches_backward,
+                test_backward_blockrows_matches_sdpa_autograd):
+        try:
+            pin()
+        except (AssertionError, IndexError, ValueError):
+            caught += 1
+    assert caught >= 1, kind
