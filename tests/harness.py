@@ -64,3 +64,18 @@ def check(name, got, ref):
     fro = np.linalg.norm(got - ref) / nr if nr > 0 else np.linalg.norm(got)
     assert fro <= FRO, f"{name}: relative Frobenius error {fro:.3e}"
     return float(err.max()), float(fro)
+
+
+def oracle_backward_whole(w, dout, q, k, v, tout, tlse, mask="workload", **window):
+    """The oracle's whole dQ, dK, dV (block-row evaluation over the selected
+    keys), fed the same Out / lse bytes the GPU backward consumes."""
+    m = w.mask if isinstance(mask, str) else mask
+    return O.backward_blockrows(f64(dout), f64(q), f64(k), f64(v), f64(tout), f64(tlse), m,
+                                (w.bx, w.by), w.seq_q, w.seq_kv, w.layout, w.N2, w.scale,
+                                **window)
+
+
+def check_whole(name, got, ref):
+    """Element-wise and relative-Frobenius check of whole output tensors."""
+    for part, g, r in zip(("dq", "dk", "dv"), got, ref):
+        check(f"{name}:{part}", f64(g) if isinstance(g, torch.Tensor) else g, r)

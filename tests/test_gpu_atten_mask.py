@@ -1,6 +1,6 @@
 """Token mask attenMaskOptional (maskType 1; 1 = the pair is masked out) on the
 GPU against the fp64 oracle: backward in both dQ modes, the forward, the
-autograd pairing and sampled rows of a full-size workload, alone and together
+autograd pairing and the whole outputs of a full-size workload, alone and together
 with the block mask and the sliding window."""
 import numpy as np
 import pytest
@@ -9,8 +9,8 @@ import torch
 import block_sparse_attention_attn_gb300 as bsa
 from block_sparse_attention_attn_gb300.workloads import make_workload, small_workload
 from oracle import bsa_oracle as O
-from tests.harness import check, f64, host_inputs, oracle_forward, rounded_out_lse
-from tests.test_gpu_parity import sampled_cols, sampled_rows
+from tests.harness import (check, check_whole, f64, host_inputs, oracle_backward_whole,
+                           oracle_forward, rounded_out_lse)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -181,10 +181,10 @@ def test_atten_mask_autograd():
         check(f"am-autograd:{name}", f64(g), r)
 
 
-def test_atten_mask_large_sampled():
+def test_atten_mask_large_whole():
     """w1 (BNSD B2 N16 S4096, Bernoulli(0.25) blocks) with causal documents of
-    200-1500 tokens as attenMask, on sampled rows and columns, plus the
-    forward on the full tensors."""
+    200-1500 tokens as attenMask: whole dQ, dK, dV against the oracle, plus
+    the forward on the full tensors."""
     w = make_workload("w1")
     am = document_am(w.Sq, w.Skv, 1601, lo=200, hi=1500).astype(np.uint8)
     win = dict(atten_mask=am)
@@ -192,25 +192,8 @@ def test_atten_mask_large_sampled():
     out, lse = oracle_forward(w, q, k, v, blockrows=True, **win)
     tout, tlse = rounded_out_lse(w, out, lse)
     del out, lse
-    dq, dk, dv = (f64(t) for t in run_grad(w, dout, q, k, v, tout, tlse, am))
-    args = (f64(dout), f64(q), f64(k), f64(v), f64(tout), f64(tlse))
-    kw = dict(mask=w.mask, block_shape=(w.bx, w.by), seq_q=w.seq_q, seq_kv=w.seq_kv,
-              layout=w.layout, num_kv_heads=w.N2, scale=w.scale, **win)
-    got_q, ref_q = [], []
-    for (b, h, s) in sampled_rows(w):
-        ref_q.append(O.backward_dq_rows(*args, b, h, np.array([s]), **kw)[0])
-        got_q.append(dq[b, h, s])
-    check("w1:am:dq", np.array(got_q), np.array(ref_q))
-    got_k, got_v, ref_k, ref_v = [], [], [], []
-    for (b, g, t) in sampled_cols(w):
-        rk, rv = O.backward_dkdv_rows(*args, b, g, np.array([t]), **kw)
-        ref_k.append(rk[0])
-        ref_v.append(rv[0])
-        got_k.append(dk[b, g, t])
-        got_v.append(dv[b, g, t])
-    check("w1:am:dk", np.array(got_k), np.array(ref_k))
-    check("w1:am:dv", np.array(got_v), np.array(ref_v))
-    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    got = run_grad(w, dout, q, k, v, tout, tlse, am)
+    check_whole("w1:am", got, oracle_backward_whole(w, dout, q, k, v, tout, tlse, **win))
     fo, fl = run_fwd(w, q, k, v, am)
     check("w1:am:fwd_out", f64(fo), f64(tout))
     fin = np.isfinite(f64(tlse))

@@ -8,8 +8,8 @@ import torch
 import block_sparse_attention_attn_gb300 as bsa
 from block_sparse_attention_attn_gb300.workloads import make_workload, small_workload
 from oracle import bsa_oracle as O
-from tests.harness import TORCH_DT, check, f64, host_inputs, oracle_forward, rounded_out_lse
-from tests.test_gpu_parity import sampled_cols, sampled_rows
+from tests.harness import (TORCH_DT, check, check_whole, f64, host_inputs,
+                           oracle_backward_whole, oracle_forward, rounded_out_lse)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -74,32 +74,16 @@ def test_deterministic_is_bitwise_repeatable_and_matches_default():
         check(f"det-vs-default:{name}", f64(a), f64(b))
 
 
-def test_deterministic_large_sampled():
-    """w2 (GQA 4, S 8192) in the deterministic mode, on sampled rows."""
+def test_deterministic_large_whole():
+    """w2 (GQA 4, S 8192) in the deterministic mode: whole dQ, dK, dV against
+    the oracle."""
     w = make_workload("w2")
     dout, q, k, v = host_inputs(w)
     out, lse = oracle_forward(w, q, k, v, blockrows=True)
     tout, tlse = rounded_out_lse(w, out, lse)
     del out, lse
-    dq, dk, dv = (f64(t) for t in run_grad(w, dout, q, k, v, tout, tlse, deterministic=True))
-    args = (f64(dout), f64(q), f64(k), f64(v), f64(tout), f64(tlse))
-    kw = dict(mask=w.mask, block_shape=(w.bx, w.by), seq_q=w.seq_q, seq_kv=w.seq_kv,
-              layout=w.layout, num_kv_heads=w.N2, scale=w.scale)
-    got_q, ref_q = [], []
-    for (b, h, s) in sampled_rows(w):
-        ref_q.append(O.backward_dq_rows(*args, b, h, np.array([s]), **kw)[0])
-        got_q.append(dq[b, h, s])
-    check("w2:det:dq", np.array(got_q), np.array(ref_q))
-    got_k, ref_k, got_v, ref_v = [], [], [], []
-    for (b, g, t) in sampled_cols(w):
-        rk, rv = O.backward_dkdv_rows(*args, b, g, np.array([t]), **kw)
-        ref_k.append(rk[0])
-        ref_v.append(rv[0])
-        got_k.append(dk[b, g, t])
-        got_v.append(dv[b, g, t])
-    check("w2:det:dk", np.array(got_k), np.array(ref_k))
-    check("w2:det:dv", np.array(got_v), np.array(ref_v))
-    assert np.all(np.isfinite(dq))
+    got = run_grad(w, dout, q, k, v, tout, tlse, deterministic=True)
+    check_whole("w2:det", got, oracle_backward_whole(w, dout, q, k, v, tout, tlse))
 
 
 @pytest.mark.parametrize("deterministic", [False, True])
@@ -136,8 +120,8 @@ def test_autograd_function(deterministic):
 
 def test_deterministic_large_token_masked():
     """w1doc (dense B2 N16 S4096 with causal documents as attenMask) in the
-    deterministic mode: two runs give identical bytes, and sampled rows match
-    the oracle."""
+    deterministic mode: two runs give identical bytes, and the whole outputs
+    match the oracle."""
     w = make_workload("w1doc")
     dout, q, k, v = host_inputs(w)
     win = dict(atten_mask=w.atten_mask)
@@ -156,21 +140,5 @@ def test_deterministic_large_token_masked():
     first, second = grad(), grad()
     for a, b in zip(first, second):
         assert torch.equal(a, b)
-    dq, dk, dv = (f64(t) for t in first)
-    args = (f64(dout), f64(q), f64(k), f64(v), f64(tout), f64(tlse))
-    kw = dict(mask=None, block_shape=(w.bx, w.by), seq_q=w.seq_q, seq_kv=w.seq_kv,
-              layout=w.layout, num_kv_heads=w.N2, scale=w.scale, **win)
-    got_q, ref_q = [], []
-    for (b, h, s) in sampled_rows(w):
-        ref_q.append(O.backward_dq_rows(*args, b, h, np.array([s]), **kw)[0])
-        got_q.append(dq[b, h, s])
-    check("w1doc:det:dq", np.array(got_q), np.array(ref_q))
-    got_k, ref_k, got_v, ref_v = [], [], [], []
-    for (b, g, t) in sampled_cols(w):
-        rk, rv = O.backward_dkdv_rows(*args, b, g, np.array([t]), **kw)
-        ref_k.append(rk[0])
-        ref_v.append(rv[0])
-        got_k.append(dk[b, g, t])
-        got_v.append(dv[b, g, t])
-    check("w1doc:det:dk", np.array(got_k), np.array(ref_k))
-    check("w1doc:det:dv", np.array(got_v), np.array(ref_v))
+    check_whole("w1doc:det", first,
+                oracle_backward_whole(w, dout, q, k, v, tout, tlse, mask=None, **win))

@@ -1,6 +1,6 @@
 """Sliding window (preTokens / nextTokens; nextTokens = 0 is the causal mask)
 on the GPU against the fp64 oracle: backward (default and deterministic dQ),
-the companion forward, the autograd pairing, and sampled rows of a full-size
+the companion forward, the autograd pairing, and the whole outputs of a full-size
 workload. attentionOut / softmaxLse come from the oracle's forward with the
 same window."""
 import numpy as np
@@ -10,8 +10,8 @@ import torch
 import block_sparse_attention_attn_gb300 as bsa
 from block_sparse_attention_attn_gb300.workloads import make_workload, small_workload
 from oracle import bsa_oracle as O
-from tests.harness import check, f64, host_inputs, oracle_forward, rounded_out_lse
-from tests.test_gpu_parity import sampled_cols, sampled_rows
+from tests.harness import (check, check_whole, f64, host_inputs, oracle_backward_whole,
+                           oracle_forward, rounded_out_lse)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -148,40 +148,18 @@ def test_causal_autograd():
 
 
 @pytest.mark.parametrize("name,pre,nxt", [("w1", NOW, 0), ("w3", 1000, 0)])
-def test_window_large_sampled(name, pre, nxt):
+def test_window_large_whole(name, pre, nxt):
     """Full-size workloads (w1: BNSD B2 N16 S4096, causal; w3: TND 8 sequences,
-    sliding window of 1000 earlier tokens) on sampled rows and columns, plus
-    the forward on the full tensors."""
+    sliding window of 1000 earlier tokens): whole dQ, dK, dV against the
+    oracle, plus the forward on the full tensors."""
     w = make_workload(name)
     win = dict(pre_tokens=pre, next_tokens=nxt)
     dout, q, k, v = host_inputs(w)
     out, lse = oracle_forward(w, q, k, v, blockrows=True, **win)
     tout, tlse = rounded_out_lse(w, out, lse)
     del out, lse
-    dq, dk, dv = (f64(t) for t in run_grad(w, dout, q, k, v, tout, tlse, pre, nxt))
-    args = (f64(dout), f64(q), f64(k), f64(v), f64(tout), f64(tlse))
-    kw = dict(mask=w.mask, block_shape=(w.bx, w.by), seq_q=w.seq_q, seq_kv=w.seq_kv,
-              layout=w.layout, num_kv_heads=w.N2, scale=w.scale, **win)
-    oq, ok_ = O.seq_offsets(w.seq_q), O.seq_offsets(w.seq_kv)
-    got_q, ref_q = [], []
-    for (b, h, s) in sampled_rows(w):
-        ref_q.append(O.backward_dq_rows(*args, b, h, np.array([s]), **kw)[0])
-        got_q.append(dq[b, h, s] if w.layout == "BNSD" else dq[oq[b] + s, h])
-    check(f"{name}:win:dq", np.array(got_q), np.array(ref_q))
-    got_k, got_v, ref_k, ref_v = [], [], [], []
-    for (b, g, t) in sampled_cols(w):
-        rk, rv = O.backward_dkdv_rows(*args, b, g, np.array([t]), **kw)
-        ref_k.append(rk[0])
-        ref_v.append(rv[0])
-        if w.layout == "BNSD":
-            got_k.append(dk[b, g, t])
-            got_v.append(dv[b, g, t])
-        else:
-            got_k.append(dk[ok_[b] + t, g])
-            got_v.append(dv[ok_[b] + t, g])
-    check(f"{name}:win:dk", np.array(got_k), np.array(ref_k))
-    check(f"{name}:win:dv", np.array(got_v), np.array(ref_v))
-    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    got = run_grad(w, dout, q, k, v, tout, tlse, pre, nxt)
+    check_whole(f"{name}:win", got, oracle_backward_whole(w, dout, q, k, v, tout, tlse, **win))
     fo, fl = run_fwd(w, q, k, v, pre, nxt)
     check(f"{name}:win:fwd_out", f64(fo), f64(tout))
     fin = np.isfinite(f64(tlse))

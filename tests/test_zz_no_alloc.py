@@ -3,8 +3,8 @@
 It serves callers that cannot allocate device memory (a caller-owned pool that
 forbids new allocations, an embedded runtime without a device allocator): it
 keeps its scratch in an array built into the library instead of a workspace.
-Its output must equal the workspace-based bsa_mask_compact exactly (integer
-index lists), on two calls in a row: the shared scratch keeps the previous
+Its output must equal the workspace-based bsa_mask_compact and the oracle's
+compaction exactly (integer index lists), on two calls in a row: the shared scratch keeps the previous
 call's contents, and a stale count must not leak into the next result.
 
 This file is collected last on purpose, so a run that stops at the first
@@ -15,6 +15,7 @@ import torch
 
 import block_sparse_attention_attn_gb300 as bsa
 from block_sparse_attention_attn_gb300 import binding as B
+from oracle import bsa_oracle as O
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -51,6 +52,10 @@ def test_noalloc_matches_workspace_compaction_twice():
         assert nnz == ref[1].numel()
         for g, r in zip(got, ref):
             np.testing.assert_array_equal(g.cpu().numpy(), r.cpu().numpy())
+        # and directly against the oracle's compaction (brute force on the host)
+        oref = O.compact_mask(mask.cpu().numpy(), bx, by, sq, skv)
+        for g, r in zip(got, oref):
+            np.testing.assert_array_equal(g.cpu().numpy(), r)
 
 
 def test_noalloc_rejects_masks_beyond_its_scratch():
