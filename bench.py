@@ -43,6 +43,10 @@ def parse():
     ap.add_argument("--workload", default="w1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations timed after the default w1 line")
+    ap.add_argument("--config-steps", type=int, default=100,
+                    help="timed steps of each other configuration")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic dQ mode (separate query-tile pass)")
     ap.add_argument("--forward", action="store_true",
@@ -204,18 +208,15 @@ def grad_executor(w, t, seq, dq, dk, dv):
 
 
 # --------------------------------------------------------------- our arm
-def bench_ours(args, rank, world, local):
+def time_backward(w, t, seq, dq, dk, dv, steps, warmup, local, world):
+    """The timed protocol of one workload: `warmup` untimed steps, then
+    `steps` steps, each after a 512 MB L2 flush, bracketed by CUDA events on
+    the launching stream, with the library's own events around the main
+    kernel. Returns (mean step ms, mean kernel ms, clocks, wall s, ws, size)."""
     import torch
 
     import block_sparse_attention_attn_gb300 as bsa
-    from block_sparse_attention_attn_gb300.workloads import make_workload, workload_summary
-    dev = torch.device("cuda", local)
-    w = make_workload(args.workload)
-    flops = w.flops()
-    t, seq = make_inputs(w, dev)
-    dq = torch.empty_like(t["query"])
-    dk = torch.empty_like(t["key"])
-    dv = torch.empty_like(t["value"])
+    dev = dq.device
     size, ex = grad_executor(w, t, seq, dq, dk, dv)
     ws = torch.empty(size, dtype=torch.uint8, device=dev)
     del ex
@@ -227,13 +228,13 @@ def bench_ours(args, rank, world, local):
             ex.set_timing_events(*ev)
         bsa.bsa_grad(ws, size, ex, stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         step(grad_executor(w, t, seq, dq, dk, dv)[1])
     torch.cuda.synchronize()
     bsa.bsa_check_status(ws)
 
-    n = args.steps
+    n = steps
     # host-side planning (first stage) happens before the timed region
     exs = [grad_executor(w, t, seq, dq, dk, dv)[1] for _ in range(n)]
     s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -259,10 +260,65 @@ def bench_ours(args, rank, world, local):
     barrier(world)
     clk = clocks.stop()
     bsa.bsa_check_status(ws)
+    del flush
     step_ms = [a.elapsed_time(b) for a, b in zip(s_ev, e_ev)]
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
     ms_step = max_over_ranks(float(np.mean(step_ms)), world)
     ms_kern = max_over_ranks(float(np.mean(kern_ms)), world)
+    return ms_step, ms_kern, clk, wall, ws, size
+
+
+# The other configurations of the workload table, timed in the same run
+# after the headline one (w1dense: configs[1] with mask = nullptr).
+OTHER_CONFIGS = ["w1dense", "w2", "w3", "w4"]
+
+
+def other_configs(args, world, local, peak):
+    """kernel / step time, roofline fraction and clocks of OTHER_CONFIGS."""
+    import torch
+
+    from block_sparse_attention_attn_gb300.workloads import make_workload
+    dev = torch.device("cuda", local)
+    res = {}
+    for name in OTHER_CONFIGS:
+        w = make_workload(name)
+        flops = w.flops()
+        t, seq = make_inputs(w, dev)
+        dq, dk, dv = (torch.empty_like(t[k_]) for k_ in ("query", "key", "value"))
+        steps = max(3, min(args.steps, args.config_steps))
+        ms_step, ms_kern, clk, _, ws, _ = time_backward(w, t, seq, dq, dk, dv, steps,
+                                                        max(3, args.warmup), local, world)
+        ach = flops / (ms_kern * 1e-3) / 1e12
+        res[name] = {"gflop_per_step": round(flops / 1e9, 2), "steps": steps,
+                     "ms_per_step": round(ms_step, 4),
+                     "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
+                     "kernel_ms": round(ms_kern, 4), "achieved": round(ach, 2),
+                     "frac": round(ach / peak, 4), "traffic": committed_traffic(name),
+                     "clocks": clk}
+        del t, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+    return res
+
+
+def bench_ours(args, rank, world, local):
+    import torch
+
+    import block_sparse_attention_attn_gb300 as bsa
+    from block_sparse_attention_attn_gb300.workloads import make_workload, workload_summary
+    dev = torch.device("cuda", local)
+    w = make_workload(args.workload)
+    flops = w.flops()
+    t, seq = make_inputs(w, dev)
+    dq = torch.empty_like(t["query"])
+    dk = torch.empty_like(t["key"])
+    dv = torch.empty_like(t["value"])
+    n = args.steps
+    ms_step, ms_kern, clk, wall, ws, size = time_backward(w, t, seq, dq, dk, dv, n, args.warmup,
+                                                          local, world)
+    stream = torch.cuda.current_stream()
+
+    def step(ex):
+        bsa.bsa_grad(ws, size, ex, stream)
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # end to end through the public API: pinned host inputs -> H2D -> first and
@@ -322,6 +378,8 @@ def bench_ours(args, rank, world, local):
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
     }
+    if args.workload == "w1" and not args.no_configs:
+        line["configs"] = other_configs(args, world, local, peak)
     if not args.no_cpu_baseline and rank == 0:
         try:
             line["cpu_baseline"] = cpu_baseline(w)
