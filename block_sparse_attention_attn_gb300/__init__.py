@@ -7,6 +7,7 @@ compute call raises if the library has not been built.
 """
 from .binding import (bsa_grad_workspace_size, bsa_grad, bsa_fwd_workspace_size,  # noqa: F401
                       bsa_fwd, bsa_mask_compact, bsa_mask_compact_noalloc, bsa_check_status,
+                      check_pending_status,
                       BsaError,
                       block_sparse_attention_grad, block_sparse_attention_fwd,
                       block_sparse_attention, BlockSparseAttentionFunction,

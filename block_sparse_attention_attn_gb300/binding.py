@@ -7,6 +7,7 @@ has not been built, every call raises :class:`BsaError` (there is no fallback).
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 from typing import Optional, Sequence
@@ -72,13 +73,14 @@ def load_library():
     lib.bsa_mask_compact_noalloc.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp,
                                              vp, vp]
     lib.bsa_check_status.argtypes = [vp, vp]
+    lib.bsa_status_async.argtypes = [vp, vp, vp]
     lib.bsa_last_error.restype = ctypes.c_char_p
     lib.bsa_version.restype = ctypes.c_int32
     for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
                  "bsa_executor_destroy", "bsa_executor_set_timing_events",
                  "bsa_executor_set_wait_test", "bsa_executor_set_deterministic",
                  "bsa_mask_compact_workspace_size", "bsa_mask_compact",
-                 "bsa_mask_compact_noalloc", "bsa_check_status"):
+                 "bsa_mask_compact_noalloc", "bsa_check_status", "bsa_status_async"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -226,6 +228,57 @@ def bsa_check_status(workspace: torch.Tensor, stream=None):
     _check(lib.bsa_check_status(workspace.data_ptr(), _stream(stream)))
 
 
+class _PendingStatus:
+    """Error words of recent runs, read without a host synchronization: each
+    run enqueues a copy of its workspace's error words into page-locked host
+    memory (bsa_status_async) and records an event; `poll` inspects the
+    copies whose event has completed and raises on a failed run. The
+    workspace stays referenced until its words have been read."""
+
+    MAX_PENDING = 64
+
+    def __init__(self):
+        self.pending = collections.deque()
+
+    def push(self, workspace: torch.Tensor):
+        """After a run on the current stream."""
+        lib = load_library()
+        words = torch.zeros(8, dtype=torch.int32, pin_memory=True)
+        stream = torch.cuda.current_stream()
+        _check(lib.bsa_status_async(workspace.data_ptr(), words.data_ptr(), stream.cuda_stream))
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self.pending.append((words, ev, workspace))
+        while len(self.pending) > self.MAX_PENDING:
+            self._pop(block=True)
+
+    def _pop(self, block: bool) -> bool:
+        words, ev, _ = self.pending[0]
+        if block:
+            ev.synchronize()
+        elif not ev.query():
+            return False
+        self.pending.popleft()
+        if int(words[0]) != 0:
+            raise BsaError(BSA_ERR_INNER, "a kernel of an earlier backward gave up a bounded "
+                                          f"wait (code {int(words[6])})")
+        return True
+
+    def poll(self, block: bool = False):
+        while self.pending and self._pop(block):
+            pass
+
+
+_PENDING = _PendingStatus()
+
+
+def check_pending_status(block: bool = True):
+    """Raises BsaError if any backward run by the autograd function since the
+    last check failed (block=True waits for all of them; False inspects only
+    those that have finished)."""
+    _PENDING.poll(block)
+
+
 def bsa_mask_compact(mask: torch.Tensor, bx: int, by: int, actual_seq_lengths=None,
                      actual_seq_lengths_kv=None, stream=None):
     """Block-level CSR/CSC of a block mask: (row_ptr, col_idx, col_ptr, row_idx),
@@ -323,12 +376,15 @@ class BlockSparseAttentionFunction(torch.autograd.Function):
     """Autograd pairing of the companion forward (Out, lse) and the backward:
     forward runs bsa_fwd, backward runs bsa_grad on the saved Q, K, V, Out and
     lse (the page's call sequence, with PyTorch driving it). The mask, block
-    shape, lengths and options are not differentiable."""
+    shape, lengths and options are not differentiable. Neither direction
+    synchronizes the host: a backward run's error words are copied
+    asynchronously and checked by later calls or by check_pending_status()."""
 
     @staticmethod
     def forward(ctx, query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
                 actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic,
                 pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
+        _PENDING.poll()   # failures of earlier backward runs surface here, without a sync
         if scale_value is None:
             scale_value = query.shape[-1] ** -0.5
         query, key, value = query.contiguous(), key.contiguous(), value.contiguous()
@@ -353,7 +409,10 @@ class BlockSparseAttentionFunction(torch.autograd.Function):
             actual_seq_lengths, actual_seq_lengths_kv, layout, num_key_value_heads, scale_value,
             deterministic=deterministic, pre_tokens=pre_tokens, next_tokens=next_tokens,
             atten_mask=ctx.atten_mask)
-        bsa_check_status(ws)
+        # no host synchronization here: the run's error words are read later
+        # (next forward, or check_pending_status())
+        _PENDING.poll()
+        _PENDING.push(ws)
         return dq, dk, dv, None, None, None, None, None, None, None, None, None, None, None
 
 

@@ -9,6 +9,7 @@
 // attenMask NULL, maskType 0) and the constraints (section 约束说明: N1 % N2 == 0,
 // equal q/kv layouts). preTokens / nextTokens define a sliding window (any
 // pair with preTokens + nextTokens >= 0) instead of being fixed at 2147483647.
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -516,6 +517,14 @@ void fill_geometry(Plan& p, const Geometry& g, double scale, int num_sms) {
   p.num_sms = num_sms;
 }
 
+// Work-list entries keep a query-tile index in 20 bits (pack_entry): the
+// longest query sequence may span at most 2^20 tiles of 128 tokens.
+bool query_tiles_fit(const Geometry& g) {
+  int64_t mqt = g.layout == kLayoutBNSD ? ceil_div_i(g.Sq, kTile) : 0;
+  for (int b = 0; b < g.B; ++b) mqt = std::max<int64_t>(mqt, ceil_div_i(g.lq[b], kTile));
+  return mqt <= ((int64_t)1 << 20);
+}
+
 void set_info_ptrs(Plan& p, const bsa_executor* ex, uint8_t* ws) {
   const int* info = reinterpret_cast<const int*>(ws + ex->off_info);
   p.lq = info + ex->n_info_off[0];
@@ -613,6 +622,8 @@ bsa_status bsa_grad_workspace_size(
     return fail(BSA_ERR_PARAM_INVALID, "dq/dk/dv shapes must equal query/key/value shapes");
   if (!out_strides_ok(dq) || !out_strides_ok(dk) || !out_strides_ok(dv))
     return fail(BSA_ERR_PARAM_INVALID, "dq/dk/dv strides must be positive");
+  if (!query_tiles_fit(g))
+    return fail(BSA_ERR_PARAM_INVALID, "query sequences longer than 2^27 tokens");
   int num_sms = query_num_sms(&st);
   if (st != BSA_OK) return fail(BSA_ERR_RUNTIME, "no CUDA device available");
 
@@ -820,6 +831,15 @@ bsa_status bsa_check_status(const void* workspace, void* stream) {
   return ok();
 }
 
+bsa_status bsa_status_async(const void* workspace, int32_t* host_words, void* stream) {
+  if (workspace == nullptr || host_words == nullptr)
+    return fail(BSA_ERR_PARAM_NULLPTR, "workspace and host_words are required");
+  const cudaError_t e = cudaMemcpyAsync(host_words, workspace, 8 * sizeof(int32_t),
+                                        cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "CUDA error: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 // ---------------------------------------------------------------------------
 // mask compaction on its own
 // ---------------------------------------------------------------------------
@@ -860,6 +880,10 @@ bsa_status bsa_mask_compact(const bsa_tensor* mask, int64_t bx, int64_t by,
     return fail(BSA_ERR_PARAM_INVALID, "sequence lengths need one entry per batch");
   if ((int64_t)B * N * Mq * Mk >= ((int64_t)1 << 31))
     return fail(BSA_ERR_PARAM_INVALID, "mask too large");
+  // the kernels keep block sizes and token positions in int
+  if (bx > INT_MAX || by > INT_MAX || (int64_t)Mq * bx > INT_MAX - 128 ||
+      (int64_t)Mk * by > INT_MAX - 128)
+    return fail(BSA_ERR_PARAM_INVALID, "block size or mask extent beyond 2^31 tokens");
   std::vector<int> lens(2 * B);
   for (int b = 0; b < B; ++b) {
     const int64_t a = actual_seq_lengths ? actual_seq_lengths[b] : (int64_t)Mq * bx;
@@ -875,7 +899,7 @@ bsa_status bsa_mask_compact(const bsa_tensor* mask, int64_t bx, int64_t by,
   int* ccnt = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(rcnt) +
                                      align256((uint64_t)B * N * (Mq + 1) * 4));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(dlens, lens.data(), lens.size() * 4, cudaMemcpyHostToDevice, s);
+  cudaError_t e = launch_upload(lens.data(), (int)lens.size(), dlens, s);
   CompactArgs ca{};
   ca.mask = static_cast<const uint8_t*>(mask->data);
   ca.sb = mask->stride[0]; ca.sh = mask->stride[1]; ca.si = mask->stride[2];
@@ -942,6 +966,8 @@ bsa_status bsa_fwd_workspace_size(
     return fail(BSA_ERR_PARAM_INVALID, "attentionOut must match query's dtype and shape");
   if (!check_lse(softmax_lse, g))
     return fail(BSA_ERR_PARAM_INVALID, "softmaxLse must be FLOAT32, contiguous, [..,Sq(,1)]");
+  if (!query_tiles_fit(g))
+    return fail(BSA_ERR_PARAM_INVALID, "query sequences longer than 2^27 tokens");
   int num_sms = query_num_sms(&st);
   if (st != BSA_OK) return fail(BSA_ERR_RUNTIME, "no CUDA device available");
   bsa_executor* ex = new bsa_executor();

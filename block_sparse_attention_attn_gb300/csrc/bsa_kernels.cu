@@ -549,11 +549,20 @@ static cudaError_t upload_t(const int* host, int n, int* dst, cudaStream_t st) {
   return cudaGetLastError();
 }
 cudaError_t launch_upload(const int* host, int n, int* dst, cudaStream_t st) {
+  // longer arrays go in several launches of 7680 ints (30 KB of parameters)
+  // each, so the caller's host array is never read after the call returns
+  // (stream capture records the parameters by value)
+  while (n > 7680) {
+    const cudaError_t e = upload_t<7680>(host, 7680, dst, st);
+    if (e != cudaSuccess) return e;
+    host += 7680;
+    dst += 7680;
+    n -= 7680;
+  }
   if (n <= 0) return cudaSuccess;
   if (n <= 256) return upload_t<256>(host, n, dst, st);
   if (n <= 2048) return upload_t<2048>(host, n, dst, st);
-  if (n <= 7680) return upload_t<7680>(host, n, dst, st);  // 30 KB of parameters
-  return cudaMemcpyAsync(dst, host, sizeof(int) * n, cudaMemcpyHostToDevice, st);
+  return upload_t<7680>(host, n, dst, st);
 }
 
 // --------------------------------------------------------------------------

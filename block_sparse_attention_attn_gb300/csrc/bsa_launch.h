@@ -39,8 +39,9 @@ struct CompactArgs {
 // Sets the thread's bsa_last_error() text (used by entry points outside bsa_api.cpp).
 void set_last_error(const char* msg);
 
-// n ints from host memory to dst: through kernel parameters when small, else
-// one cudaMemcpyAsync.
+// n ints from host memory to dst, through kernel parameters (one launch per
+// 7680 ints): the host array may be reused as soon as the call returns, and
+// the upload can be captured in a CUDA graph.
 cudaError_t launch_upload(const int* host, int n, int* dst, cudaStream_t st);
 cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st);
 

@@ -16,10 +16,14 @@
 // contents, so calls that overlap on the GPU (different streams with no
 // ordering between them) race and corrupt each other's results. The first call
 // on a device looks up the array's device address (once per device, with that
-// device current); make that first call before any stream capture.
+// device current); make that first call before any stream capture. The address
+// is looked up again when the device's context has changed since (after a
+// cudaDeviceReset the library's module, and with it the array, is loaded anew).
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "bsa.h"
@@ -38,6 +42,33 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // id of the context the address belongs to
+
+// Unique id of the calling thread's current context (driver entry points
+// through the runtime, no link dependency on libcuda); 0 if unavailable.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
@@ -75,6 +106,9 @@ extern "C" bsa_status bsa_mask_compact_noalloc(const bsa_tensor* mask, int64_t b
   if ((actual_seq_lengths && n_seq != B) || (actual_seq_lengths_kv && n_seq_kv != B))
     return fail(BSA_ERR_PARAM_INVALID, "sequence lengths need one entry per batch");
   if (B * N * Mq * Mk >= ((int64_t)1 << 31)) return fail(BSA_ERR_PARAM_INVALID, "mask too large");
+  // the kernels keep block sizes and token positions in int
+  if (bx > INT_MAX || by > INT_MAX || Mq * bx > INT_MAX - 128 || Mk * by > INT_MAX - 128)
+    return fail(BSA_ERR_PARAM_INVALID, "block size or mask extent beyond 2^31 tokens");
   // scratch layout: lengths [2B] | row counts [B*N*(Mq+1)] | column counts [B*N*(Mk+1)]
   const uint64_t off_rows = align256(2 * (uint64_t)B * 4);
   const uint64_t off_cols = off_rows + align256((uint64_t)(B * N * (Mq + 1)) * 4);
@@ -101,7 +135,8 @@ extern "C" bsa_status bsa_mask_compact_noalloc(const bsa_tensor* mask, int64_t b
   uint8_t* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || p == nullptr) {
@@ -109,6 +144,8 @@ extern "C" bsa_status bsa_mask_compact_noalloc(const bsa_tensor* mask, int64_t b
         return fail(BSA_ERR_RUNTIME, "cudaGetSymbolAddress of the built-in scratch failed");
       }
       g_scratch_ptr[dev] = p;
+      // the runtime's call above made the device's primary context current
+      g_scratch_ctx[dev] = ctx != 0 ? ctx : current_context_id();
     }
     scratch = static_cast<uint8_t*>(g_scratch_ptr[dev]);
   }
@@ -118,7 +155,8 @@ extern "C" bsa_status bsa_mask_compact_noalloc(const bsa_tensor* mask, int64_t b
   int* ccnt = reinterpret_cast<int*>(scratch + off_cols);
   // every count the kernels read is written by the count passes first, so only
   // the lengths have to be refreshed (the array keeps the previous call's data)
-  cudaError_t e = cudaMemcpyAsync(dlens, lens, 2 * (size_t)B * 4, cudaMemcpyHostToDevice, st);
+  // through kernel parameters: the stack array is not read after the return
+  cudaError_t e = bsa::launch_upload(lens, 2 * (int)B, dlens, st);
   bsa::CompactArgs ca{};
   ca.mask = static_cast<const uint8_t*>(mask->data);
   ca.sb = mask->stride[0];

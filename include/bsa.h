@@ -215,7 +215,10 @@ bsa_status bsa_mask_compact(const bsa_tensor* block_sparse_mask, int64_t bx, int
  * fit, and B > 1024. All calls share the array and it keeps the last call's
  * contents: calls that overlap on the GPU race. The first call on a device
  * looks up the array's address (with that device current); make it before any
- * stream capture. Asynchronous on `stream`. */
+ * stream capture. The lookup is repeated when the device's context has
+ * changed (e.g. after cudaDeviceReset). The sequence lengths travel as kernel
+ * parameters, so the host arrays may be reused once the call returns.
+ * Asynchronous on `stream`. */
 bsa_status bsa_mask_compact_noalloc(const bsa_tensor* block_sparse_mask, int64_t bx, int64_t by,
                                     const int64_t* actual_seq_lengths, int64_t n_seq,
                                     const int64_t* actual_seq_lengths_kv, int64_t n_seq_kv,
@@ -226,6 +229,15 @@ bsa_status bsa_mask_compact_noalloc(const bsa_tensor* block_sparse_mask, int64_t
  * of `workspace`: BSA_OK, or BSA_ERR_INNER if a kernel gave up a bounded wait
  * (the outputs are then not valid). 361001 if the CUDA calls fail. */
 bsa_status bsa_check_status(const void* workspace, void* stream);
+
+/* The same error words without a host synchronization: enqueues on `stream` a
+ * copy of the first 8 int32 words of `workspace` into `host_words` (caller-owned
+ * host memory of at least 32 bytes; page-locked memory keeps the copy
+ * asynchronous). Once the stream has passed the copy, host_words[0] != 0 means
+ * a kernel of the preceding run gave up a bounded wait (host_words[6] holds the
+ * code of the first failed wait). 161001 for NULL pointers, 361001 if the copy
+ * cannot be enqueued. */
+bsa_status bsa_status_async(const void* workspace, int32_t* host_words, void* stream);
 
 /* One-line description of the last failure in this thread ("" if none). */
 const char* bsa_last_error(void);
