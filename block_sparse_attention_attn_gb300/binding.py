@@ -230,27 +230,39 @@ def bsa_check_status(workspace: torch.Tensor, stream=None):
 
 class _PendingStatus:
     """Error words of recent runs, read without a host synchronization: each
-    run enqueues a copy of its workspace's error words into page-locked host
-    memory (bsa_status_async) and records an event; `poll` inspects the
-    copies whose event has completed and raises on a failed run. The
-    workspace stays referenced until its words have been read."""
+    run enqueues a copy of its workspace's error words into a slot of a
+    page-locked ring (bsa_status_async) and records an event; `poll` inspects
+    the copies whose event has completed and raises on a failed run. The
+    workspace stays referenced until its words have been read. The ring is
+    allocated once (`reserve`, called by the autograd forward), since a
+    page-locked allocation may itself wait for the device."""
 
-    MAX_PENDING = 64
+    SLOTS = 64
 
     def __init__(self):
         self.pending = collections.deque()
+        self.words = None
+        self.next = 0
+
+    def reserve(self):
+        if self.words is None:
+            self.words = torch.zeros((self.SLOTS, 8), dtype=torch.int32, pin_memory=True)
 
     def push(self, workspace: torch.Tensor):
         """After a run on the current stream."""
-        lib = load_library()
-        words = torch.zeros(8, dtype=torch.int32, pin_memory=True)
+        self.reserve()
+        while len(self.pending) >= self.SLOTS:   # slots are reused in FIFO order
+            self._pop(block=True)
+        slot = self.next
+        self.next = (slot + 1) % self.SLOTS
+        words = self.words[slot]
+        words.zero_()
         stream = torch.cuda.current_stream()
-        _check(lib.bsa_status_async(workspace.data_ptr(), words.data_ptr(), stream.cuda_stream))
+        _check(load_library().bsa_status_async(workspace.data_ptr(), words.data_ptr(),
+                                               stream.cuda_stream))
         ev = torch.cuda.Event()
         ev.record(stream)
         self.pending.append((words, ev, workspace))
-        while len(self.pending) > self.MAX_PENDING:
-            self._pop(block=True)
 
     def _pop(self, block: bool) -> bool:
         words, ev, _ = self.pending[0]
@@ -384,6 +396,7 @@ class BlockSparseAttentionFunction(torch.autograd.Function):
     def forward(ctx, query, key, value, block_sparse_mask, block_shape, actual_seq_lengths,
                 actual_seq_lengths_kv, layout, num_key_value_heads, scale_value, deterministic,
                 pre_tokens=NO_WINDOW, next_tokens=NO_WINDOW, atten_mask=None):
+        _PENDING.reserve()
         _PENDING.poll()   # failures of earlier backward runs surface here, without a sync
         if scale_value is None:
             scale_value = query.shape[-1] ** -0.5

@@ -21,12 +21,21 @@ def test_multi_layer_backward_does_not_sync():
     dout, q, k, v = host_inputs(w)
     mask = torch.from_numpy(w.mask).to(DEV)
     layers = 4
-    qs = [q.to(DEV).requires_grad_(True) for _ in range(layers)]
-    kd, vd = k.to(DEV).requires_grad_(True), v.to(DEV).requires_grad_(True)
-    outs = [bsa.block_sparse_attention(x, kd, vd, block_sparse_mask=mask, block_shape=[128, 128],
-                                       num_key_value_heads=w.N2, scale_value=w.scale)
-            for x in qs]
-    loss = sum((o.float() * dout.to(DEV).float()).sum() for o in outs)
+
+    def step():
+        qs = [q.to(DEV).requires_grad_(True) for _ in range(layers)]
+        kd, vd = k.to(DEV).requires_grad_(True), v.to(DEV).requires_grad_(True)
+        outs = [bsa.block_sparse_attention(x, kd, vd, block_sparse_mask=mask,
+                                           block_shape=[128, 128], num_key_value_heads=w.N2,
+                                           scale_value=w.scale)
+                for x in qs]
+        loss = sum((o.float() * dout.to(DEV).float()).sum() for o in outs)
+        return qs, kd, vd, outs, loss
+    # one warm-up step: first-use set-up (device and page-locked allocations,
+    # the library's side stream) may wait for the device
+    step()[-1].backward()
+    bsa.check_pending_status()
+    qs, kd, vd, outs, loss = step()
     torch.cuda.synchronize()
     torch.cuda._sleep(2_000_000_000)     # ~1 s of GPU time ahead of the backward
     loss.backward()

@@ -119,10 +119,12 @@ def test_autograd_function(deterministic):
 
 
 def test_deterministic_large_token_masked():
-    """w1doc (dense B2 N16 S4096 with causal documents as attenMask) in the
-    deterministic mode: two runs give identical bytes, and the whole outputs
-    match the oracle."""
+    """w1doc's shape and token mask (dense B2 N16 S4096 with causal documents
+    as attenMask) in the deterministic mode, in fp16 (see
+    test_atten_mask_large_whole): two runs give identical bytes, and the whole
+    outputs match the oracle."""
     w = make_workload("w1doc")
+    w.dtype = "f16"
     dout, q, k, v = host_inputs(w)
     win = dict(atten_mask=w.atten_mask)
     out, lse = oracle_forward(w, q, k, v, blockrows=True, **win)
