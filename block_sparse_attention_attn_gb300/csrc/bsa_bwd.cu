@@ -9,7 +9,7 @@
 //     dQ   = dS K                  -> fp32 accumulator in global memory (atomics)
 // with D = rowsum(dO o attentionOut) from the preprocess kernel.
 //
-// Design (one persistent CTA per SM, 480 threads, warp-specialised):
+// Design (one persistent CTA per SM, 512 threads, warp-specialised):
 //   warp 12     TMA producer: K/V tiles of the key tile (once per work item),
 //               then a 2-stage ring of Q tiles (with their lse/D rows) and
 //               one dO buffer.
@@ -19,9 +19,11 @@
 //               handles query columns [64w, 64w+64): P^T (into TMEM, packed, as
 //               the A operand of the dV MMA) and dS (into shared memory, the
 //               operand of both the dQ and the dK MMA).
-//   warps 8-11  drain: dQ tile TMEM -> fp32 accumulator (TMA reduce-add); at
-//               the end of a work item, dK/dV TMEM -> output (or fp32 slot for
-//               split columns).
+//   warps 8-11  drain: dQ tile TMEM -> registers (the whole row in one load, so
+//               the columns go straight back to the next dP) -> fp32
+//               accumulator (TMA reduce-add); at the end of a work item, dK/dV
+//               TMEM -> output (or fp32 slot for split columns). Warp 15 only
+//               lends its registers to the drain warps.
 // A work item is one key tile (b, kv head g, jt) with the query tiles of all
 // G query heads of the group that select it (so the GQA sum happens in TMEM),
 // or a chunk of such a list when the planner split a long column.
@@ -45,14 +47,20 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 480;
-constexpr int kProducerWarp = 12;
+constexpr int kThreads = 512;
+constexpr int kProducerWarp = 12;  // warps 12-15: producer, two MMA issuers, one idle warp
 constexpr int kMmaWarp = 13;   // dP, dV, S; TMEM owner
 constexpr int kMma2Warp = 14;  // dQ, dK
 constexpr int kDrainWarp0 = 8;
 constexpr int kPanel = 128 * 128;  // 128 rows x 128 bytes (64 x 16-bit), one swizzle span
 constexpr int kStages = 2;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColP = 384;
+// Registers per thread after the hand-over (launch: 512 x 128): the control
+// warpgroup gives 48 of its 128 to the drain warpgroup, which reads a whole
+// dQ row (D values) out of TMEM at once: 128 + 128 + 176 + 80 = 4 x 128.
+// Each budget has its own copy of the out-of-line wait loop (wait tags).
+constexpr int kRegsCtl = 80, kRegsDrain = 176;
+constexpr int kTagCtl = 1, kTagSoftmax = 2, kTagDrain = 3;
 
 // Offset of K-step k (16 elements) inside a 128-byte-swizzled tile, in the
 // 16-byte units of a shared-memory descriptor's address field: K-major tiles
@@ -248,6 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // was last read by the current item's final dP, and its V into the buffer
   // whose K was last read by the final dQ, so both loads overlap the end of
   // the current item.
+  if (warp >= kProducerWarp) {
+  regs_release<kRegsCtl>();  // all four warps of the control warpgroup
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     uint32_t n = 0, fc = 0, ic = 0;  // tiles, ring slots filled, non-empty items
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // through the aux barrier, its rows past the key length are cleared and
     // then the full barrier is released by hand.
     auto load_buf = [&](int bi, const CUtensorMap* tm, const ItemInfo& it, int t_valid) -> bool {
-      if (!mbar_wait(&bars[kBufEmpty0 + bi], (ic & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kBufEmpty0 + bi], (ic & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitKV);
         return false;
       }
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pending_buf[bi] = tail ? 0 : 1;
       pending_buf_aux[bi] = tail ? 1 : 0;
       if (tail) {
-        if (!mbar_wait(&bars[kBufAux0 + bi], buf_aux_cnt[bi] & 1, abort_flag)) {
+        if (!mbar_wait<kTagCtl>(&bars[kBufAux0 + bi], buf_aux_cnt[bi] & 1, abort_flag)) {
           record_error(p.header, kErrWaitKV);
           return false;
         }
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok) {
       const int4 raw = next;
       const int slot = fc & 1;
-      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((fc >> 1) & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kItemEmpty0 + slot], ((fc >> 1) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitItem);
         break;
       }
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c1 = p.layout == kLayoutBNSD ? q0 : h;
         const int c2 = p.layout == kLayoutBNSD ? ii.b * p.N1 + h : p.cu_q[ii.b] + q0;
         // Q (stage st) with its lse / D rows
-        if (!mbar_wait(&bars[kQEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait<kTagCtl>(&bars[kQEmpty0 + st], ((n >> 1) & 1) ^ 1, abort_flag)) {
           record_error(p.header, kErrWaitQ);
           ok = false;
           break;
@@ -365,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (tail) {
-          if (!mbar_wait(&bars[kQAux0 + st], aux_cnt[st] & 1, abort_flag)) {
+          if (!mbar_wait<kTagCtl>(&bars[kQAux0 + st], aux_cnt[st] & 1, abort_flag)) {
             record_error(p.header, kErrWaitQ);
             ok = false;
             break;
@@ -388,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         // dO (single buffer): free once the previous tile's dV MMA completed
-        if (!mbar_wait(&bars[kDoEmpty], (n & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait<kTagCtl>(&bars[kDoEmpty], (n & 1) ^ 1, abort_flag)) {
           record_error(p.header, kErrWaitQ);
           ok = false;
           break;
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pending_do = tail ? 0 : 1;
         pending_do_aux = tail ? 1 : 0;
         if (tail) {
-          if (!mbar_wait(&bars[kDoAux], do_aux_cnt & 1, abort_flag)) {
+          if (!mbar_wait<kTagCtl>(&bars[kDoAux], do_aux_cnt & 1, abort_flag)) {
             record_error(p.header, kErrWaitQ);
             ok = false;
             break;
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch = [&](int& e0, int& e1) -> int {
       while (true) {
         const int slot = fc & 1;
-        if (!mbar_wait(&bars[kItemFull0 + slot], (fc >> 1) & 1, abort_flag)) return -1;
+        if (!mbar_wait<kTagCtl>(&bars[kItemFull0 + slot], (fc >> 1) & 1, abort_flag)) return -1;
         const int4 raw = item_slot[slot];
         __syncwarp();
         if (elect_one()) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -463,9 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have > 0) {  // S of the very first tile
       // test of the bounded waits: a barrier no one arrives at runs out, the
       // CTA unwinds and the host reads the error code
-      if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) where = kErrWaitTest;
-      else if (!mbar_wait(&bars[kBufFull0], 0, abort_flag)) where = kErrWaitKV;
-      else if (!mbar_wait(&bars[kQFull0], 0, abort_flag)) where = kErrWaitQ;
+      if (p.wait_test && !mbar_wait<kTagCtl>(&bars[kNeverBar], 0, abort_flag)) where = kErrWaitTest;
+      else if (!mbar_wait<kTagCtl>(&bars[kBufFull0], 0, abort_flag)) where = kErrWaitKV;
+      else if (!mbar_wait<kTagCtl>(&bars[kQFull0], 0, abort_flag)) where = kErrWaitQ;
       else {
         tc_fence_after();
         issue_s(0, aBuf0);
@@ -481,9 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool last = e + 1 == ce1;
         // dP^T = V dO^T: the dP columns hold dQ of the previous tile until
         // the drain warps have read it
-        if (!mbar_wait(&bars[kDqEmpty], (n & 1) ^ 1, abort_flag)) { where = kErrWaitDQ; break; }
-        if (first && !mbar_wait(&bars[kBufFull0 + vb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
-        if (!mbar_wait(&bars[kDoFull], n & 1, abort_flag)) { where = kErrWaitQ; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kDqEmpty], (n & 1) ^ 1, abort_flag)) { where = kErrWaitDQ; break; }
+        if (first && !mbar_wait<kTagCtl>(&bars[kBufFull0 + vb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kDoFull], n & 1, abort_flag)) { where = kErrWaitQ; break; }
         tc_fence_after();
         if (elect_one()) {  // dP^T = V dO^T
           const uint64_t dV = sdesc_sw128(aV, 16, 1024), dO = sdesc_sw128(adO, 16, 1024);
@@ -495,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (last) tc_commit(&bars[kBufEmpty0 + vb]);  // V read for the last time
         }
         __syncwarp();
-        if (!mbar_wait(&bars[kPReady], n & 1, abort_flag)) { where = kErrWaitP; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kPReady], n & 1, abort_flag)) { where = kErrWaitP; break; }
         // the first dV/dK MMAs of an item overwrite the accumulators: the drain
         // warps must have read the previous item's dK/dV
-        if (first && !mbar_wait(&bars[kAccEmpty], (ic & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        if (first && !mbar_wait<kTagCtl>(&bars[kAccEmpty], (ic & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
         tc_fence_after();
         if (elect_one()) {  // dV^T += P^T dO  (A = P^T in TMEM, packed)
           const uint64_t dOmn = sdesc_sw128(adO, kPanel, 1024);
@@ -520,14 +530,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           have_next = fetch(ne0, ne1);
           if (have_next < 0) { where = kErrWaitItem; break; }
           if (have_next > 0) {
-            if (p.wait_test && !mbar_wait(&bars[kNeverBar], 0, abort_flag)) { where = kErrWaitTest; break; }
-            if (!mbar_wait(&bars[kBufFull0 + vb], (ic + 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
+            if (p.wait_test && !mbar_wait<kTagCtl>(&bars[kNeverBar], 0, abort_flag)) { where = kErrWaitTest; break; }
+            if (!mbar_wait<kTagCtl>(&bars[kBufFull0 + vb], (ic + 1) & 1, abort_flag)) { where = kErrWaitKV; break; }
             next_s = true;
           }
         }
         if (next_s) {
-          if (!mbar_wait(&bars[kDvDone], n & 1, abort_flag)) { where = kErrWaitMisc; break; }
-          if (!mbar_wait(&bars[kQFull0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1, abort_flag)) {
+          if (!mbar_wait<kTagCtl>(&bars[kDvDone], n & 1, abort_flag)) { where = kErrWaitMisc; break; }
+          if (!mbar_wait<kTagCtl>(&bars[kQFull0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1, abort_flag)) {
             where = kErrWaitQ;
             break;
           }
@@ -560,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int4 raw = item_slot[slot];
       __syncwarp();
       if (elect_one()) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -574,10 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool first = e == e0, last = e + 1 == e1;
         const int st = n & 1;
         const uint32_t aQ = smem_u32(sQ0 + st * S::kTileBytes);
-        if (!mbar_wait(&bars[kDsReady], n & 1, abort_flag)) { where = kErrWaitDS; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kDsReady], n & 1, abort_flag)) { where = kErrWaitDS; break; }
         if (first) {  // this item's K, and dK of the previous item read out
-          if (!mbar_wait(&bars[kBufFull0 + kb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
-          if (!mbar_wait(&bars[kAccEmpty], (ic & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+          if (!mbar_wait<kTagCtl>(&bars[kBufFull0 + kb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
+          if (!mbar_wait<kTagCtl>(&bars[kAccEmpty], (ic & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
         }
         tc_fence_after();
         if (elect_one()) {
@@ -616,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       mbar_wait_drain(&bars[kDrainBar2], 0);
     }
+  }
   } else if (warp < kDrainWarp0) {
     // ------------------------------------------------------------- softmax
     const int wg = warp >> 2;  // query columns [64 wg, 64 wg + 64)
@@ -626,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagSoftmax>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int4 raw = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -670,8 +681,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const int st = n & 1;
-        if (!mbar_wait(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
-        if (!mbar_wait(&bars[kSFull], n & 1, abort_flag)) { where = kErrWaitS; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kSFull], n & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
         const float* lse2 = sLse + st * 128;
         const float* dv = sDv + st * 128;
@@ -708,8 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kPReady]);
-        if (!mbar_wait(&bars[kDpFull], n & 1, abort_flag)) { where = kErrWaitDP; break; }
-        if (!mbar_wait(&bars[kDsFree], (n & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kDpFull], n & 1, abort_flag)) { where = kErrWaitDP; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kDsFree], (n & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -754,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (where) record_error(p.header, where);
   } else {
+    regs_claim<kRegsDrain>();
     // -------------------------------------------------------------- drain
     const int qd = warp & 3;
     const int r = qd * 32 + lane;  // TMEM lane: query row (dQ) / key row (dK, dV)
@@ -762,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagDrain>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int4 raw = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -774,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t ent = p.entries[e];
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
-        if (!mbar_wait(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
+        if (!mbar_wait<kTagDrain>(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
         tc_fence_after();
         if (p.det) {  // no dQ here: the columns go straight back to the next dP
           tc_fence_before();
@@ -783,58 +795,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
           continue;
         }
-        // dQ tile -> fp32 accumulator with TMA reduce-adds. Each warp owns 32
-        // rows and an 8 KB part of the staging buffer: two 32 x 32 fp32 boxes
-        // (128-byte swizzled), i.e. 64 columns at a time. With D = 128 the
-        // columns [64, 128) wait in registers while the first boxes are read,
-        // so the TMEM columns go back to the next dP at once. Rows past the
-        // query length carry exact zeros (dS = 0 there) and land in the padded
-        // part of the accumulator.
+        // dQ tile -> fp32 accumulator with TMA reduce-adds. The thread's whole
+        // row (D columns) comes out of TMEM in one load, so the columns go
+        // back to the next dP before any staging. Each warp owns 32 rows and
+        // an 8 KB part of the staging buffer: two 32 x 32 fp32 boxes
+        // (128-byte swizzled), i.e. 64 columns at a time. Rows past the query
+        // length carry exact zeros (dS = 0 there) and land in the padded part
+        // of the accumulator.
         const int grow = h * p.Rq + p.qrow[ii.b] + it * 128 + qd * 32;
         uint8_t* boxes = sStg + qd * 8192;
         uint8_t* rowp = boxes + lane * 128;
-        if (lane == 0) bulk_wait_read_all();  // the previous tile's boxes were read
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + kColP + 32 * c, x);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(rowp + c * 4096 + ((j ^ (lane & 7)) << 4)) =
-                make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-        }
-        uint32_t hold[2][32];
-        if constexpr (D == 128) {
-          tmem_ld32(tmem + lane_off + kColP + 64, hold[0]);
-          tmem_ld32(tmem + lane_off + kColP + 96, hold[1]);
-        }
+        uint32_t acc[D];
+        if constexpr (D == 128) tmem_ld128(tmem + lane_off + kColP, acc);
+        else tmem_ld64(tmem + lane_off + kColP, acc);
         tc_fence_before();
-        fence_async_smem();
         __syncwarp();
-        const uint64_t pol = l2_policy_evict_last();  // keep dQ accumulator rows in L2
-        if (lane == 0) {
-          mbar_arrive(&bars[kDqEmpty]);  // TMEM columns free for the next dP
-          tma_reduce_add_2d_hint(&tm_acc, boxes, 0, grow, pol);
-          tma_reduce_add_2d_hint(&tm_acc, boxes + 4096, 32, grow, pol);
-          bulk_commit_group();
-        }
-        if constexpr (D == 128) {
-          if (lane == 0) bulk_wait_read_all();  // the first boxes were read
+        if (lane == 0) mbar_arrive(&bars[kDqEmpty]);  // TMEM columns free for the next dP
+        const uint64_t pol = l2_policy_evict_last();   // keep dQ accumulator rows in L2
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          if (lane == 0) bulk_wait_read_all();  // the boxes' previous contents were read
           __syncwarp();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+            for (int j = 0; j < 8; ++j) {
+              const int x0 = 64 * hf + 32 * c + 4 * j;
               *reinterpret_cast<uint4*>(rowp + c * 4096 + ((j ^ (lane & 7)) << 4)) =
-                  make_uint4(hold[c][4 * j], hold[c][4 * j + 1], hold[c][4 * j + 2],
-                             hold[c][4 * j + 3]);
+                  make_uint4(acc[x0], acc[x0 + 1], acc[x0 + 2], acc[x0 + 3]);
+            }
           }
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d_hint(&tm_acc, boxes, 64, grow, pol);
-            tma_reduce_add_2d_hint(&tm_acc, boxes + 4096, 96, grow, pol);
+            tma_reduce_add_2d_hint(&tm_acc, boxes, 64 * hf, grow, pol);
+            tma_reduce_add_2d_hint(&tm_acc, boxes + 4096, 64 * hf + 32, grow, pol);
             bulk_commit_group();
           }
         }
@@ -843,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (where) break;
       // dK / dV of the key tile
-      if (!mbar_wait(&bars[kAccFull], ic & 1, abort_flag)) { where = kErrWaitAcc; break; }
+      if (!mbar_wait<kTagDrain>(&bars[kAccFull], ic & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const int trow = ii.jt * 128 + r;
       const bool row_ok = (p.layout == kLayoutBNSD) ? (trow < p.Skv) : (trow < Lk);
@@ -974,6 +969,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int DT, bool EM>
 cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
   const size_t smem = Smem<D>::kBytes;
+  // The register hand-over only balances when every thread starts with 128
+  // registers (the claim would otherwise wait for registers nobody frees).
+  static const int regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, k_bwd<D, DT, EM>) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  static_assert(2 * 128 + kRegsDrain + kRegsCtl == 4 * 128, "register hand-over must balance");
+  if (regs != 128) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(k_bwd<D, DT, EM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
