@@ -863,38 +863,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool tma_out = p.dkv_tma && slot_base == nullptr &&
                            (p.layout == kLayoutBNSD || ii.jt * 128 + 128 <= Lk);
       if (tma_out) {
+        // The accumulator rows leave TMEM before any TMA store: dK is read,
+        // scaled, packed and staged, then dV is read and packed, and the
+        // columns go back to the next item's first dV / dK; the stores follow.
         uint8_t* boxes = sStg + qd * 8192;
         const int trow0 = ii.jt * 128 + qd * 32;
-        if (lane == 0) bulk_wait_read_all();  // dQ boxes of the last tile were read
-        __syncwarp();
-#pragma unroll 1
-        for (int which = 0; which < 2; ++which) {
-          if (D == 128 && which == 1) {  // the dK boxes must be read before dV reuses them
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-          }
-          const uint32_t col = which == 0 ? kColDK : kColDV;
-          const float mul = which == 0 ? p.scale : 1.f;
-          uint8_t* wb = (D == 64) ? boxes + which * 4096 : boxes;
+        uint8_t* wk = boxes;
+        uint8_t* wv = (D == 64) ? boxes + 4096 : boxes;
+        // packed row words (16 per 32 columns) -> 128-byte-swizzled 32 x 64 boxes
+        auto stage = [&](const uint32_t (&w)[D / 2], uint8_t* wb) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_off + col + 32 * c, x);
             uint8_t* rowp = wb + (c >> 1) * 4096 + lane * 128;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 u;
-              u.x = E::pack(__uint_as_float(x[8 * q]) * mul, __uint_as_float(x[8 * q + 1]) * mul);
-              u.y = E::pack(__uint_as_float(x[8 * q + 2]) * mul, __uint_as_float(x[8 * q + 3]) * mul);
-              u.z = E::pack(__uint_as_float(x[8 * q + 4]) * mul, __uint_as_float(x[8 * q + 5]) * mul);
-              u.w = E::pack(__uint_as_float(x[8 * q + 6]) * mul, __uint_as_float(x[8 * q + 7]) * mul);
-              *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + q) ^ (lane & 7)) << 4)) = u;
-            }
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(rowp + ((((c & 1) * 4 + q) ^ (lane & 7)) << 4)) =
+                  make_uint4(w[16 * c + 4 * q], w[16 * c + 4 * q + 1], w[16 * c + 4 * q + 2],
+                             w[16 * c + 4 * q + 3]);
           }
           fence_async_smem();
           __syncwarp();
+        };
+        auto store = [&](uint8_t* wb, const CUtensorMap* tm) {
           if (lane == 0) {
-            const CUtensorMap* tm = which == 0 ? &tm_dk : &tm_dv;
 #pragma unroll
             for (int bx = 0; bx < D / 64; ++bx) {
               if (p.layout == kLayoutBNSD)
@@ -904,7 +895,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bulk_commit_group();
           }
+        };
+        {
+          uint32_t kp[D / 2];
+#pragma unroll
+          for (int hf = 0; hf < D / 64; ++hf) {
+            uint32_t x[64];
+            tmem_ld64(tmem + lane_off + kColDK + 64 * hf, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              kp[32 * hf + j] = E::pack(__uint_as_float(x[2 * j]) * p.scale,
+                                        __uint_as_float(x[2 * j + 1]) * p.scale);
+          }
+          if (lane == 0) bulk_wait_read_all();  // dQ boxes of the last tile were read
+          __syncwarp();
+          stage(kp, wk);
         }
+        uint32_t vp[D / 2];
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          uint32_t x[64];
+          tmem_ld64(tmem + lane_off + kColDV + 64 * hf, x);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            vp[32 * hf + j] = E::pack(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kAccEmpty]);  // TMEM dK / dV free
+        store(wk, &tm_dk);
+        if (D == 128) {  // the dK boxes must be read before dV reuses them
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        }
+        stage(vp, wv);
+        store(wv, &tm_dv);
       } else {  // rare: kept compact (not unrolled)
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
@@ -947,10 +972,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kAccEmpty]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kAccEmpty]);
       ++itc;
       ++ic;
     }
