@@ -689,32 +689,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T of this thread's 64 columns, packed to the operand type (the
         // same rounded values feed the dV MMA and dS = P o (dP - D))
         uint32_t Ppk[32];
+        {
+          uint32_t x[64];  // both 32-column chunks in one TMEM load
+          tmem_ld64(tmem + lane_off + kColS + 64 * wg, x);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + kColS + 64 * wg + 32 * c, x);
-          const int s0 = 64 * wg + 32 * c;
+          for (int c = 0; c < 2; ++c) {
+            const int s0 = 64 * wg + 32 * c;
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 l4 = reinterpret_cast<const float4*>(lse2 + s0)[j4];
-            const float p0 = ex2_approx(fmaf(__uint_as_float(x[4 * j4]), p.scale_log2, -l4.x));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 1]), p.scale_log2, -l4.y));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 2]), p.scale_log2, -l4.z));
-            const float p3 = ex2_approx(fmaf(__uint_as_float(x[4 * j4 + 3]), p.scale_log2, -l4.w));
-            Ppk[16 * c + 2 * j4] = E::pack(p0, p1) & rmask;
-            Ppk[16 * c + 2 * j4 + 1] = E::pack(p2, p3) & rmask;
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 l4 = reinterpret_cast<const float4*>(lse2 + s0)[j4];
+              const int xi = 32 * c + 4 * j4;
+              const float p0 = ex2_approx(fmaf(__uint_as_float(x[xi]), p.scale_log2, -l4.x));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(x[xi + 1]), p.scale_log2, -l4.y));
+              const float p2 = ex2_approx(fmaf(__uint_as_float(x[xi + 2]), p.scale_log2, -l4.z));
+              const float p3 = ex2_approx(fmaf(__uint_as_float(x[xi + 3]), p.scale_log2, -l4.w));
+              Ppk[16 * c + 2 * j4] = E::pack(p0, p1) & rmask;
+              Ppk[16 * c + 2 * j4 + 1] = E::pack(p2, p3) & rmask;
+            }
+            if (wcut) {  // word j holds columns 2j (low half) and 2j + 1 (high half)
+              const uint32_t wm = c ? wm1 : wm0;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                Ppk[16 * c + j] &= ((wm >> (2 * j)) & 1u ? 0x0000FFFFu : 0u) |
+                                   ((wm >> (2 * j + 1)) & 1u ? 0xFFFF0000u : 0u);
+            }
           }
-          if (wcut) {  // word j holds columns 2j (low half) and 2j + 1 (high half)
-            const uint32_t wm = c ? wm1 : wm0;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              Ppk[16 * c + j] &= ((wm >> (2 * j)) & 1u ? 0x0000FFFFu : 0u) |
-                                 ((wm >> (2 * j + 1)) & 1u ? 0xFFFF0000u : 0u);
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = Ppk[16 * c + j];
-          tmem_st16(tmem + lane_off + kColS + 64 * wg + 16 * c, pk);
+          // packed P^T over the first half of this warpgroup's S columns
+          tmem_st32(tmem + lane_off + kColS + 64 * wg, Ppk);
         }
         tc_fence_before();
         __syncwarp();
@@ -722,36 +723,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait<kTagSoftmax>(&bars[kDpFull], n & 1, abort_flag)) { where = kErrWaitDP; break; }
         if (!mbar_wait<kTagSoftmax>(&bars[kDsFree], (n & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
+        {
+          uint32_t y[64];  // dP of both 32-column chunks in one TMEM load
+          tmem_ld64(tmem + lane_off + kColP + 64 * wg, y);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t y[32];
-          tmem_ld32(tmem + lane_off + kColP + 64 * wg + 32 * c, y);
-          const int s0 = 64 * wg + 32 * c;
-          uint32_t pk[16];
+          for (int c = 0; c < 2; ++c) {
+            const int s0 = 64 * wg + 32 * c;
+            uint32_t pk[16];
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 d4 = reinterpret_cast<const float4*>(dv + s0)[j4];
-            const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-            float ds[4];
-            const float2 p01 = E::unpack(Ppk[16 * c + 2 * j4]);
-            const float2 p23 = E::unpack(Ppk[16 * c + 2 * j4 + 1]);
-            ds[0] = p01.x * (__uint_as_float(y[4 * j4 + 0]) - dd[0]);
-            ds[1] = p01.y * (__uint_as_float(y[4 * j4 + 1]) - dd[1]);
-            ds[2] = p23.x * (__uint_as_float(y[4 * j4 + 2]) - dd[2]);
-            ds[3] = p23.y * (__uint_as_float(y[4 * j4 + 3]) - dd[3]);
-            pk[2 * j4] = E::pack(ds[0], ds[1]);
-            pk[2 * j4 + 1] = E::pack(ds[2], ds[3]);
-          }
-          // dS into shared memory: panel wg, row t, 16-byte chunk cc holds
-          // s = 64 wg + 8 cc .. +7, swizzled by t & 7 -- the MN-major A
-          // operand (M = query s) of the dQ MMA and the K-major A operand
-          // (M = key t) of the dK MMA.
-          uint8_t* rowp = sdS + wg * kPanel + t * 128;
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 d4 = reinterpret_cast<const float4*>(dv + s0)[j4];
+              const int yi = 32 * c + 4 * j4;
+              const float2 p01 = E::unpack(Ppk[16 * c + 2 * j4]);
+              const float2 p23 = E::unpack(Ppk[16 * c + 2 * j4 + 1]);
+              pk[2 * j4] = E::pack(p01.x * (__uint_as_float(y[yi]) - d4.x),
+                                   p01.y * (__uint_as_float(y[yi + 1]) - d4.y));
+              pk[2 * j4 + 1] = E::pack(p23.x * (__uint_as_float(y[yi + 2]) - d4.z),
+                                       p23.y * (__uint_as_float(y[yi + 3]) - d4.w));
+            }
+            // dS into shared memory: panel wg, row t, 16-byte chunk cc holds
+            // s = 64 wg + 8 cc .. +7, swizzled by t & 7 -- the MN-major A
+            // operand (M = query s) of the dQ MMA and the K-major A operand
+            // (M = key t) of the dK MMA.
+            uint8_t* rowp = sdS + wg * kPanel + t * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int cc = 4 * c + q;
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ (t & 7)) << 4)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) {
+              const int cc = 4 * c + q;
+              *reinterpret_cast<uint4*>(rowp + ((cc ^ (t & 7)) << 4)) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
           }
         }
         fence_async_smem();
