@@ -13,13 +13,18 @@
 //               with P read from TMEM) and TMEM owner; O += P(m-1) V(m-1) is
 //               issued after S(m), so the softmax of tile m overlaps both;
 //   warps 0-7   softmax, two warpgroups: TMEM lane s = query row s, warpgroup
-//               wg owns keys [64 wg, 64 wg + 64) of every tile and columns
-//               [wg D/2, wg D/2 + D/2) of O. The two halves of a row swap their
-//               partial maxima (and at the end their partial sums) through
-//               shared memory. The live keys of a tile (length, window,
-//               sub-block, token mask) are one bit word per 32 columns.
-// The rescale is lazy: O is only rescaled when a row max grows by more than
-// 8 (log2 units), so P stays below 2^8 and most tiles skip the TMEM round trip.
+//               wg owns keys [64 wg, 64 wg + 64) of every tile and runs its
+//               own online softmax over them (its own running max and sum)
+//               into its own O accumulator O_wg += P_wg V_wg (a K = 64
+//               product), so the two warpgroups never wait for each other
+//               within an item; at the end of an item they swap their maxima
+//               and sums through shared memory and each writes half of the
+//               output columns from O_0 and O_1 rescaled to the common max.
+//               The live keys of a tile (length, window, sub-block, token
+//               mask) are one bit word per 32 columns.
+// The rescale is lazy: O_wg is only rescaled when its row max grows by more
+// than 8 (log2 units), so P stays below 2^8 and most tiles skip the TMEM
+// round trip.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,14 +41,16 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPanel = 128 * 128;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;  // O_wg at kColO + wg * D
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kStages = 3;  // K/V ring depth
 
 enum Bar {
   kQFull = 0, kQEmpty,
   kKvFull0, kKvFull1, kKvFull2, kKvEmpty0, kKvEmpty1, kKvEmpty2, kKvAux0, kKvAux1, kKvAux2,
-  kSFull0, kSFull1, kPReady0, kPReady1, kPvDone0, kPvDone1,
+  kSFull0, kSFull1,
+  kPReady00, kPReady01, kPReady10, kPReady11,  // [S buffer][warpgroup]
+  kPvDone00, kPvDone01, kPvDone10, kPvDone11,  // [S buffer][warpgroup]
   kOFull, kOEmpty, kXch0, kXch1,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
   kDrain,
@@ -144,11 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kKvEmpty0 + i], 1 + kSoftmaxWarps);  // MMA + softmax warps
       mbar_init(&bars[kKvAux0 + i], 1);
     }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[kPReady00 + i], kSoftmaxWarps / 2);  // the warps of one warpgroup
+      mbar_init(&bars[kPvDone00 + i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kSFull0 + i], 1);
-      mbar_init(&bars[kPReady0 + i], kSoftmaxWarps);
-      mbar_init(&bars[kXch0 + i], 32 * kSoftmaxWarps);  // every softmax thread posts its max
-      mbar_init(&bars[kPvDone0 + i], 1);
+      mbar_init(&bars[kXch0 + i], 32 * kSoftmaxWarps);  // every softmax thread posts a value
       mbar_init(&bars[kItemFull0 + i], 1);
       mbar_init(&bars[kItemEmpty0 + i], 1 + kSoftmaxWarps);
     }
@@ -281,23 +290,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t m = 0;           // m: computed key tiles (S/P buffers, PV commits)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ);
-    // O += P(mm) V: A = P (TMEM, packed in S buffer mm & 1), B = V of stage vst
-    // (MN-major); `first` starts the item's accumulator. false = a wait gave up.
+    // O_wg += P_wg(mm) V_wg for both warpgroups, each as soon as its P is
+    // ready: A = P_wg (TMEM, packed over the warpgroup's S columns of buffer
+    // mm & 1), B = rows [64 wg, 64 wg + 64) of V of stage vst (MN-major);
+    // `first` starts the item's accumulators. false = a wait gave up.
     auto issue_pv = [&](uint32_t mm, int vst, bool first) -> bool {
-      if (!mbar_wait(&bars[kPReady0 + (mm & 1)], (mm >> 1) & 1, abort_flag)) { where = kErrWaitP; return false; }
-      if (first && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; return false; }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t colS = (mm & 1) ? kColS1 : kColS0;
-        const uint32_t aV = smem_u32(sV0 + vst * S::kTileBytes);
+      const uint32_t colS = (mm & 1) ? kColS1 : kColS0;
+      const uint32_t aV = smem_u32(sV0 + vst * S::kTileBytes);
+      for (int wg = 0; wg < 2; ++wg) {
+        if (!mbar_wait(&bars[kPReady00 + 2 * (mm & 1) + wg], (mm >> 1) & 1, abort_flag)) {
+          where = kErrWaitP;
+          return false;
+        }
+        if (first && wg == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
+          where = kErrWaitAcc;
+          return false;
+        }
+        tc_fence_after();
+        if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColO, tmem + colS + (k >> 2) * 64 + (k & 3) * 8,
-                 sdesc_sw128(aV + k * 2048, kPanel, 1024), kIdO, (first && k == 0) ? 0u : 1u);
-        tc_commit(&bars[kPvDone0 + (mm & 1)]);
-        tc_commit(&bars[kKvEmpty0 + vst]);
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + kColO + wg * D, tmem + colS + 64 * wg + 8 * k,
+                   sdesc_sw128(aV + (4 * wg + k) * 2048, kPanel, 1024), kIdO,
+                   (first && k == 0) ? 0u : 1u);
+          tc_commit(&bars[kPvDone00 + 2 * (mm & 1) + wg]);
+          if (wg == 1) tc_commit(&bars[kKvEmpty0 + vst]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
       return true;
     };
     while (true) {
@@ -320,9 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
           break;
         }
-        // S(m) into buffer m & 1 once the PV of tile m-2 has read its P
+        // S(m) into buffer m & 1 once both PV halves of tile m-2 have read its P
         const uint32_t sb = m & 1;
-        if (!mbar_wait(&bars[kPvDone0 + sb], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
+        if (!mbar_wait(&bars[kPvDone00 + 2 * sb], ((m >> 1) & 1) ^ 1, abort_flag) ||
+            !mbar_wait(&bars[kPvDone00 + 2 * sb + 1], ((m >> 1) & 1) ^ 1, abort_flag)) {
+          where = kErrWaitMisc;
+          break;
+        }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
         const uint32_t colS = sb ? kColS1 : kColS0;
@@ -415,96 +439,127 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b = bit_range(t_lo - 32 * c, t_hi - 32 * c);
           return amr != nullptr ? b & ~amr[c] : b;
         };
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + colS + 32 * c, x);
-          const uint32_t live = live_bits(c);
+        // this warpgroup's 64 keys of the tile, read once
+        uint32_t x[64];
+        tmem_ld64(tmem + lane_off + colS + 64 * wg, x);
+        const uint32_t live0 = live_bits(2 * wg), live1 = live_bits(2 * wg + 1);
+        // every key of the half takes part (the common case): no per-key tests
+        const bool all_live = (live0 & live1) == 0xFFFFFFFFu;
+        float mx;
+        {
+          // the max of the raw scores, scaled once (a negative scale turns it
+          // into the min)
+          const bool pos = p.scale_log2 >= 0.f;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (all_live) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            mx = fmaxf(mx, ((live >> k) & 1u) ? __uint_as_float(x[k]) * p.scale_log2 : -INFINITY);
+            for (int k = 0; k < 64; ++k)
+              m4[k & 3] = fmaxf(m4[k & 3], pos ? __uint_as_float(x[k]) : -__uint_as_float(x[k]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+              const uint32_t lv = k < 32 ? live0 : live1;
+              const float v = pos ? __uint_as_float(x[k]) : -__uint_as_float(x[k]);
+              m4[k & 3] = fmaxf(m4[k & 3], ((lv >> (k & 31)) & 1u) ? v : -INFINITY);
+            }
+          }
+          const float mr = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          mx = mr == -INFINITY ? -INFINITY : (pos ? mr : -mr) * p.scale_log2;
         }
-        {  // the row's maximum over both halves
-          float* xb = xch + (xs & 1) * 256;
-          xb[wg * 128 + s] = mx;
-          mbar_arrive(&bars[kXch0 + (xs & 1)]);
-          if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
-          mx = fmaxf(mx, xb[(wg ^ 1) * 128 + s]);
-          ++xs;
-        }
-        float m_use = m;
         const bool grow = mx > m + kRescaleThreshold || (m == -INFINITY && mx > -INFINITY);
-        if (__any_sync(0xffffffffu, grow) && j > 0) {
-          // rescale O rows whose max grew, after the previous PV has landed
-          const uint32_t pb = (m_step - 1) & 1;
-          if (!mbar_wait(&bars[kPvDone0 + pb], ((m_step - 1) >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
-          tc_fence_after();
-          const float alpha = grow ? ex2_approx(m - mx) : 1.f;
+        // O rows of this warpgroup whose max grows are rescaled by alpha (after
+        // the P of this tile is computed, so the scores are no longer live)
+        const float alpha = (grow && m != -INFINITY) ? ex2_approx(m - mx) : 1.f;
+        if (grow) {
+          l = (m == -INFINITY) ? 0.f : l * alpha;
+          m = mx;
+        }
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+        if (all_live) {
 #pragma unroll
-          for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+          for (int k = 0; k < 32; ++k) {
+            const float e0 = ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -m));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -m));
+            rs4[k & 3] += e0 + e1;
+            pk[k] = E::pack(e0, e1);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const uint32_t lv = k < 16 ? live0 : live1;
+            const int b0 = (2 * k) & 31;
+            const float e0 = ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -m));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -m));
+            const float p0 = ((lv >> b0) & 1u) ? e0 : 0.f;
+            const float p1 = ((lv >> (b0 + 1)) & 1u) ? e1 : 0.f;
+            rs4[k & 3] += p0 + p1;
+            pk[k] = E::pack(p0, p1);
+          }
+        }
+        const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        if (__any_sync(0xffffffffu, grow) && j > 0) {
+          // after this warpgroup's previous PV product has landed
+          const uint32_t pb = (m_step - 1) & 1;
+          if (!mbar_wait(&bars[kPvDone00 + 2 * pb + wg], ((m_step - 1) >> 1) & 1, abort_flag)) {
+            where = kErrWaitMisc;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
-            if (grow) {
+            tmem_ld32(tmem + lane_off + kColO + wg * D + 32 * c, o);
+            if (alpha != 1.f) {
 #pragma unroll
               for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
             }
-            uint32_t lo[16], hi[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) { lo[k] = o[k]; hi[k] = o[16 + k]; }
-            tmem_st16(tmem + lane_off + kColO + 32 * c, lo);
-            tmem_st16(tmem + lane_off + kColO + 32 * c + 16, hi);
+            tmem_st32(tmem + lane_off + kColO + wg * D + 32 * c, o);
           }
         }
-        if (grow) {
-          l = (m == -INFINITY) ? 0.f : l * ex2_approx(m - mx);
-          m_use = mx;
-          m = mx;
-        }
-        float rs = 0.f;
-#pragma unroll 1
-        for (int c = 2 * wg; c < 2 * wg + 2; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + colS + 32 * c, x);
-          const uint32_t live = live_bits(c);
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -m_use));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -m_use));
-            const float p0 = ((live >> (2 * k)) & 1u) ? e0 : 0.f;
-            const float p1 = ((live >> (2 * k + 1)) & 1u) ? e1 : 0.f;
-            rs += p0 + p1;
-            pk[k] = E::pack(p0, p1);
-          }
-          // P packed in place over this warpgroup's own S columns: keys
-          // 64 wg + 32 (c & 1) .. +31 at columns 64 wg + 16 (c & 1)
-          tmem_st16(tmem + lane_off + colS + 64 * wg + 16 * (c & 1), pk);
-        }
+        // P packed in place over the first half of this warpgroup's S columns
+        tmem_st32(tmem + lane_off + colS + 64 * wg, pk);
         l += rs;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kPReady0 + sb]);
+        if (lane == 0) mbar_arrive(&bars[kPReady00 + 2 * sb + wg]);
         ++j;
         ++n;
         ++m_step;
       }
       if (where) break;
-      // epilogue: Out = O / l, lse = (m + log2 l) * ln 2, l summed over both halves
+      // epilogue: the common max M = max(m_0, m_1) and sum L = sum_wg l_wg 2^(m_wg - M)
+      // (two exchanges through shared memory), Out = sum_wg O_wg 2^(m_wg - M) / L,
+      // lse = (M + log2 L) * ln 2; warpgroup wg writes columns [wg D/2, wg D/2 + D/2)
+      float m_o;
       {
-        float* lb = xch + (xs & 1) * 256;
-        lb[wg * 128 + s] = l;
+        float* xb = xch + (xs & 1) * 256;
+        xb[wg * 128 + s] = m;
         mbar_arrive(&bars[kXch0 + (xs & 1)]);
         if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
-        l += lb[(wg ^ 1) * 128 + s];
+        m_o = xb[(wg ^ 1) * 128 + s];
         ++xs;
       }
+      const float M = fmaxf(m, m_o);
+      const float a_own = M == -INFINITY ? 0.f : ex2_approx(m - M);
+      const float a_oth = M == -INFINITY ? 0.f : ex2_approx(m_o - M);
+      {
+        float* lb = xch + (xs & 1) * 256;
+        lb[wg * 128 + s] = l * a_own;
+        mbar_arrive(&bars[kXch0 + (xs & 1)]);
+        if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        l = l * a_own + lb[(wg ^ 1) * 128 + s];
+        ++xs;
+      }
+      m = M;
       if (!mbar_wait(&bars[kOFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const int srow = fi.it * 128 + s;
       const bool write_row = p.layout == kLayoutBNSD ? (srow < p.Sq) : (srow < Lq);
       const bool live = s_ok && l > 0.f;
       const float inv = live ? 1.f / l : 0.f;
+      // weights of O_0 and O_1 for this row
+      const float w0 = (wg == 0 ? a_own : a_oth) * inv, w1 = (wg == 0 ? a_oth : a_own) * inv;
       int64_t ooff;
       int64_t sd;
       if (p.layout == kLayoutBNSD) {
@@ -517,24 +572,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       T* out = static_cast<T*>(f.out) + ooff;
 #pragma unroll 1
       for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
-        uint32_t o[32];
-        if (j > 0) tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+        uint32_t o0[32], o1[32];
+        if (j > 0) {
+          tmem_ld32(tmem + lane_off + kColO + 32 * c, o0);
+          tmem_ld32(tmem + lane_off + kColO + D + 32 * c, o1);
+        }
         if (write_row) {
+          // combined row values, kept in o0
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            o0[k] = __float_as_uint((live && j > 0)
+                                        ? __uint_as_float(o0[k]) * w0 + __uint_as_float(o1[k]) * w1
+                                        : 0.f);
           if (f.out_vec) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 u;
-              const float* of = reinterpret_cast<const float*>(o);
-              u.x = E::pack(live ? of[8 * q] * inv : 0.f, live ? of[8 * q + 1] * inv : 0.f);
-              u.y = E::pack(live ? of[8 * q + 2] * inv : 0.f, live ? of[8 * q + 3] * inv : 0.f);
-              u.z = E::pack(live ? of[8 * q + 4] * inv : 0.f, live ? of[8 * q + 5] * inv : 0.f);
-              u.w = E::pack(live ? of[8 * q + 6] * inv : 0.f, live ? of[8 * q + 7] * inv : 0.f);
+              u.x = E::pack(__uint_as_float(o0[8 * q]), __uint_as_float(o0[8 * q + 1]));
+              u.y = E::pack(__uint_as_float(o0[8 * q + 2]), __uint_as_float(o0[8 * q + 3]));
+              u.z = E::pack(__uint_as_float(o0[8 * q + 4]), __uint_as_float(o0[8 * q + 5]));
+              u.w = E::pack(__uint_as_float(o0[8 * q + 6]), __uint_as_float(o0[8 * q + 7]));
               *reinterpret_cast<uint4*>(out + 32 * c + 8 * q) = u;
             }
           } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-              const uint32_t pk = E::pack(live ? __uint_as_float(o[k]) * inv : 0.f, 0.f);
+              const uint32_t pk = E::pack(__uint_as_float(o0[k]), 0.f);
               out[(32 * c + k) * sd] = *reinterpret_cast<const T*>(&pk);
             }
           }
