@@ -268,14 +268,17 @@ def time_backward(w, t, seq, dq, dk, dv, steps, warmup, local, world):
     return ms_step, ms_kern, clk, wall, ws, size
 
 
-def e2e_pipelined(w, t, seq, dq, dk, dv, n_steps):
+def e2e_pipelined(t, outs, size_of, launch, n_steps):
     """End-to-end time per step through the public API: every step copies
-    its inputs from pinned host memory to the device, runs both stages of
-    bsa_grad and reads dQ, dK and dV back into pinned host memory. Two device
-    buffer sets alternate, and the copies run on their own streams, so the
-    host-to-device copy of step i+1 and the read-back of step i-1 overlap the
-    compute of step i. Returns (ms per step, H2D bytes, D2H bytes per step),
-    timed with CUDA events from the first copy to the last read-back."""
+    its inputs (the device tensors of dict `t`) from pinned host memory to the
+    device, runs both stages of the library call (`size_of(inputs, outputs)`
+    gives the workspace size, `launch(inputs, outputs, ws, size, stream)` runs
+    the first and second stage) and reads the outputs `outs` back into pinned
+    host memory. Two device buffer sets alternate, and the copies run on their
+    own streams, so the host-to-device copy of step i+1 and the read-back of
+    step i-1 overlap the compute of step i. Returns (ms per step, H2D bytes,
+    D2H bytes per step), timed with CUDA events from the first copy to the
+    last read-back."""
     import torch
 
     import block_sparse_attention_attn_gb300 as bsa
@@ -286,11 +289,11 @@ def e2e_pipelined(w, t, seq, dq, dk, dv, n_steps):
     sets = []
     for k in range(2):
         ti = dict(t) if k == 0 else {k_: (None if x is None else x.clone()) for k_, x in t.items()}
-        outs = (dq, dk, dv) if k == 0 else tuple(torch.empty_like(x) for x in (dq, dk, dv))
-        size, _ = grad_executor(w, ti, seq, *outs)
-        ws = torch.empty(size, dtype=torch.uint8, device=dq.device)
-        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
-        sets.append((ti, outs, ws, size, h_out))
+        oi = tuple(outs) if k == 0 else tuple(torch.empty_like(x) for x in outs)
+        size = size_of(ti, oi)
+        ws = torch.empty(max(size, 256), dtype=torch.uint8, device=outs[0].device)
+        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in oi]
+        sets.append((ti, oi, ws, size, h_out))
     h2d = sum(x.numel() * x.element_size() for x in host.values())
     d2h = sum(x.numel() * x.element_size() for x in sets[0][4])
     ns = N_COPY_STREAMS
@@ -301,7 +304,7 @@ def e2e_pipelined(w, t, seq, dq, dk, dv, n_steps):
 
     def run(i):
         k = i % 2
-        ti, outs, ws, size, h_out = sets[k]
+        ti, oi, ws, size, h_out = sets[k]
         for j, st in enumerate(s_in):
             with torch.cuda.stream(st):
                 if i >= 2:
@@ -314,13 +317,12 @@ def e2e_pipelined(w, t, seq, dq, dk, dv, n_steps):
         if i >= 2:
             for e in ev_out[k]:
                 compute.wait_event(e)         # step i-2's outputs have been read back
-        _, ex = grad_executor(w, ti, seq, *outs)
-        bsa.bsa_grad(ws, size, ex, compute)
+        launch(ti, oi, ws, size, compute)
         ev_c[k].record(compute)
         for j, st in enumerate(s_out):
             with torch.cuda.stream(st):
                 st.wait_event(ev_c[k])
-                for hd, dd in list(zip(h_out, outs))[j::ns]:
+                for hd, dd in list(zip(h_out, oi))[j::ns]:
                     hd.copy_(dd, non_blocking=True)
                 ev_out[k][j].record(st)
 
@@ -338,7 +340,7 @@ def e2e_pipelined(w, t, seq, dq, dk, dv, n_steps):
         compute.wait_stream(st)
     end.record(compute)
     torch.cuda.synchronize()
-    for ti, outs, ws, size, h_out in sets:
+    for ti, oi, ws, size, h_out in sets:
         bsa.bsa_check_status(ws)
     return start.elapsed_time(end) / n_steps, h2d, d2h
 
@@ -401,7 +403,10 @@ def bench_ours(args, rank, world, local):
     # end to end through the public API: pinned host inputs -> H2D -> first and
     # second stage -> D2H of dq, dk, dv, every step (copies of one step overlap
     # the compute of the previous one)
-    e2e_ms, h2d, d2h = e2e_pipelined(w, t, seq, dq, dk, dv, max(3, min(n, 20)))
+    e2e_ms, h2d, d2h = e2e_pipelined(
+        t, (dq, dk, dv), lambda ti, o: grad_executor(w, ti, seq, *o)[0],
+        lambda ti, o, ws, size, st: bsa.bsa_grad(ws, size, grad_executor(w, ti, seq, *o)[1], st),
+        max(3, min(n, 20)))
     e2e_ms = max_over_ranks(e2e_ms, world)
 
     peaks, src = load_peaks()
@@ -510,25 +515,19 @@ def bench_forward(args, rank, world, local):
     ms_step = max_over_ranks(float(np.mean([e[0].elapsed_time(e[3]) for e in ev])), world)
     ms_kern = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
     # end to end: pinned host Q, K, V (and masks) -> H2D -> both stages -> D2H of Out, lse
-    host = {k_: t[k_].cpu().pin_memory() for k_ in ("query", "key", "value", "block_sparse_mask",
-                                                   "atten_mask") if t[k_] is not None}
-    h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (out, lse)]
-    h2d = sum(x.numel() * x.element_size() for x in host.values())
-    d2h = sum(x.numel() * x.element_size() for x in h_out)
-    times = []
-    for i in range(max(3, min(n, 20)) + 1):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for k_, x in host.items():
-            t[k_].copy_(x, non_blocking=True)
-        bsa.bsa_fwd(ws, size, fwd_executor()[1], stream)
-        for hd, dd in zip(h_out, (out, lse)):
-            hd.copy_(dd, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if i > 0:
-            times.append(a.elapsed_time(b))
-    e2e_ms = max_over_ranks(float(np.mean(times)), world)
+    fin = {k_: t[k_] for k_ in ("query", "key", "value", "block_sparse_mask", "atten_mask")}
+
+    def fwd_size(ti, o):
+        return bsa.bsa_fwd_workspace_size(
+            ti["query"], ti["key"], ti["value"], ti["block_sparse_mask"], [w.bx, w.by],
+            seq["actual_seq_lengths"], seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2,
+            w.scale, w.pre_tokens, w.next_tokens, o[0], o[1], ti["atten_mask"])
+
+    e2e_ms, h2d, d2h = e2e_pipelined(
+        fin, (out, lse), lambda ti, o: fwd_size(ti, o)[0],
+        lambda ti, o, ws, size, st: bsa.bsa_fwd(ws, size, fwd_size(ti, o)[1], st),
+        max(3, min(n, 20)))
+    e2e_ms = max_over_ranks(e2e_ms, world)
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
     achieved = flops / (ms_kern * 1e-3) / 1e12
@@ -549,7 +548,9 @@ def bench_forward(args, rank, world, local):
                      if src == "measured" else "fallback 1.9 PFLOP/s bf16"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "schedule": "two device buffer sets; the H2D copy of step i+1 and the D2H "
+                            "read-back of step i-1 run on copy streams during step i"},
         "gpu_launches": (3 if w.atten_mask is not None else 2) * n,  # info upload, [mask packing,] forward
         "clocks": clk,
     }

@@ -505,41 +505,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P of this warpgroup's 64 keys, rounded to the operand type as in the
         // dV/dK kernel, kept packed in registers
         uint32_t Ppk[32];
+        {
+          uint32_t x[64];  // both 32-column chunks in one TMEM load
+          tmem_ld64(tmem + lane_off + sb + 64 * wg, x);
+          if ((live0 & live1) == 0xFFFFFFFFu) {  // every key takes part: no per-key tests
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t x[32];
-          tmem_ld32(tmem + lane_off + sb + 64 * wg + 32 * c, x);
-          const uint32_t live = c ? live1 : live0;
+            for (int k = 0; k < 32; ++k)
+              Ppk[k] = E::pack(ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -lse2)),
+                               ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -lse2)));
+          } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float pv[2];
+            for (int k = 0; k < 32; ++k) {
+              const uint32_t live = k < 16 ? live0 : live1;
+              float pv[2];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const bool on = (live >> (2 * k + u)) & 1u;
-              pv[u] = on ? ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)) : 0.f;
+              for (int u = 0; u < 2; ++u) {
+                const bool on = (live >> ((2 * k + u) & 31)) & 1u;
+                pv[u] = on ? ex2_approx(fmaf(__uint_as_float(x[2 * k + u]), p.scale_log2, -lse2)) : 0.f;
+              }
+              Ppk[k] = E::pack(pv[0], pv[1]);
             }
-            Ppk[16 * c + k] = E::pack(pv[0], pv[1]);
           }
         }
         if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
         tc_fence_after();
-        uint32_t y[2][32];
-        tmem_ld32(tmem + lane_off + kColP + 64 * wg, y[0]);
-        tmem_ld32(tmem + lane_off + kColP + 64 * wg + 32, y[1]);
+        uint32_t y[64];
+        tmem_ld64(tmem + lane_off + kColP + 64 * wg, y);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kDpFree]);  // the MMA may write dP(m+1)
         // dS = P o (dP - D), packed in place over this warpgroup's S columns
+        {
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 pp = E::unpack(Ppk[16 * c + k]);
-            pk[k] = E::pack(pp.x * (__uint_as_float(y[c][2 * k]) - dsum),
-                            pp.y * (__uint_as_float(y[c][2 * k + 1]) - dsum));
+          for (int k = 0; k < 32; ++k) {
+            const float2 pp = E::unpack(Ppk[k]);
+            pk[k] = E::pack(pp.x * (__uint_as_float(y[2 * k]) - dsum),
+                            pp.y * (__uint_as_float(y[2 * k + 1]) - dsum));
           }
-          tmem_st16(tmem + lane_off + sb + 96 * wg + 16 * c, pk);
+          tmem_st32(tmem + lane_off + sb + 96 * wg, pk);
         }
         tc_fence_before();
         __syncwarp();
