@@ -47,6 +47,8 @@ def parse():
                     help="skip the other configurations timed after the default w1 line")
     ap.add_argument("--config-steps", type=int, default=100,
                     help="timed steps of each other configuration")
+    ap.add_argument("--key-block64", action="store_true",
+                    help="blockShape [bx, 64] workloads: one query-major step per 64-key block")
     ap.add_argument("--deterministic", action="store_true",
                     help="time the deterministic dQ mode (separate query-tile pass)")
     ap.add_argument("--forward", action="store_true",
@@ -192,6 +194,7 @@ def make_inputs(w, dev):
 
 
 DETERMINISTIC = False  # set from --deterministic
+KEY_BLOCK64 = False    # set from --key-block64
 
 
 def grad_executor(w, t, seq, dq, dk, dv):
@@ -204,6 +207,8 @@ def grad_executor(w, t, seq, dq, dk, dv):
         dq=dq, dk=dk, dv=dv)
     if DETERMINISTIC:
         ex.set_deterministic(True)
+    if KEY_BLOCK64:
+        ex.set_key_block64(True)
     return size, ex
 
 
@@ -424,6 +429,7 @@ def bench_ours(args, rank, world, local):
                    "gflop_per_step": round(flops / 1e9, 2), "parallelism": f"replicas x{world}",
                    "l2": "flushed (512 MB write) before every timed step",
                    "dq_mode": "deterministic (query-tile pass)" if DETERMINISTIC else "fp32 reduce-add",
+                   "key_block64": KEY_BLOCK64 and w.by == 64 and w.D == 128 and not w.token_masked(),
                    "window": ([w.pre_tokens, w.next_tokens] if w.windowed() else None),
                    "atten_mask": (w.atten_mask_desc or None)},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
@@ -654,8 +660,9 @@ def main():
             return
         print(json.dumps(bench_reference(args, rank, world)), flush=True)
         return
-    global DETERMINISTIC
+    global DETERMINISTIC, KEY_BLOCK64
     DETERMINISTIC = args.deterministic
+    KEY_BLOCK64 = args.key_block64
     rank, world, local = dist_setup(args.gpus)
     line = (bench_forward if args.forward else bench_ours)(args, rank, world, local)
     if rank == 0:

@@ -67,6 +67,7 @@ def load_library():
     lib.bsa_executor_set_timing_events.argtypes = [vp, vp, vp]
     lib.bsa_executor_set_wait_test.argtypes = [vp, ctypes.c_int32]
     lib.bsa_executor_set_deterministic.argtypes = [vp, ctypes.c_int32]
+    lib.bsa_executor_set_key_block64.argtypes = [vp, ctypes.c_int32]
     lib.bsa_mask_compact_workspace_size.argtypes = [T, i64, i64, P(u64)]
     lib.bsa_mask_compact.argtypes = [T, i64, i64, P(i64), i64, P(i64), i64, vp, vp, vp, vp, vp,
                                      u64, vp]
@@ -79,6 +80,7 @@ def load_library():
     for name in ("bsa_grad_workspace_size", "bsa_grad", "bsa_fwd_workspace_size", "bsa_fwd",
                  "bsa_executor_destroy", "bsa_executor_set_timing_events",
                  "bsa_executor_set_wait_test", "bsa_executor_set_deterministic",
+                 "bsa_executor_set_key_block64",
                  "bsa_mask_compact_workspace_size", "bsa_mask_compact",
                  "bsa_mask_compact_noalloc", "bsa_check_status", "bsa_status_async"):
         getattr(lib, name).restype = ctypes.c_int
@@ -152,6 +154,12 @@ class Executor:
         """dQ from a separate query-tile pass: bitwise identical results on
         every run (backward executors only)."""
         _check(load_library().bsa_executor_set_deterministic(self.handle, 1 if enable else 0))
+
+    def set_key_block64(self, enable: bool = True):
+        """blockShape [bx, 64], D = 128, no window or token mask: one
+        query-major step per selected 64-key block (backward executors only;
+        ignored otherwise)."""
+        _check(load_library().bsa_executor_set_key_block64(self.handle, 1 if enable else 0))
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:

@@ -23,8 +23,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libbsa.so")
 
-SOURCES = ["bsa_api.cpp", "bsa_kernels.cu", "bsa_bwd.cu", "bsa_bwd_dq.cu", "bsa_fwd.cu",
-           "bsa_noalloc.cu"]
+SOURCES = ["bsa_api.cpp", "bsa_kernels.cu", "bsa_bwd.cu", "bsa_bwd_k64.cu", "bsa_bwd_dq.cu",
+           "bsa_fwd.cu", "bsa_noalloc.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -97,10 +97,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D view (d, rows, heads) of a 16-bit tensor: box 64 x 128 x 1 (BNSD) or
-// (d, heads, tokens) with box 64 x 1 x 128 (TND); 128-byte swizzle.
+// 3-D view (d, rows, heads) of a 16-bit tensor: box 64 x box_rows x 1 (BNSD)
+// or (d, heads, tokens) with box 64 x 1 x box_rows (TND); 128-byte swizzle.
 bool encode_map(CUtensorMap* m, const void* base, int dtype, int layout, int64_t D, int64_t rows,
-                int64_t heads) {
+                int64_t heads, int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   const CUtensorMapDataType dt =
@@ -112,11 +112,11 @@ bool encode_map(CUtensorMap* m, const void* base, int dtype, int layout, int64_t
   if (layout == kLayoutBNSD) {  // rows = S per head, heads = B*N
     dims[0] = D; dims[1] = rows; dims[2] = heads;
     strides[0] = D * 2; strides[1] = rows * D * 2;
-    box[0] = 64; box[1] = 128; box[2] = 1;
+    box[0] = 64; box[1] = (cuuint32_t)box_rows; box[2] = 1;
   } else {  // rows = T tokens, heads = N
     dims[0] = D; dims[1] = heads; dims[2] = rows;
     strides[0] = D * 2; strides[1] = heads * D * 2;
-    box[0] = 64; box[1] = 1; box[2] = 128;
+    box[0] = 64; box[1] = 1; box[2] = (cuuint32_t)box_rows;
   }
   CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -173,9 +173,10 @@ bool encode_out_map(CUtensorMap* m, const bsa_tensor* t, int layout) {
   return r == CUDA_SUCCESS;
 }
 
-// One non-blocking side stream per device (created once, never destroyed):
-// the backward's preprocess runs there, between events, while the mask
-// compaction and the planner run on the caller's stream.
+// One non-blocking side stream per device (created once, never destroyed),
+// at the greatest priority: the backward's mask compaction and planner (small,
+// latency-bound launches) run there, between events, and take SMs ahead of
+// the bandwidth-bound preprocess that fills the GPU from the caller's stream.
 constexpr int kMaxSideDevices = 64;
 cudaStream_t side_stream(int dev) {
   static cudaStream_t streams[kMaxSideDevices] = {};
@@ -183,8 +184,15 @@ cudaStream_t side_stream(int dev) {
   if (dev < 0 || dev >= kMaxSideDevices) return nullptr;
   std::call_once(once[dev], [dev] {
     cudaStream_t s = nullptr;
-    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess) streams[dev] = s;
-    else cudaGetLastError();
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) {
+      cudaGetLastError();
+      greatest = 0;
+    }
+    if (cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest) == cudaSuccess)
+      streams[dev] = s;
+    else
+      cudaGetLastError();
   });
   return streams[dev];
 }
@@ -375,7 +383,8 @@ struct bsa_executor {
   uint64_t off_am_row = 0, off_am_col = 0, off_am_sub = 0;
   uint64_t ws_size = 0;
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;      // owned: side-stream preprocess
+  int k64 = 0;  // 64-key-block backward requested (bsa_executor_set_key_block64)
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;      // owned: side-stream compaction
   ~bsa_executor() {
     if (ev_fork) cudaEventDestroy(ev_fork);
     if (ev_join) cudaEventDestroy(ev_join);
@@ -564,6 +573,13 @@ bsa_status bsa_executor_set_deterministic(bsa_executor* executor, int32_t enable
   if (executor == nullptr) return fail(BSA_ERR_PARAM_NULLPTR, "executor is NULL");
   if (executor->kind != 1) return fail(BSA_ERR_PARAM_INVALID, "not a backward executor");
   executor->plan.det = enable ? 1 : 0;
+  return ok();
+}
+
+bsa_status bsa_executor_set_key_block64(bsa_executor* executor, int32_t enable) {
+  if (executor == nullptr) return fail(BSA_ERR_PARAM_NULLPTR, "executor is NULL");
+  if (executor->kind != 1) return fail(BSA_ERR_PARAM_INVALID, "not a backward executor");
+  executor->k64 = enable ? 1 : 0;
   return ok();
 }
 
@@ -758,6 +774,10 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
     return fail(BSA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed");
   maps.dk = ex->map_dk;
   maps.dv = ex->map_dv;
+  const bool k64 = ex->k64 && bwd_k64_applies(p);
+  if (k64 && (!encode_map(&maps.k64, ex->k, g.dtype, g.layout, g.D, rows_k, heads_k, 64) ||
+              !encode_map(&maps.v64, ex->v, g.dtype, g.layout, g.D, rows_k, heads_k, 64)))
+    return fail(BSA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed");
 
   cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
                                 reinterpret_cast<int*>(ws + ex->off_info), st);
@@ -776,37 +796,35 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.win = p.win; ca.win_pre = p.win_pre; ca.win_next = p.win_next;
   ca.am_sub = p.am ? p.am_sub : nullptr; ca.am_sk = p.am_sk;
   ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
-  // The preprocess (bandwidth-bound) runs on a side stream while the mask
-  // compaction and the planner (latency-bound, one block) run on `st`.
+  // The mask compaction and the planner (latency-bound, one block) run on a
+  // high-priority side stream while the preprocess (bandwidth-bound) runs on
+  // `st`.
   cudaStream_t side = nullptr;
   {
     int dev = 0;
     if (ex->ev_fork && cudaGetDevice(&dev) == cudaSuccess) side = side_stream(dev);
     cudaGetLastError();
   }
-  const char* what = "preprocess";
-  if (side) {
-    if ((e = cudaEventRecord(ex->ev_fork, st)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(side, ex->ev_fork, 0)) != cudaSuccess ||
-        (e = launch_preprocess(p, side)) != cudaSuccess ||
-        (e = cudaEventRecord(ex->ev_join, side)) != cudaSuccess)
-      goto launch_fail;
-  }
-  what = "column count";
-  if ((e = launch_columns(ca, 0, st)) != cudaSuccess) goto launch_fail;
-  what = "planner";
-  if ((e = launch_plan(p, st)) != cudaSuccess) goto launch_fail;
-  what = "column fill";
-  if ((e = launch_columns(ca, 1, st)) != cudaSuccess) goto launch_fail;
-  what = "preprocess";
-  if (side) {
-    if ((e = cudaStreamWaitEvent(st, ex->ev_join, 0)) != cudaSuccess) goto launch_fail;
-  } else if ((e = launch_preprocess(p, st)) != cudaSuccess) {
+  cudaStream_t cs = side ? side : st;  // stream of the compaction chain
+  const char* what = "fork";
+  if (side && ((e = cudaEventRecord(ex->ev_fork, st)) != cudaSuccess ||
+               (e = cudaStreamWaitEvent(side, ex->ev_fork, 0)) != cudaSuccess))
     goto launch_fail;
-  }
+  what = "column count";
+  if ((e = launch_columns(ca, 0, cs)) != cudaSuccess) goto launch_fail;
+  what = "planner";
+  if ((e = launch_plan(p, cs)) != cudaSuccess) goto launch_fail;
+  what = "column fill";
+  if ((e = launch_columns(ca, 1, cs)) != cudaSuccess) goto launch_fail;
+  if (side && (e = cudaEventRecord(ex->ev_join, side)) != cudaSuccess) goto launch_fail;
+  what = "preprocess";
+  if ((e = launch_preprocess(p, st)) != cudaSuccess) goto launch_fail;
+  what = "join";
+  if (side && (e = cudaStreamWaitEvent(st, ex->ev_join, 0)) != cudaSuccess) goto launch_fail;
   what = "backward";
   if (ex->ev_before && (e = cudaEventRecord(ex->ev_before, st)) != cudaSuccess) goto launch_fail;
-  if ((e = launch_bwd(p, maps, st)) != cudaSuccess) goto launch_fail;
+  if ((e = k64 ? launch_bwd_k64(p, maps, st) : launch_bwd(p, maps, st)) != cudaSuccess)
+    goto launch_fail;
   if (p.det) {
     what = "deterministic dQ";
     if ((e = launch_bwd_dq(p, maps, st)) != cudaSuccess) goto launch_fail;

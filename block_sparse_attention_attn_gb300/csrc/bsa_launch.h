@@ -70,8 +70,13 @@ struct BwdMaps {
   CUtensorMap q, k, v, dout;
   CUtensorMap dqacc;  // fp32 [N1*Rq rows, D], box 32 x 32, 128-byte swizzle (reduce-add)
   CUtensorMap dk, dv; // outputs, box 64 x 32 rows, 128-byte swizzle: BNSD (d, s, n, b), TND (d, n, t)
+  CUtensorMap k64, v64; // K, V with 64-row boxes (the 64-key-block kernel only)
 };
 cudaError_t launch_bwd(const Plan& p, const BwdMaps& m, cudaStream_t st);
+// Backward for key blocks of 64 tokens with D = 128 and no element masks
+// (query-major tiles, one pass per key block of a 128-key tile).
+bool bwd_k64_applies(const Plan& p);
+cudaError_t launch_bwd_k64(const Plan& p, const BwdMaps& m, cudaStream_t st);
 // Deterministic dQ pass (query-tile stationary), used when p.det is set.
 cudaError_t launch_bwd_dq(const Plan& p, const BwdMaps& m, cudaStream_t st);
 size_t bwd_smem_bytes(int D);

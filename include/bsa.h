@@ -183,6 +183,22 @@ bsa_status bsa_executor_set_wait_test(bsa_executor* executor, int32_t enable);
  * aclnnBlockSparseAttentionGrad page, section 约束说明. */
 bsa_status bsa_executor_set_deterministic(bsa_executor* executor, int32_t enable);
 
+/* Key blocks of 64 tokens (backward executors only). With enable != 0, a run
+ * whose blockShape is [bx, 64] with head dim 128 and neither sliding window nor
+ * token mask computes the five products of every selected 64-key block as one
+ * query-major step (S = Q K_h^T with N = 64 keys; dV_h^T, dK_h^T accumulated
+ * with the head dimension on the tensor-memory lanes), one pass per key block
+ * of a 128-key tile, so an unselected half of a tile is never loaded or
+ * multiplied: the tensor-core work equals the algorithmic work (blockShape row
+ * of the aclnnBlockSparseAttentionGrad parameter table: bx and by need not be
+ * equal). Off by default: 64-wide products run at a lower rate per FLOP on
+ * the tensor cores and every block sends its own dQ partial, so on GB300 the
+ * default path (128 x 128 tiles with the unselected half masked) is faster
+ * even when most tiles hold only one selected block. Ignored when the run does
+ * not meet the conditions above; results equal the default path's up to
+ * rounding order. */
+bsa_status bsa_executor_set_key_block64(bsa_executor* executor, int32_t enable);
+
 /* Frees an executor that was never passed to a run call. NULL is a no-op. */
 bsa_status bsa_executor_destroy(bsa_executor* executor);
 

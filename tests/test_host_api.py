@@ -150,6 +150,10 @@ def test_deterministic_switch_needs_a_backward_executor(lib):
     assert lib.bsa_executor_set_deterministic(None, 1) == B.BSA_ERR_PARAM_NULLPTR
 
 
+def test_key_block64_switch_needs_a_backward_executor(lib):
+    assert lib.bsa_executor_set_key_block64(None, 1) == B.BSA_ERR_PARAM_NULLPTR
+
+
 def _fwd_status(**kw):
     try:
         bsa.bsa_fwd_workspace_size(**kw)
