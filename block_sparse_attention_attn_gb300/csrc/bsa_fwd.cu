@@ -6,12 +6,17 @@
 // running row max m and sum l are updated per key tile and the partial PV
 // product is rescaled by exp(m_old - m_new) when the max grows.
 //
-// One persistent CTA per SM, 320 threads:
+// One persistent CTA per SM, 352 threads:
 //   warp 8      producer: scans the mask row(s) of its query tile for selected
 //               key tiles and streams K/V tiles through a 3-stage TMA ring;
-//   warp 9      MMA issuer (S = Q K^T into one of two TMEM buffers, O += P V
-//               with P read from TMEM) and TMEM owner; O += P(m-1) V(m-1) is
-//               issued after S(m), so the softmax of tile m overlaps both;
+//   warp 9      MMA issuer of S = Q K^T (into one of two TMEM buffers, as soon
+//               as the P of tile m-2 in that buffer has been read) and TMEM
+//               owner;
+//   warp 10     MMA issuer of O_wg += P_wg V_wg (P read from TMEM), per
+//               warpgroup as soon as its P is ready. Two issuers, because an
+//               issuing thread blocks while the tensor pipe's queue is full:
+//               with one, the PV product of tile m-1 waited behind the issue
+//               of S(m), and so did S(m+1), which needs that PV's S buffer;
 //   warps 0-7   softmax, two warpgroups: TMEM lane s = query row s, warpgroup
 //               wg owns keys [64 wg, 64 wg + 64) of every tile and runs its
 //               own online softmax over them (its own running max and sum)
@@ -36,10 +41,11 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;   // S = Q K^T; TMEM owner
+constexpr int kPvWarp = 10;   // O += P V
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;  // O_wg at kColO + wg * D
 constexpr float kRescaleThreshold = 8.f;
@@ -53,7 +59,7 @@ enum Bar {
   kPvDone00, kPvDone01, kPvDone10, kPvDone11,  // [S buffer][warpgroup]
   kOFull, kOEmpty, kXch0, kXch1,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
-  kDrain,
+  kDrain, kDrain2,
   kNumBars
 };
 
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kQEmpty], 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars[kKvFull0 + i], 1);
-      mbar_init(&bars[kKvEmpty0 + i], 1 + kSoftmaxWarps);  // MMA + softmax warps
+      mbar_init(&bars[kKvEmpty0 + i], 2 + kSoftmaxWarps);  // both MMA warps + softmax warps
       mbar_init(&bars[kKvAux0 + i], 1);
     }
     for (int i = 0; i < 4; ++i) {
@@ -159,11 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kSFull0 + i], 1);
       mbar_init(&bars[kXch0 + i], 32 * kSoftmaxWarps);  // every softmax thread posts a value
       mbar_init(&bars[kItemFull0 + i], 1);
-      mbar_init(&bars[kItemEmpty0 + i], 1 + kSoftmaxWarps);
+      mbar_init(&bars[kItemEmpty0 + i], 2 + kSoftmaxWarps);
     }
     mbar_init(&bars[kOFull], 1);
     mbar_init(&bars[kOEmpty], kSoftmaxWarps);
     mbar_init(&bars[kDrain], 1);
+    mbar_init(&bars[kDrain2], 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
@@ -285,41 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------ MMA issuer: S
     uint32_t n = 0, itc = 0;  // n: K/V stages (end markers included)
-    uint32_t m = 0;           // m: computed key tiles (S/P buffers, PV commits)
+    uint32_t m = 0;           // m: computed key tiles (S/P buffers)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ);
-    // O_wg += P_wg(mm) V_wg for both warpgroups, each as soon as its P is
-    // ready: A = P_wg (TMEM, packed over the warpgroup's S columns of buffer
-    // mm & 1), B = rows [64 wg, 64 wg + 64) of V of stage vst (MN-major);
-    // `first` starts the item's accumulators. false = a wait gave up.
-    auto issue_pv = [&](uint32_t mm, int vst, bool first) -> bool {
-      const uint32_t colS = (mm & 1) ? kColS1 : kColS0;
-      const uint32_t aV = smem_u32(sV0 + vst * S::kTileBytes);
-      for (int wg = 0; wg < 2; ++wg) {
-        if (!mbar_wait(&bars[kPReady00 + 2 * (mm & 1) + wg], (mm >> 1) & 1, abort_flag)) {
-          where = kErrWaitP;
-          return false;
-        }
-        if (first && wg == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
-          where = kErrWaitAcc;
-          return false;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kColO + wg * D, tmem + colS + 64 * wg + 8 * k,
-                   sdesc_sw128(aV + (4 * wg + k) * 2048, kPanel, 1024), kIdO,
-                   (first && k == 0) ? 0u : 1u);
-          tc_commit(&bars[kPvDone00 + 2 * (mm & 1) + wg]);
-          if (wg == 1) tc_commit(&bars[kKvEmpty0 + vst]);
-        }
-        __syncwarp();
-      }
-      return true;
-    };
     while (true) {
       const int slot = itc & 1;
       if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
@@ -329,13 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx < 0) break;
       if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
       tc_fence_after();
-      int j = 0, st_prev = 0;
       while (true) {
         const int st = n % kStages;
         if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
+        __syncwarp();
         if (mt < 0) {
-          __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
           ++n;
           break;
@@ -357,29 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + colS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS, k > 0);
           }
           tc_commit(&bars[kSFull0 + sb]);
+          tc_commit(&bars[kKvEmpty0 + st]);  // K of the stage read
         }
         __syncwarp();
-        // O += P(m-1) V(m-1) after S(m) is queued, so the softmax of tile m
-        // overlaps with the tensor cores
-        if (j > 0 && !issue_pv(m - 1, st_prev, j == 1)) break;
-        st_prev = st;
-        ++j;
         ++n;
         ++m;
       }
       if (where) break;
-      if (j > 0) {
-        if (!issue_pv(m - 1, st_prev, j == 1)) break;
-      } else if (!mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
-        // every item waits for the previous epilogue exactly once (a parity
-        // wait cannot tell phase c from phase c-2, so no item may skip it)
-        where = kErrWaitAcc;
-        break;
-      }
-      if (lane == 0) {
-        tc_commit(&bars[kOFull]);
-        tc_commit(&bars[kQEmpty]);
-      }
+      if (lane == 0) tc_commit(&bars[kQEmpty]);  // the item's last S has read Q
       __syncwarp();
       ++itc;
     }
@@ -388,6 +349,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) tc_commit(&bars[kDrain]);
       __syncwarp();
       mbar_wait_drain(&bars[kDrain], 0);
+    }
+  } else if (warp == kPvWarp) {
+    // --------------------------------------------------- MMA issuer: P V
+    uint32_t n = 0, itc = 0, m = 0;  // as in the S issuer
+    int where = 0;
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int idx = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      if (idx < 0) break;
+      int j = 0;
+      while (true) {
+        const int st = n % kStages;
+        if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int mt = meta[st];
+        __syncwarp();
+        if (mt < 0) {
+          if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
+          ++n;
+          break;
+        }
+        // O_wg += P_wg(m) V_wg for both warpgroups, each as soon as its P is
+        // ready: A = P_wg (TMEM, packed over the warpgroup's S columns of
+        // buffer m & 1), B = rows [64 wg, 64 wg + 64) of V of stage st
+        // (MN-major); the item's first product starts the accumulators
+        const uint32_t colS = (m & 1) ? kColS1 : kColS0;
+        const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
+        for (int wg = 0; wg < 2 && !where; ++wg) {
+          if (!mbar_wait(&bars[kPReady00 + 2 * (m & 1) + wg], (m >> 1) & 1, abort_flag)) {
+            where = kErrWaitP;
+            break;
+          }
+          if (j == 0 && wg == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
+            where = kErrWaitAcc;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ts(tmem + kColO + wg * D, tmem + colS + 64 * wg + 8 * k,
+                     sdesc_sw128(aV + (4 * wg + k) * 2048, kPanel, 1024), kIdO,
+                     (j == 0 && k == 0) ? 0u : 1u);
+            tc_commit(&bars[kPvDone00 + 2 * (m & 1) + wg]);
+            if (wg == 1) tc_commit(&bars[kKvEmpty0 + st]);  // V of the stage read
+          }
+          __syncwarp();
+        }
+        if (where) break;
+        ++j;
+        ++n;
+        ++m;
+      }
+      if (where) break;
+      // every item waits for the previous epilogue exactly once (a parity
+      // wait cannot tell phase c from phase c-2, so no item may skip it)
+      if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
+        where = kErrWaitAcc;
+        break;
+      }
+      if (lane == 0) tc_commit(&bars[kOFull]);
+      __syncwarp();
+      ++itc;
+    }
+    if (where) record_error(p.header, where);
+    if (*abort_flag) {
+      if (lane == 0) tc_commit(&bars[kDrain2]);
+      __syncwarp();
+      mbar_wait_drain(&bars[kDrain2], 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
