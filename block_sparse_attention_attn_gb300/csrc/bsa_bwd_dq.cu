@@ -8,16 +8,19 @@
 // other CTAs finish: no fp32 reduce-adds, the same bits on every run. The
 // key-tile-stationary kernel then computes dK and dV only.
 //
-// One persistent CTA per SM, 320 threads:
+// One persistent CTA per SM, 352 threads:
 //   warp 8      producer: Q and dO of the query tile, then K and V tiles of
 //               the selected key tiles (found by scanning the mask row)
 //               through TMA rings of 3 (K: read by S and the later dQ) and
 //               2 (V: read by dP only) stages;
-//   warp 9      MMA issuer and TMEM owner. Per key tile m it issues S(m) =
-//               Q K^T into one of two S buffers, dP(m) = dO V^T once the
-//               softmax warps have read dP(m-1), then dQ += dS(m-1) K(m-1)
-//               (dS read from TMEM): the tensor cores compute tile m while
-//               the softmax warps work on tile m-1;
+//   warp 9      MMA issuer of S(m) = Q K^T (into one of two S buffers) and
+//               dP(m) = dO V^T (once the softmax warps have read dP(m-1)),
+//               and TMEM owner;
+//   warp 10     MMA issuer of dQ += dS(m) K(m) (dS read from TMEM) as soon as
+//               the softmax warps have written dS(m): the tensor cores compute
+//               tile m+1 while the softmax warps work on tile m, and neither
+//               issuer waits behind the other's issue (an issuing thread
+//               blocks while the tensor pipe's queue is full);
 //   warps 0-7   two warpgroups, TMEM lane s = query row s, warpgroup wg owns
 //               keys [64 wg, 64 wg + 64): P and dS (lse and D are per-thread
 //               values here), then the dQ epilogue (columns split by wg).
@@ -36,10 +39,11 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;   // S, dP; TMEM owner
+constexpr int kDqWarp = 10;   // dQ
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColP = 256, kColQ = 384;
 constexpr int kKStages = 3, kVStages = 2;
@@ -53,7 +57,7 @@ enum Bar {
   kVFull0, kVFull1, kVEmpty0, kVEmpty1, kVAux0, kVAux1,
   kSFull0, kSFull1, kSFree0, kSFree1, kDpFull, kDpFree, kDsReady, kDqFull, kDqEmpty,
   kItemFull0, kItemFull1, kItemEmpty0, kItemEmpty1,
-  kDrain,
+  kDrain, kDrain2,
   kNumBars
 };
 
@@ -148,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kQEmpty], 1);
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bars[kKFull0 + i], 1);
-      mbar_init(&bars[kKEmpty0 + i], 1 + kSoftmaxWarps);  // MMA (commit or arrive) + softmax warps
+      mbar_init(&bars[kKEmpty0 + i], 2 + kSoftmaxWarps);  // both MMA warps (commit or arrive) + softmax warps
       mbar_init(&bars[kKAux0 + i], 1);
     }
     for (int i = 0; i < kVStages; ++i) {
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kItemFull0 + i], 1);
-      mbar_init(&bars[kItemEmpty0 + i], 1 + kSoftmaxWarps);
+      mbar_init(&bars[kItemEmpty0 + i], 2 + kSoftmaxWarps);
       mbar_init(&bars[kSFull0 + i], 1);   // S MMA commit
       mbar_init(&bars[kSFree0 + i], 1);   // dQ MMA commit: the buffer's dS was read
     }
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kDqFull], 1);
     mbar_init(&bars[kDqEmpty], kSoftmaxWarps);
     mbar_init(&bars[kDrain], 1);
+    mbar_init(&bars[kDrain2], 1);
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
@@ -341,27 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------------- MMA issuer: S and dP
     uint32_t nk = 0, nv = 0, itc = 0;  // K stages (end markers included), V stages
     uint32_t m = 0;                    // m: computed key tiles (S buffer m & 1)
     int where = 0;
     const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO);
-    // dQ += dS(mm) K: A = dS in S buffer mm & 1 (TMEM), B = K of stage kst
-    // (MN-major); `first` starts the item's accumulator
-    auto issue_dq = [&](uint32_t mm, int kst, bool first) {
-      tc_fence_after();
-      if (lane == 0) {
-        const uint64_t dKmn = sdesc_sw128(smem_u32(sK0 + kst * S::kTileBytes), kPanel, 1024);
-        const uint32_t sb = kColS0 + 128 * (mm & 1);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + kColQ, tmem + sb + ds_col(k), dKmn + (uint64_t)((k * 2048) >> 4), kIdQ,
-                 (first && k == 0) ? 0u : 1u);
-        tc_commit(&bars[kSFree0 + (mm & 1)]);
-        tc_commit(&bars[kKEmpty0 + kst]);  // K read for the last time
-      }
-      __syncwarp();
-    };
     while (true) {
       const int slot = itc & 1;
       if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
@@ -370,13 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
       if (idx < 0) break;
       if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
-      int j = 0, st_prev = 0;
       while (true) {
         const int st = nk % kKStages;
         if (!mbar_wait(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
+        __syncwarp();
         if (mt < 0) {
-          __syncwarp();
           if (lane == 0) {
             mbar_arrive(&bars[kKEmpty0 + st]);
             tc_commit(&bars[kQEmpty]);  // Q and dO: their last readers are issued
@@ -398,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(tmem + sb, dQk + off, dKk + off, kIdS, k > 0);
           }
           tc_commit(&bars[kSFull0 + (m & 1)]);
+          tc_commit(&bars[kKEmpty0 + st]);  // this warp's read of K (S)
         }
         __syncwarp();
         // dP has one buffer: the softmax warps must have read dP(m-1)
@@ -418,24 +407,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         ++nv;
-        if (j > 0) {  // dQ of the previous key tile, while the softmax works on this one
-          if (!mbar_wait(&bars[kDsReady], (m - 1) & 1, abort_flag)) { where = kErrWaitDS; break; }
-          // the first dQ MMA of an item overwrites the accumulator: the
-          // previous item's epilogue must have read it
-          if (j == 1 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
-          issue_dq(m - 1, st_prev, j == 1);
+        ++nk;
+        ++m;
+      }
+      if (where) break;
+      ++itc;
+    }
+    if (where) record_error(p.header, where);
+    if (*abort_flag) {
+      if (lane == 0) tc_commit(&bars[kDrain]);
+      __syncwarp();
+      mbar_wait_drain(&bars[kDrain], 0);
+    }
+  } else if (warp == kDqWarp) {
+    // ----------------------------------------------------- MMA issuer: dQ
+    uint32_t nk = 0, itc = 0, m = 0;  // as in the S / dP issuer
+    int where = 0;
+    while (true) {
+      const int slot = itc & 1;
+      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      const int idx = item_slot[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
+      if (idx < 0) break;
+      int j = 0;
+      while (true) {
+        const int st = nk % kKStages;
+        if (!mbar_wait(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        const int mt = meta[st];
+        __syncwarp();
+        if (mt < 0) {
+          if (lane == 0) mbar_arrive(&bars[kKEmpty0 + st]);
+          ++nk;
+          break;
         }
-        st_prev = st;
+        if (!mbar_wait(&bars[kDsReady], m & 1, abort_flag)) { where = kErrWaitDS; break; }
+        // the first dQ MMA of an item overwrites the accumulator: the
+        // previous item's epilogue must have read it
+        if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        tc_fence_after();
+        if (lane == 0) {  // dQ += dS(m) K: A = dS in S buffer m & 1 (TMEM), B = K (MN-major)
+          const uint64_t dKmn = sdesc_sw128(smem_u32(sK0 + st * S::kTileBytes), kPanel, 1024);
+          const uint32_t sb = kColS0 + 128 * (m & 1);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + kColQ, tmem + sb + ds_col(k), dKmn + (uint64_t)((k * 2048) >> 4), kIdQ,
+                   (j == 0 && k == 0) ? 0u : 1u);
+          tc_commit(&bars[kSFree0 + (m & 1)]);
+          tc_commit(&bars[kKEmpty0 + st]);  // K read for the last time
+        }
+        __syncwarp();
         ++j;
         ++nk;
         ++m;
       }
       if (where) break;
-      if (j > 0) {  // the item's last key tile
-        if (!mbar_wait(&bars[kDsReady], (m - 1) & 1, abort_flag)) { where = kErrWaitDS; break; }
-        if (j == 1 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
-        issue_dq(m - 1, st_prev, j == 1);
-      } else if (!mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) {  // once per item
+      if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) {  // once per item
         where = kErrWaitAcc;
         break;
       }
@@ -445,9 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (where) record_error(p.header, where);
     if (*abort_flag) {
-      if (lane == 0) tc_commit(&bars[kDrain]);
+      if (lane == 0) tc_commit(&bars[kDrain2]);
       __syncwarp();
-      mbar_wait_drain(&bars[kDrain], 0);
+      mbar_wait_drain(&bars[kDrain2], 0);
     }
   } else {
     // ----------------------------------------------------- P, dS, epilogue
