@@ -584,6 +584,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool first = e == e0, last = e + 1 == e1;
         const int st = n & 1;
         const uint32_t aQ = smem_u32(sQ0 + st * S::kTileBytes);
+        // with two 64-key blocks per tile, dS is zero on the keys of an
+        // unselected block: the dQ product skips their K-steps (keys 16k ..
+        // 16k + 15 for step k)
+        int kq0 = 0, kq1 = 8;
+        if (p.cb == 2) {
+          const int sub = entry_sub(p.entries[e]);
+          const bool h0 = ((sub | (sub >> 2)) & 1) != 0, h1 = ((sub | (sub >> 2)) & 2) != 0;
+          if (h0 != h1) {
+            kq0 = h0 ? 0 : 4;
+            kq1 = h0 ? 4 : 8;
+          }
+        }
         if (!mbar_wait<kTagCtl>(&bars[kDsReady], n & 1, abort_flag)) { where = kErrWaitDS; break; }
         if (first) {  // this item's K, and dK of the previous item read out
           if (!mbar_wait<kTagCtl>(&bars[kBufFull0 + kb], ic & 1, abort_flag)) { where = kErrWaitKV; break; }
@@ -597,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dSmn = sdesc_sw128(adS, kPanel, 1024), dKmn = sdesc_sw128(aK, kPanel, 1024);
           const uint64_t dSk = sdesc_sw128(adS, 16, 1024), dQmn = sdesc_sw128(aQ, kPanel, 1024);
           if (!p.det) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              mma_ss(tmem + kColP, dSmn + mn_step(k), dKmn + mn_step(k), kIdQ, k > 0);
+#pragma unroll 1
+            for (int k = kq0; k < kq1; ++k) {
+              mma_ss(tmem + kColP, dSmn + mn_step(k), dKmn + mn_step(k), kIdQ, k > kq0);
             }
           }
           tc_commit(&bars[kDqFull]);
