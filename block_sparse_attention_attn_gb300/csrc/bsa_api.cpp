@@ -468,11 +468,17 @@ uint64_t reserve_amask(bsa_executor* ex, const bsa_tensor* am, uint64_t off) {
 }
 
 // Points the plan at the packed token mask in `ws` and queues its packing.
-cudaError_t launch_amask_for(const bsa_executor* ex, Plan& p, uint8_t* ws, cudaStream_t st) {
-  if (!p.am) return cudaSuccess;
+// Points the plan at the packed token mask in the workspace (before anything
+// that copies the plan's pointers, such as the compaction arguments).
+void set_amask_ptrs(const bsa_executor* ex, Plan& p, uint8_t* ws) {
+  if (!p.am) return;
   p.am_row = reinterpret_cast<const uint32_t*>(ws + ex->off_am_row);
   p.am_col = reinterpret_cast<const uint32_t*>(ws + ex->off_am_col);
   p.am_sub = ws + ex->off_am_sub;
+}
+
+cudaError_t launch_amask_for(const bsa_executor* ex, const Plan& p, uint8_t* ws, cudaStream_t st) {
+  if (!p.am) return cudaSuccess;
   AmaskArgs a{};
   a.m = ex->am_ptr; a.st0 = ex->am_st0; a.st1 = ex->am_st1;
   a.rows = ex->am_rows; a.cols = ex->am_cols;
@@ -782,8 +788,7 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
                                 reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "copy of sequence info: %s", cudaGetErrorString(e));
-  if ((e = launch_amask_for(ex, p, ws, st)) != cudaSuccess)
-    return fail(BSA_ERR_RUNTIME, "token mask packing launch failed: %s", cudaGetErrorString(e));
+  set_amask_ptrs(ex, p, ws);
   CompactArgs ca{};
   ca.mask = p.mask; ca.sb = p.mask_sb; ca.sh = p.mask_sh; ca.si = p.mask_si;
   ca.has_mask = p.has_mask;
@@ -796,9 +801,9 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.win = p.win; ca.win_pre = p.win_pre; ca.win_next = p.win_next;
   ca.am_sub = p.am ? p.am_sub : nullptr; ca.am_sk = p.am_sk;
   ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
-  // The mask compaction and the planner (latency-bound, one block) run on a
-  // high-priority side stream while the preprocess (bandwidth-bound) runs on
-  // `st`.
+  // The token-mask packing, the mask compaction and the planner (small or
+  // latency-bound launches) run on a high-priority side stream while the
+  // preprocess (bandwidth-bound) runs on `st`.
   cudaStream_t side = nullptr;
   {
     int dev = 0;
@@ -810,6 +815,8 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   if (side && ((e = cudaEventRecord(ex->ev_fork, st)) != cudaSuccess ||
                (e = cudaStreamWaitEvent(side, ex->ev_fork, 0)) != cudaSuccess))
     goto launch_fail;
+  what = "token mask packing";
+  if ((e = launch_amask_for(ex, p, ws, cs)) != cudaSuccess) goto launch_fail;
   what = "column count";
   if ((e = launch_columns(ca, 0, cs)) != cudaSuccess) goto launch_fail;
   what = "planner";
@@ -1049,6 +1056,7 @@ bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* execu
   cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
                                 reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, kHdrWords * 4, st);
+  set_amask_ptrs(ex, f.p, ws);
   if (e == cudaSuccess) e = launch_amask_for(ex, f.p, ws, st);
   if (e == cudaSuccess && ex->ev_before) e = cudaEventRecord(ex->ev_before, st);
   if (e == cudaSuccess) e = launch_fwd(f, maps, st);

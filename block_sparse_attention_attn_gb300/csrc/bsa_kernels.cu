@@ -128,16 +128,35 @@ __global__ void k_rows(CompactArgs a, int fill) {
 // One 256-thread block per 64x64 sub-block (i, j): the bytes go through shared
 // memory once and come out as two 32-bit words per query row (keys
 // 64j .. 64j+63), two per key row (queries 64i .. 64i+63) and the sub-block's
-// class. Positions outside the matrix count as masked.
+// class. Positions outside the matrix count as masked. A whole sub-block of a
+// row-contiguous, 16-byte aligned matrix is read 16 bytes per thread.
 __global__ void __launch_bounds__(256) k_amask(AmaskArgs a) {
-  __shared__ uint8_t tile[64][65];
+  __shared__ __align__(16) uint8_t tile[64][80];  // 80-byte rows: 16-byte aligned, fewer conflicts
   const int i = blockIdx.y, j = blockIdx.x, tid = threadIdx.x;
-  for (int e = tid; e < 64 * 64; e += 256) {
-    const int r = e >> 6, c = e & 63;
-    const int s = i * 64 + r, t = j * 64 + c;
-    uint8_t v = 1;
-    if (s < a.rows && t < a.cols) v = a.m[(int64_t)s * a.st0 + (int64_t)t * a.st1] != 0;
-    tile[r][c] = v;
+  const bool whole = (i + 1) * 64 <= a.rows && (j + 1) * 64 <= a.cols;
+  const bool vec = whole && a.st1 == 1 && (a.st0 & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(a.m) & 15) == 0;
+  if (vec) {
+    const int r = tid >> 2, c0 = 16 * (tid & 3);
+    const uint4 u = *reinterpret_cast<const uint4*>(a.m + (int64_t)(i * 64 + r) * a.st0 + j * 64 + c0);
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // each byte -> 0 or 1 (bit 0 ORs the byte's bits)
+      uint32_t x = w[k];
+      x |= x >> 4;
+      x |= x >> 2;
+      x |= x >> 1;
+      w[k] = x & 0x01010101u;
+    }
+    *reinterpret_cast<uint4*>(&tile[r][c0]) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    for (int e = tid; e < 64 * 64; e += 256) {
+      const int r = e >> 6, c = e & 63;
+      const int s = i * 64 + r, t = j * 64 + c;
+      uint8_t v = 1;
+      if (s < a.rows && t < a.cols) v = a.m[(int64_t)s * a.st0 + (int64_t)t * a.st1] != 0;
+      tile[r][c] = v;
+    }
   }
   __syncthreads();
   const int r = tid >> 2, q = tid & 3;  // row / column r, 16-wide quarter q
