@@ -203,3 +203,30 @@ def test_atten_mask_large_whole():
     fin = np.isfinite(f64(tlse))
     np.testing.assert_array_equal(np.isneginf(f64(fl)), ~fin)
     np.testing.assert_allclose(f64(fl)[fin], f64(tlse)[fin], rtol=1e-4, atol=2e-3)
+
+
+def test_token_mask_drops_fully_masked_blocks():
+    """Blocks whose every pair the token mask masks never reach the work lists:
+    the number of (query tile, key tile) entries the compaction writes (header
+    word 3) equals a host count of the selected blocks that keep a pair. A
+    plan that lost the packed mask still computes correct gradients (the
+    element masks zero the extra tiles), so only this count shows it."""
+    w = small_workload(B=1, N1=2, N2=2, D=128, bx=128, by=128, seq_q=(1024,), seq_kv=(1024,),
+                       p=0.6, seed=71)
+    am = document_am(1024, 1024, seed=73, lo=60, hi=400)
+    dout, q, k, v = host_inputs(w)
+    g = [t.to(DEV) for t in (dout, q, k, v)]
+    out, lse = run_fwd(w, q, k, v, am)
+    dq, dk, dv = (torch.empty_like(g[i]) for i in (1, 2, 3))
+    size, ex = bsa.bsa_grad_workspace_size(*g, out, lse, torch.from_numpy(w.mask).to(DEV),
+                                           torch.from_numpy(am).to(DEV), [128, 128],
+                                           list(w.seq_q), list(w.seq_kv), "BNSD", "BNSD", 2, 1,
+                                           w.scale, dq=dq, dk=dk, dv=dv)
+    ws = torch.empty(size, dtype=torch.uint8, device=DEV)
+    bsa.bsa_grad(ws, size, ex)
+    bsa.bsa_check_status(ws)
+    hdr = ws[:64].view(torch.int32).cpu().numpy()
+    keeps = ~am.reshape(8, 128, 8, 128).all(axis=(1, 3))     # block (i, j) keeps a pair
+    expect = int(((w.mask[0] != 0) & keeps[None]).sum())
+    assert 0 < expect < w.mask[0].size
+    assert int(hdr[3]) == expect
