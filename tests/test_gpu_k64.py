@@ -10,9 +10,10 @@ import pytest
 import torch
 
 import block_sparse_attention_attn_gb300 as bsa
-from block_sparse_attention_attn_gb300.workloads import small_workload
+from block_sparse_attention_attn_gb300.workloads import make_workload, small_workload
 from oracle import bsa_oracle as O
-from tests.harness import check, f64, host_inputs, oracle_forward, rounded_out_lse
+from tests.harness import (check, check_whole, f64, host_inputs, oracle_backward_whole,
+                           oracle_forward, rounded_out_lse)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -20,12 +21,14 @@ DEV = "cuda:0"
 
 def run_grad(w, dout, q, k, v, out, lse, dq=None, dk=None, dv=None, det=False):
     mask = torch.from_numpy(w.mask).to(DEV)
+    seq_q = list(w.seq_q) if w.seq_q is not None else None
+    seq_kv = list(w.seq_kv) if w.seq_kv is not None else None
     g = [t.to(DEV) for t in (dout, q, k, v, out, lse)]
     dq = torch.empty_like(g[1]) if dq is None else dq
     dk = torch.empty_like(g[2]) if dk is None else dk
     dv = torch.empty_like(g[3]) if dv is None else dv
     size, ex = bsa.bsa_grad_workspace_size(
-        *g, mask, None, [w.bx, w.by], list(w.seq_q), list(w.seq_kv), w.layout, w.layout,
+        *g, mask, None, [w.bx, w.by], seq_q, seq_kv, w.layout, w.layout,
         w.N2, 0, w.scale, dq=dq, dk=dk, dv=dv)
     ex.set_key_block64(True)
     if det:
@@ -122,3 +125,15 @@ def test_k64_bounded_wait_reports_error():
     hdr = ws[:128].view(torch.int32).cpu().tolist()
     assert hdr[6] == 12 or hdr[16 + 12] > 0
     full_case(w)
+
+
+def test_k64_w3_whole():
+    """The full-size 128x64 workload (TND fp16, 8 sequences, GQA 4): every
+    element of dQ, dK and dV against the oracle's block-row evaluation."""
+    w = make_workload("w3")
+    dout, q, k, v = host_inputs(w)
+    out, lse = oracle_forward(w, q, k, v, blockrows=True)
+    tout, tlse = rounded_out_lse(w, out, lse)
+    del out, lse
+    dq, dk, dv, _, _ = run_grad(w, dout, q, k, v, tout, tlse)
+    check_whole("w3:k64", (dq, dk, dv), oracle_backward_whole(w, dout, q, k, v, tout, tlse))
