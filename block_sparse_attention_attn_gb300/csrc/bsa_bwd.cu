@@ -140,6 +140,32 @@ __device__ __noinline__ void mma_s_tile(uint32_t d_tmem, uint32_t aK, uint32_t a
   tc_commit(bar);
 }
 
+// Packed fp32 pairs (two lanes of one 64-bit register): one instruction for
+// two columns of the dS computation.
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Claims the next work item from the device queue (lane 0) and hands it to
 // every lane of the warp; x = -1 marks the end of the work.
 __device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
@@ -370,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t ro = (int64_t)h * p.Rq + p.qrow[ii.b] + q0 + 4 * lane;
           const float4 l4 = *reinterpret_cast<const float4*>(p.lse2 + ro);
           const float4 d4 = *reinterpret_cast<const float4*>(p.dvec + ro);
-          reinterpret_cast<float4*>(sLse + st * 128)[lane] = l4;
+          // negated: the softmax warps add it with a packed fp32x2 FMA
+          reinterpret_cast<float4*>(sLse + st * 128)[lane] = make_float4(-l4.x, -l4.y, -l4.z, -l4.w);
           reinterpret_cast<float4*>(sDv + st * 128)[lane] = d4;
         }
         __syncwarp();
@@ -696,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait<kTagSoftmax>(&bars[kQFull0 + st], (n >> 1) & 1, abort_flag)) { where = kErrWaitQ; break; }
         if (!mbar_wait<kTagSoftmax>(&bars[kSFull], n & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
-        const float* lse2 = sLse + st * 128;
+        const float* nlse2 = sLse + st * 128;  // -lse2 of the tile's query columns
         const float* dv = sDv + st * 128;
         // P^T of this thread's 64 columns, packed to the operand type (the
         // same rounded values feed the dV MMA and dS = P o (dP - D))
@@ -704,17 +731,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint32_t x[64];  // both 32-column chunks in one TMEM load
           tmem_ld64(tmem + lane_off + kColS + 64 * wg, x);
+          const uint64_t c2 = f2(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int s0 = 64 * wg + 32 * c;
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 l4 = reinterpret_cast<const float4*>(lse2 + s0)[j4];
+              const float4 l4 = reinterpret_cast<const float4*>(nlse2 + s0)[j4];
               const int xi = 32 * c + 4 * j4;
-              const float p0 = ex2_approx(fmaf(__uint_as_float(x[xi]), p.scale_log2, -l4.x));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(x[xi + 1]), p.scale_log2, -l4.y));
-              const float p2 = ex2_approx(fmaf(__uint_as_float(x[xi + 2]), p.scale_log2, -l4.z));
-              const float p3 = ex2_approx(fmaf(__uint_as_float(x[xi + 3]), p.scale_log2, -l4.w));
+              float t0, t1, t2, t3;
+              f2split(fma2(f2(x[xi], x[xi + 1]), c2, f2(__float_as_uint(l4.x), __float_as_uint(l4.y))), t0, t1);
+              f2split(fma2(f2(x[xi + 2], x[xi + 3]), c2, f2(__float_as_uint(l4.z), __float_as_uint(l4.w))), t2, t3);
+              const float p0 = ex2_approx(t0);
+              const float p1 = ex2_approx(t1);
+              const float p2 = ex2_approx(t2);
+              const float p3 = ex2_approx(t3);
               Ppk[16 * c + 2 * j4] = E::pack(p0, p1) & rmask;
               Ppk[16 * c + 2 * j4 + 1] = E::pack(p2, p3) & rmask;
             }
@@ -748,10 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int yi = 32 * c + 4 * j4;
               const float2 p01 = E::unpack(Ppk[16 * c + 2 * j4]);
               const float2 p23 = E::unpack(Ppk[16 * c + 2 * j4 + 1]);
-              pk[2 * j4] = E::pack(p01.x * (__uint_as_float(y[yi]) - d4.x),
-                                   p01.y * (__uint_as_float(y[yi + 1]) - d4.y));
-              pk[2 * j4 + 1] = E::pack(p23.x * (__uint_as_float(y[yi + 2]) - d4.z),
-                                       p23.y * (__uint_as_float(y[yi + 3]) - d4.w));
+              // two columns per packed fp32x2 subtract and multiply
+              float a0, a1, b0, b1;
+              f2split(mul2(sub2(f2(y[yi], y[yi + 1]), f2(__float_as_uint(d4.x), __float_as_uint(d4.y))),
+                           f2(__float_as_uint(p01.x), __float_as_uint(p01.y))), a0, a1);
+              f2split(mul2(sub2(f2(y[yi + 2], y[yi + 3]), f2(__float_as_uint(d4.z), __float_as_uint(d4.w))),
+                           f2(__float_as_uint(p23.x), __float_as_uint(p23.y))), b0, b1);
+              pk[2 * j4] = E::pack(a0, a1);
+              pk[2 * j4 + 1] = E::pack(b0, b1);
             }
             // dS into shared memory: panel wg, row t, 16-byte chunk cc holds
             // s = 64 wg + 8 cc .. +7, swizzled by t & 7 -- the MN-major A
