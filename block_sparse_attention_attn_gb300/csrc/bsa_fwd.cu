@@ -6,7 +6,7 @@
 // running row max m and sum l are updated per key tile and the partial PV
 // product is rescaled by exp(m_old - m_new) when the max grows.
 //
-// One persistent CTA per SM, 352 threads:
+// One persistent CTA per SM, 384 threads:
 //   warp 8      producer: scans the mask row(s) of its query tile for selected
 //               key tiles and streams K/V tiles through a 3-stage TMA ring;
 //   warp 9      MMA issuer of S = Q K^T (into one of two TMEM buffers, as soon
@@ -41,11 +41,17 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;   // S = Q K^T; TMEM owner
-constexpr int kPvWarp = 10;   // O += P V
+constexpr int kPvWarp = 10;   // O += P V; warp 11 only lends its registers
+// Registers per thread after the hand-over (launch: 384 x 168): the control
+// warpgroup (warps 8-11) keeps 64, the two softmax warpgroups get 208 each
+// (2 x 208 + 64 <= 3 x 168). Each budget has its own copy of the out-of-line
+// wait loop (wait tags).
+constexpr int kRegsLaunch = 168, kRegsCtl = 64, kRegsSoftmax = 208;
+constexpr int kTagCtl = 1, kTagSoftmax = 2;
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;  // O_wg at kColO + wg * D
 constexpr float kRescaleThreshold = 8.f;
@@ -185,6 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK0 = smem + S::oK;
   uint8_t* sV0 = smem + S::oV;
 
+  if (warp >= kProdWarp) {
+  regs_release<kRegsCtl>();  // all four warps of the control warpgroup
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     uint32_t n = 0, itc = 0, aux[kStages] = {0u, 0u, 0u};
@@ -193,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par_kv[kStages] = {0u, 0u, 0u};
     while (ok) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitItem);
         break;
       }
@@ -209,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Lq = p.lq[fi.b], Lk = p.lk[fi.b];
       const int q0 = fi.it * 128;
       const bool has_rows = q0 < Lq;
-      if (!mbar_wait(&bars[kQEmpty], (itc & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kQEmpty], (itc & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitQ);
         break;
       }
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jsel = jt0 + src;
           const int bsel = __shfl_sync(0xffffffffu, bits, src);
           const int st = n % kStages;
-          if (!mbar_wait(&bars[kKvEmpty0 + st], ((n / kStages) & 1) ^ 1, abort_flag)) {
+          if (!mbar_wait<kTagCtl>(&bars[kKvEmpty0 + st], ((n / kStages) & 1) ^ 1, abort_flag)) {
             record_error(p.header, kErrWaitKV);
             ok = false;
             break;
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           par_kv[st] = (n / kStages) & 1;
           if (tail) {
             pend_aux[st] = 1;
-            if (!mbar_wait(&bars[kKvAux0 + st], aux[st] & 1, abort_flag)) {
+            if (!mbar_wait<kTagCtl>(&bars[kKvAux0 + st], aux[st] & 1, abort_flag)) {
               record_error(p.header, kErrWaitKV);
               ok = false;
               break;
@@ -272,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // end-of-item marker
       const int st = n % kStages;
-      if (!mbar_wait(&bars[kKvEmpty0 + st], ((n / kStages) & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kKvEmpty0 + st], ((n / kStages) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitKV);
         break;
       }
@@ -299,16 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aQ = smem_u32(sQ);
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int idx = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
       if (idx < 0) break;
-      if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
       tc_fence_after();
       while (true) {
         const int st = n % kStages;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (mt < 0) {
@@ -318,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // S(m) into buffer m & 1 once both PV halves of tile m-2 have read its P
         const uint32_t sb = m & 1;
-        if (!mbar_wait(&bars[kPvDone00 + 2 * sb], ((m >> 1) & 1) ^ 1, abort_flag) ||
-            !mbar_wait(&bars[kPvDone00 + 2 * sb + 1], ((m >> 1) & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait<kTagCtl>(&bars[kPvDone00 + 2 * sb], ((m >> 1) & 1) ^ 1, abort_flag) ||
+            !mbar_wait<kTagCtl>(&bars[kPvDone00 + 2 * sb + 1], ((m >> 1) & 1) ^ 1, abort_flag)) {
           where = kErrWaitMisc;
           break;
         }
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int idx = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -364,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0;
       while (true) {
         const int st = n % kStages;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (mt < 0) {
@@ -379,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t colS = (m & 1) ? kColS1 : kColS0;
         const uint32_t aV = smem_u32(sV0 + st * S::kTileBytes);
         for (int wg = 0; wg < 2 && !where; ++wg) {
-          if (!mbar_wait(&bars[kPReady00 + 2 * (m & 1) + wg], (m >> 1) & 1, abort_flag)) {
+          if (!mbar_wait<kTagCtl>(&bars[kPReady00 + 2 * (m & 1) + wg], (m >> 1) & 1, abort_flag)) {
             where = kErrWaitP;
             break;
           }
-          if (j == 0 && wg == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
+          if (j == 0 && wg == 0 && !mbar_wait<kTagCtl>(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
             where = kErrWaitAcc;
             break;
           }
@@ -407,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (where) break;
       // every item waits for the previous epilogue exactly once (a parity
       // wait cannot tell phase c from phase c-2, so no item may skip it)
-      if (j == 0 && !mbar_wait(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
+      if (j == 0 && !mbar_wait<kTagCtl>(&bars[kOEmpty], (itc & 1) ^ 1, abort_flag)) {
         where = kErrWaitAcc;
         break;
       }
@@ -421,7 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       mbar_wait_drain(&bars[kDrain2], 0);
     }
+  }
   } else {
+    regs_claim<kRegsSoftmax>();
     // ------------------------------------------------------------- softmax
     const int qd = warp & 3, wg = warp >> 2;
     const int s = qd * 32 + lane;  // query row within the tile
@@ -432,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagSoftmax>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int idx = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -444,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0;
       while (true) {
         const int st = n % kStages;
-        if (!mbar_wait(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kKvFull0 + st], (n / kStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kKvEmpty0 + st]);
@@ -452,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jt = mt & 0xFFFFFF, bits = mt >> 24;
         const uint32_t sb = m_step & 1;
         const uint32_t colS = sb ? kColS1 : kColS0;
-        if (!mbar_wait(&bars[kSFull0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kSFull0 + sb], (m_step >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
         // live columns: inside the key length and the sliding window ([t_lo,
         // t_hi)), in a selected key sub-block, kept by the token mask;
@@ -533,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, grow) && j > 0) {
           // after this warpgroup's previous PV product has landed
           const uint32_t pb = (m_step - 1) & 1;
-          if (!mbar_wait(&bars[kPvDone00 + 2 * pb + wg], ((m_step - 1) >> 1) & 1, abort_flag)) {
+          if (!mbar_wait<kTagSoftmax>(&bars[kPvDone00 + 2 * pb + wg], ((m_step - 1) >> 1) & 1, abort_flag)) {
             where = kErrWaitMisc;
             break;
           }
@@ -568,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* xb = xch + (xs & 1) * 256;
         xb[wg * 128 + s] = m;
         mbar_arrive(&bars[kXch0 + (xs & 1)]);
-        if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
         m_o = xb[(wg ^ 1) * 128 + s];
         ++xs;
       }
@@ -579,12 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* lb = xch + (xs & 1) * 256;
         lb[wg * 128 + s] = l * a_own;
         mbar_arrive(&bars[kXch0 + (xs & 1)]);
-        if (!mbar_wait(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kXch0 + (xs & 1)], (xs >> 1) & 1, abort_flag)) { where = kErrWaitMisc; break; }
         l = l * a_own + lb[(wg ^ 1) * 128 + s];
         ++xs;
       }
       m = M;
-      if (!mbar_wait(&bars[kOFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
+      if (!mbar_wait<kTagSoftmax>(&bars[kOFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const int srow = fi.it * 128 + s;
       const bool write_row = p.layout == kLayoutBNSD ? (srow < p.Sq) : (srow < Lq);
@@ -661,6 +671,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int DT>
 cudaError_t launch_t(const FwdPlan& f, const FwdMaps& m, cudaStream_t st) {
   const size_t smem = Smem<D>::kBytes;
+  // The register hand-over only balances when every thread starts with
+  // kRegsLaunch registers (a claim beyond what the others release would wait
+  // for registers nobody frees).
+  static const int regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, k_fwd<D, DT>) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  static_assert(2 * kRegsSoftmax + kRegsCtl <= 3 * kRegsLaunch, "register hand-over must balance");
+  static_assert(kRegsLaunch * kThreads <= 65536, "launch registers");
+  if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(k_fwd<D, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int grid = f.p.num_sms;
