@@ -90,6 +90,37 @@ __device__ __forceinline__ void zero_rows(uint8_t* tile, int panels, int r0, int
   }
 }
 
+// Packed fp32 pairs (two lanes of one 64-bit register) and three-input
+// min / max: one instruction for two elements of the softmax loops.
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 struct FItem {
   int b, h, it;
 };
@@ -493,10 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // into the min)
           const bool pos = p.scale_log2 >= 0.f;
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (all_live) {
+          if (all_live && pos) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k)
-              m4[k & 3] = fmaxf(m4[k & 3], pos ? __uint_as_float(x[k]) : -__uint_as_float(x[k]));
+            for (int k = 0; k < 64; k += 2)
+              m4[(k >> 1) & 3] = max3(m4[(k >> 1) & 3], __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+          } else if (all_live) {
+            float n4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+#pragma unroll
+            for (int k = 0; k < 64; k += 2)
+              n4[(k >> 1) & 3] = min3(n4[(k >> 1) & 3], __uint_as_float(x[k]), __uint_as_float(x[k + 1]));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) m4[i] = -n4[i];
           } else {
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
@@ -519,13 +557,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
         if (all_live) {
+          // pairs of keys: one packed FMA for both exponents, one packed add
+          // into two running pair sums
+          const uint64_t c2 = f2(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+          const uint64_t nm2 = f2(__float_as_uint(-m), __float_as_uint(-m));
+          uint64_t sA = 0ull, sB = 0ull;
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -m));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -m));
-            rs4[k & 3] += e0 + e1;
+            float t0, t1;
+            f2split(fma2(f2(x[2 * k], x[2 * k + 1]), c2, nm2), t0, t1);
+            const float e0 = ex2_approx(t0);
+            const float e1 = ex2_approx(t1);
+            const uint64_t e = f2(__float_as_uint(e0), __float_as_uint(e1));
+            if (k & 1) sB = add2(sB, e);
+            else sA = add2(sA, e);
             pk[k] = E::pack(e0, e1);
           }
+          f2split(sA, rs4[0], rs4[1]);
+          f2split(sB, rs4[2], rs4[3]);
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
