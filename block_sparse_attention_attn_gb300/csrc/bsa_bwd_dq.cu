@@ -8,7 +8,7 @@
 // other CTAs finish: no fp32 reduce-adds, the same bits on every run. The
 // key-tile-stationary kernel then computes dK and dV only.
 //
-// One persistent CTA per SM, 352 threads:
+// One persistent CTA per SM, 384 threads:
 //   warp 8      producer: Q and dO of the query tile, then K and V tiles of
 //               the selected key tiles (found by scanning the mask row)
 //               through TMA rings of 3 (K: read by S and the later dQ) and
@@ -39,11 +39,16 @@
 namespace bsa {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;   // S, dP; TMEM owner
-constexpr int kDqWarp = 10;   // dQ
+constexpr int kDqWarp = 10;   // dQ; warp 11 only lends its registers
+// Registers per thread after the hand-over (launch: 384 x 168): the control
+// warpgroup (warps 8-11) keeps 64, the two softmax warpgroups get 208 each.
+// Each budget has its own copy of the out-of-line wait loop (wait tags).
+constexpr int kRegsLaunch = 168, kRegsCtl = 64, kRegsSoftmax = 208;
+constexpr int kTagCtl = 1, kTagSoftmax = 2;
 constexpr int kPanel = 128 * 128;
 constexpr uint32_t kColS0 = 0, kColP = 256, kColQ = 384;
 constexpr int kKStages = 3, kVStages = 2;
@@ -74,12 +79,38 @@ struct Smem {
   static constexpr int kBytes = oMisc + 128;
 };
 
-__device__ __noinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
+__device__ __forceinline__ void zero_rows(uint8_t* tile, int panels, int r0, int lane) {
   const int n16 = (128 - r0) * 8;
   for (int pnl = 0; pnl < panels; ++pnl) {
     uint4* base = reinterpret_cast<uint4*>(tile + pnl * kPanel + r0 * 128);
     for (int i = lane; i < n16; i += 32) base[i] = make_uint4(0u, 0u, 0u, 0u);
   }
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register): one instruction for
+// two columns of the P and dS loops.
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 struct QItem {
@@ -195,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV0 = smem + S::oV;
   const int n_items = p.B * p.N1 * p.Mq_t;
 
+  if (warp >= kProdWarp) {
+  regs_release<kRegsCtl>();  // all four warps of the control warpgroup
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ producer
     uint32_t nk = 0, nv = 0, itc = 0, qaux = 0;  // K stages (end markers included), V stages
@@ -206,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par_k[kKStages] = {0u, 0u, 0u}, par_v[kVStages] = {0u, 0u};
     while (ok) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kItemEmpty0 + slot], ((itc >> 1) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitItem);
         break;
       }
@@ -223,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = qi.it * 128;
       const bool has_rows = q0 < Lq;
       // Q and dO of the query tile (rows past the query length cleared)
-      if (!mbar_wait(&bars[kQEmpty], (itc & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kQEmpty], (itc & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitQ);
         break;
       }
@@ -241,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pend_q = qtail ? 0 : 1;
       pend_qaux = qtail ? 1 : 0;
       if (qtail) {
-        if (!mbar_wait(&bars[kQAux], qaux & 1, abort_flag)) {
+        if (!mbar_wait<kTagCtl>(&bars[kQAux], qaux & 1, abort_flag)) {
           record_error(p.header, kErrWaitQ);
           break;
         }
@@ -266,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jsel = jt0 + src;
           const int bsel = __shfl_sync(0xffffffffu, bits, src);
           const int kst = nk % kKStages, vst = nv % kVStages;
-          if (!mbar_wait(&bars[kKEmpty0 + kst], ((nk / kKStages) & 1) ^ 1, abort_flag) ||
-              !mbar_wait(&bars[kVEmpty0 + vst], ((nv / kVStages) & 1) ^ 1, abort_flag)) {
+          if (!mbar_wait<kTagCtl>(&bars[kKEmpty0 + kst], ((nk / kKStages) & 1) ^ 1, abort_flag) ||
+              !mbar_wait<kTagCtl>(&bars[kVEmpty0 + vst], ((nv / kVStages) & 1) ^ 1, abort_flag)) {
             record_error(p.header, kErrWaitKV);
             ok = false;
             break;
@@ -295,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tail) {  // K and V rows past the key length must be finite zeros
             pend_kaux[kst] = 1;
             pend_vaux[vst] = 1;
-            if (!mbar_wait(&bars[kKAux0 + kst], kaux[kst] & 1, abort_flag) ||
-                !mbar_wait(&bars[kVAux0 + vst], vaux[vst] & 1, abort_flag)) {
+            if (!mbar_wait<kTagCtl>(&bars[kKAux0 + kst], kaux[kst] & 1, abort_flag) ||
+                !mbar_wait<kTagCtl>(&bars[kVAux0 + vst], vaux[vst] & 1, abort_flag)) {
               record_error(p.header, kErrWaitKV);
               ok = false;
               break;
@@ -321,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // end-of-item marker (a K stage without a copy)
       const int kst = nk % kKStages;
-      if (!mbar_wait(&bars[kKEmpty0 + kst], ((nk / kKStages) & 1) ^ 1, abort_flag)) {
+      if (!mbar_wait<kTagCtl>(&bars[kKEmpty0 + kst], ((nk / kKStages) & 1) ^ 1, abort_flag)) {
         record_error(p.header, kErrWaitKV);
         break;
       }
@@ -353,15 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO);
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int idx = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
       if (idx < 0) break;
-      if (!mbar_wait(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kQFull], itc & 1, abort_flag)) { where = kErrWaitQ; break; }
       while (true) {
         const int st = nk % kKStages;
-        if (!mbar_wait(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (mt < 0) {
@@ -375,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sb = kColS0 + 128 * (m & 1);
         // the S buffer is free once the dQ MMA of tile m-2 has read its dS
-        if (!mbar_wait(&bars[kSFree0 + (m & 1)], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kSFree0 + (m & 1)], ((m >> 1) & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
         const uint32_t aK = smem_u32(sK0 + st * S::kTileBytes);
         if (lane == 0) {
@@ -391,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // dP has one buffer: the softmax warps must have read dP(m-1)
         const int vst = nv % kVStages;
-        if (!mbar_wait(&bars[kDpFree], (m & 1) ^ 1, abort_flag)) { where = kErrWaitDP; break; }
-        if (!mbar_wait(&bars[kVFull0 + vst], (nv / kVStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kDpFree], (m & 1) ^ 1, abort_flag)) { where = kErrWaitDP; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kVFull0 + vst], (nv / kVStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         tc_fence_after();
         if (lane == 0) {
           const uint64_t dOk = sdesc_sw128(adO, 16, 1024);
@@ -425,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagCtl>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int idx = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -433,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0;
       while (true) {
         const int st = nk % kKStages;
-        if (!mbar_wait(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kKFull0 + st], (nk / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (mt < 0) {
@@ -441,10 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nk;
           break;
         }
-        if (!mbar_wait(&bars[kDsReady], m & 1, abort_flag)) { where = kErrWaitDS; break; }
+        if (!mbar_wait<kTagCtl>(&bars[kDsReady], m & 1, abort_flag)) { where = kErrWaitDS; break; }
         // the first dQ MMA of an item overwrites the accumulator: the
         // previous item's epilogue must have read it
-        if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
+        if (j == 0 && !mbar_wait<kTagCtl>(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) { where = kErrWaitAcc; break; }
         tc_fence_after();
         if (lane == 0) {  // dQ += dS(m) K: A = dS in S buffer m & 1 (TMEM), B = K (MN-major)
           const uint64_t dKmn = sdesc_sw128(smem_u32(sK0 + st * S::kTileBytes), kPanel, 1024);
@@ -462,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++m;
       }
       if (where) break;
-      if (j == 0 && !mbar_wait(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) {  // once per item
+      if (j == 0 && !mbar_wait<kTagCtl>(&bars[kDqEmpty], (itc & 1) ^ 1, abort_flag)) {  // once per item
         where = kErrWaitAcc;
         break;
       }
@@ -476,7 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       mbar_wait_drain(&bars[kDrain2], 0);
     }
+  }
   } else {
+    regs_claim<kRegsSoftmax>();
     // ----------------------------------------------------- P, dS, epilogue
     const int qd = warp & 3, wg = warp >> 2;
     const int s = qd * 32 + lane;  // query row within the tile
@@ -485,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int where = 0;
     while (true) {
       const int slot = itc & 1;
-      if (!mbar_wait(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
+      if (!mbar_wait<kTagSoftmax>(&bars[kItemFull0 + slot], (itc >> 1) & 1, abort_flag)) { where = kErrWaitItem; break; }
       const int idx = item_slot[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kItemEmpty0 + slot]);
@@ -503,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = 0;
       while (true) {
         const int st = n % kKStages;
-        if (!mbar_wait(&bars[kKFull0 + st], (n / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kKFull0 + st], (n / kKStages) & 1, abort_flag)) { where = kErrWaitKV; break; }
         const int mt = meta[st];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kKEmpty0 + st]);
@@ -527,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t live0 = row_on ? bit_range(t_lo - 64 * wg, t_hi - 64 * wg) & ~amw.x : 0u;
         const uint32_t live1 = row_on ? bit_range(t_lo - 64 * wg - 32, t_hi - 64 * wg - 32) & ~amw.y : 0u;
         const uint32_t sb = kColS0 + 128 * (m & 1);
-        if (!mbar_wait(&bars[kSFull0 + (m & 1)], (m >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kSFull0 + (m & 1)], (m >> 1) & 1, abort_flag)) { where = kErrWaitS; break; }
         tc_fence_after();
         // P of this warpgroup's 64 keys, rounded to the operand type as in the
         // dV/dK kernel, kept packed in registers
@@ -536,10 +571,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t x[64];  // both 32-column chunks in one TMEM load
           tmem_ld64(tmem + lane_off + sb + 64 * wg, x);
           if ((live0 & live1) == 0xFFFFFFFFu) {  // every key takes part: no per-key tests
+            const uint64_t c2 = f2(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+            const uint64_t nl2 = f2(__float_as_uint(-lse2), __float_as_uint(-lse2));
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-              Ppk[k] = E::pack(ex2_approx(fmaf(__uint_as_float(x[2 * k]), p.scale_log2, -lse2)),
-                               ex2_approx(fmaf(__uint_as_float(x[2 * k + 1]), p.scale_log2, -lse2)));
+            for (int k = 0; k < 32; ++k) {
+              float t0, t1;
+              f2split(fma2(f2(x[2 * k], x[2 * k + 1]), c2, nl2), t0, t1);
+              Ppk[k] = E::pack(ex2_approx(t0), ex2_approx(t1));
+            }
           } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
@@ -554,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (!mbar_wait(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
+        if (!mbar_wait<kTagSoftmax>(&bars[kDpFull], m & 1, abort_flag)) { where = kErrWaitDP; break; }
         tc_fence_after();
         uint32_t y[64];
         tmem_ld64(tmem + lane_off + kColP + 64 * wg, y);
@@ -564,11 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS = P o (dP - D), packed in place over this warpgroup's S columns
         {
           uint32_t pk[32];
+          const uint64_t d2 = f2(__float_as_uint(dsum), __float_as_uint(dsum));
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < 32; ++k) {  // two columns per packed subtract and multiply
             const float2 pp = E::unpack(Ppk[k]);
-            pk[k] = E::pack(pp.x * (__uint_as_float(y[2 * k]) - dsum),
-                            pp.y * (__uint_as_float(y[2 * k + 1]) - dsum));
+            float a0, a1;
+            f2split(mul2(sub2(f2(y[2 * k], y[2 * k + 1]), d2), f2(__float_as_uint(pp.x), __float_as_uint(pp.y))),
+                    a0, a1);
+            pk[k] = E::pack(a0, a1);
           }
           tmem_st32(tmem + lane_off + sb + 96 * wg, pk);
         }
@@ -582,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (where) break;
       // epilogue: dQ = scale * accumulator (zeros when no key tile was
       // selected); warpgroup wg writes the columns [wg D/2, wg D/2 + D/2)
-      if (!mbar_wait(&bars[kDqFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
+      if (!mbar_wait<kTagSoftmax>(&bars[kDqFull], itc & 1, abort_flag)) { where = kErrWaitAcc; break; }
       tc_fence_after();
       const bool write_row = p.layout == kLayoutBNSD ? (srow < p.Sq) : s_ok;
       int64_t ooff, sd;
@@ -641,6 +683,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int DT>
 cudaError_t launch_t(const Plan& p, const BwdMaps& m, cudaStream_t st) {
+  // The register hand-over only balances when every thread starts with
+  // kRegsLaunch registers.
+  static const int regs = [] {
+    cudaFuncAttributes fa{};
+    return cudaFuncGetAttributes(&fa, k_bwd_dq<D, DT>) == cudaSuccess ? fa.numRegs : -1;
+  }();
+  static_assert(2 * kRegsSoftmax + kRegsCtl <= 3 * kRegsLaunch, "register hand-over must balance");
+  static_assert(kRegsLaunch * kThreads <= 65536, "launch registers");
+  if (regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const size_t smem = Smem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
