@@ -358,33 +358,63 @@ N_COPY_STREAMS = 1
 
 # The other configurations of the workload table, timed in the same run
 # after the headline one (w1dense: configs[1] with mask = nullptr).
-OTHER_CONFIGS = ["w1dense", "w2", "w3", "w4"]
+# (record name, workload, mode): mode "grad" is the default backward, "det"
+# the deterministic dQ mode, "k64" the 64-key-block kernel, "fwd" the forward
+OTHER_CONFIGS = [("w1dense", "w1dense", "grad"), ("w2", "w2", "grad"), ("w3", "w3", "grad"),
+                 ("w4", "w4", "grad"), ("w3_key_block64", "w3", "k64"),
+                 ("w1_deterministic", "w1", "det"), ("w4_deterministic", "w4", "det"),
+                 ("w1_forward", "w1", "fwd"), ("w4_forward", "w4", "fwd")]
 
 
 def other_configs(args, world, local, peak):
     """kernel / step time, roofline fraction and clocks of OTHER_CONFIGS."""
     import torch
 
+    import block_sparse_attention_attn_gb300 as bsa
     from block_sparse_attention_attn_gb300.workloads import make_workload
+    global DETERMINISTIC, KEY_BLOCK64
     dev = torch.device("cuda", local)
     res = {}
-    for name in OTHER_CONFIGS:
+    saved = (DETERMINISTIC, KEY_BLOCK64)
+    for key, name, mode in OTHER_CONFIGS:
         w = make_workload(name)
-        flops = w.flops()
+        flops = (0.4 if mode == "fwd" else 1.0) * w.flops()
         t, seq = make_inputs(w, dev)
-        dq, dk, dv = (torch.empty_like(t[k_]) for k_ in ("query", "key", "value"))
         steps = max(3, min(args.steps, args.config_steps))
-        ms_step, ms_kern, clk, _, ws, _ = time_backward(w, t, seq, dq, dk, dv, steps,
-                                                        max(3, args.warmup), local, world)
+        if mode == "fwd":
+            q, k, v = t["query"], t["key"], t["value"]
+            out, lse = torch.empty_like(t["attention_out"]), torch.empty_like(t["softmax_lse"])
+
+            def fwd_executor():
+                return bsa.bsa_fwd_workspace_size(
+                    q, k, v, t["block_sparse_mask"], [w.bx, w.by], seq["actual_seq_lengths"],
+                    seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, w.scale,
+                    w.pre_tokens, w.next_tokens, out, lse, t["atten_mask"])
+            ms_step, ms_kern, clk = time_forward(fwd_executor, steps, max(3, args.warmup),
+                                                 local, world)
+            del q, k, v, out, lse
+        else:
+            DETERMINISTIC, KEY_BLOCK64 = mode == "det", mode == "k64"
+            dq, dk, dv = (torch.empty_like(t[k_]) for k_ in ("query", "key", "value"))
+            ms_step, ms_kern, clk, _, ws, _ = time_backward(w, t, seq, dq, dk, dv, steps,
+                                                            max(3, args.warmup), local, world)
+            DETERMINISTIC, KEY_BLOCK64 = saved
+            del dq, dk, dv, ws
         ach = flops / (ms_kern * 1e-3) / 1e12
-        res[name] = {"gflop_per_step": round(flops / 1e9, 2), "steps": steps,
-                     "ms_per_step": round(ms_step, 4),
-                     "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
-                     "kernel_ms": round(ms_kern, 4), "achieved": round(ach, 2),
-                     "frac": round(ach / peak, 4), "traffic": committed_traffic(name),
-                     "clocks": clk}
-        del t, dq, dk, dv, ws
+        res[key] = {"workload": name, "mode": {"grad": "default backward",
+                                               "det": "backward, deterministic dQ",
+                                               "k64": "backward, 64-key blocks",
+                                               "fwd": "companion forward (4*D FLOP per pair)"}[mode],
+                    "gflop_per_step": round(flops / 1e9, 2), "steps": steps,
+                    "ms_per_step": round(ms_step, 4),
+                    "value": round(world * flops / (ms_step * 1e-3) / 1e12, 2),
+                    "kernel_ms": round(ms_kern, 4), "achieved": round(ach, 2),
+                    "frac": round(ach / peak, 4),
+                    "traffic": committed_traffic(name) if mode == "grad" else None,
+                    "clocks": clk}
+        del t
         torch.cuda.empty_cache()
+    DETERMINISTIC, KEY_BLOCK64 = saved
     return res
 
 
@@ -467,36 +497,24 @@ def bench_ours(args, rank, world, local):
 FWD_METRIC = "block-sparse attn fwd TFLOP/s (companion forward, active blocks)"
 
 
-def bench_forward(args, rank, world, local):
-    """The same protocol for bsa_fwd: Out and lse of one workload per step;
-    4*D FLOP per (query, key) pair per query head (S = QK^T and O = PV)."""
+def time_forward(fwd_executor, steps, warmup, local, world):
+    """The timed protocol of the forward (as time_backward's): `warmup`
+    untimed steps, then `steps` steps, each after a 512 MB L2 flush, with CUDA
+    events around the call and around the main kernel. Returns (mean step ms,
+    mean kernel ms, clocks)."""
     import torch
 
     import block_sparse_attention_attn_gb300 as bsa
-    from block_sparse_attention_attn_gb300.workloads import make_workload
-    dev = torch.device("cuda", local)
-    w = make_workload(args.workload)
-    flops = 0.4 * w.flops()
-    t, seq = make_inputs(w, dev)
-    q, k, v = t["query"], t["key"], t["value"]
-    out, lse = torch.empty_like(t["attention_out"]), torch.empty_like(t["softmax_lse"])
-
-    def fwd_executor():
-        return bsa.bsa_fwd_workspace_size(
-            q, k, v, t["block_sparse_mask"], [w.bx, w.by], seq["actual_seq_lengths"],
-            seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, w.scale, w.pre_tokens,
-            w.next_tokens, out, lse, t["atten_mask"])
-
     size, _ = fwd_executor()
-    ws = torch.empty(size, dtype=torch.uint8, device=dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ws = torch.empty(size, dtype=torch.uint8, device=torch.cuda.current_device())
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=ws.device)
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         bsa.bsa_fwd(ws, size, fwd_executor()[1], stream)
     torch.cuda.synchronize()
     bsa.bsa_check_status(ws)
-    n = args.steps
+    n = steps
     exs = [fwd_executor()[1] for _ in range(n)]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
     for e in ev:
@@ -520,6 +538,31 @@ def bench_forward(args, rank, world, local):
     bsa.bsa_check_status(ws)
     ms_step = max_over_ranks(float(np.mean([e[0].elapsed_time(e[3]) for e in ev])), world)
     ms_kern = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
+    del flush
+    return ms_step, ms_kern, clk
+
+
+def bench_forward(args, rank, world, local):
+    """The same protocol for bsa_fwd: Out and lse of one workload per step;
+    4*D FLOP per (query, key) pair per query head (S = QK^T and O = PV)."""
+    import torch
+
+    import block_sparse_attention_attn_gb300 as bsa
+    from block_sparse_attention_attn_gb300.workloads import make_workload
+    dev = torch.device("cuda", local)
+    w = make_workload(args.workload)
+    flops = 0.4 * w.flops()
+    t, seq = make_inputs(w, dev)
+    q, k, v = t["query"], t["key"], t["value"]
+    out, lse = torch.empty_like(t["attention_out"]), torch.empty_like(t["softmax_lse"])
+
+    def fwd_executor():
+        return bsa.bsa_fwd_workspace_size(
+            q, k, v, t["block_sparse_mask"], [w.bx, w.by], seq["actual_seq_lengths"],
+            seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, w.scale, w.pre_tokens,
+            w.next_tokens, out, lse, t["atten_mask"])
+
+    ms_step, ms_kern, clk = time_forward(fwd_executor, args.steps, args.warmup, local, world)
     # end to end: pinned host Q, K, V (and masks) -> H2D -> both stages -> D2H of Out, lse
     fin = {k_: t[k_] for k_ in ("query", "key", "value", "block_sparse_mask", "atten_mask")}
 
