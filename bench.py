@@ -562,7 +562,8 @@ def bench_forward(args, rank, world, local):
             seq["actual_seq_lengths_kv"], w.layout, w.layout, w.N2, w.scale, w.pre_tokens,
             w.next_tokens, out, lse, t["atten_mask"])
 
-    ms_step, ms_kern, clk = time_forward(fwd_executor, args.steps, args.warmup, local, world)
+    n = args.steps
+    ms_step, ms_kern, clk = time_forward(fwd_executor, n, args.warmup, local, world)
     # end to end: pinned host Q, K, V (and masks) -> H2D -> both stages -> D2H of Out, lse
     fin = {k_: t[k_] for k_ in ("query", "key", "value", "block_sparse_mask", "atten_mask")}
 
