@@ -10,6 +10,7 @@
 // equal q/kv layouts). preTokens / nextTokens define a sliding window (any
 // pair with preTokens + nextTokens >= 0) instead of being fixed at 2147483647.
 #include <climits>
+#include <cstdlib>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -171,6 +172,17 @@ bool encode_out_map(CUtensorMap* m, const bsa_tensor* t, int layout) {
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// BSA_LOG (environment, any value but "0"): the first-stage call prints the
+// plan, the run call the kernels it launches, and bsa_check_status the device
+// work-list counts, one line each on stderr.
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("BSA_LOG");
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+  }();
+  return on;
 }
 
 // One non-blocking side stream per device (created once, never destroyed),
@@ -733,6 +745,15 @@ bsa_status bsa_grad_workspace_size(
   }
   *workspace_size = off;
   *executor = ex;
+  if (log_enabled())
+    std::fprintf(stderr,
+                 "[bsa] grad plan: layout=%s dtype=%s B=%d N1=%d N2=%d D=%d Sq=%d Skv=%d "
+                 "block=[%d,%d] tiles q=%d k=%d block_mask=%s window=%s token_mask=%s "
+                 "waves=%d max_items=%d max_split_slots=%d workspace=%llu bytes\n",
+                 g.layout == kLayoutBNSD ? "BNSD" : "TND", g.dtype == kDtBF16 ? "bf16" : "f16", g.B,
+                 g.N1, g.N2, g.D, g.Sq, g.Skv, g.bx, g.by, p.Mq_t, p.Mk_t, p.has_mask ? "yes" : "no",
+                 p.win ? "yes" : "no", p.am ? "yes" : "no", p.n_waves, p.max_items, p.max_slots,
+                 static_cast<unsigned long long>(off));
   return ok();
 }
 
@@ -829,6 +850,11 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   what = "join";
   if (side && (e = cudaStreamWaitEvent(st, ex->ev_join, 0)) != cudaSuccess) goto launch_fail;
   what = "backward";
+  if (log_enabled())
+    std::fprintf(stderr, "[bsa] grad run: kernel=%s dQ=%s\n",
+                 k64 ? "k_bwd_k64 (64-key blocks)"
+                     : (p.win || p.am ? "k_bwd (element masks)" : "k_bwd"),
+                 p.det ? "deterministic query-tile pass (k_bwd_dq)" : "fp32 reduce-add + k_finalize");
   if (ex->ev_before && (e = cudaEventRecord(ex->ev_before, st)) != cudaSuccess) goto launch_fail;
   if ((e = k64 ? launch_bwd_k64(p, maps, st) : launch_bwd(p, maps, st)) != cudaSuccess)
     goto launch_fail;
@@ -851,6 +877,12 @@ bsa_status bsa_check_status(const void* workspace, void* stream) {
   cudaError_t e = cudaStreamSynchronize(st);
   if (e == cudaSuccess) e = cudaMemcpy(hdr, workspace, sizeof(hdr), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "CUDA error: %s", cudaGetErrorString(e));
+  if (log_enabled())
+    std::fprintf(stderr,
+                 "[bsa] status: active tiles=%d work items=%d split columns=%d chunk=%d "
+                 "finalize tiles=%d error=%d where=%d\n",
+                 hdr[kHdrTotalTiles], hdr[kHdrNumItems], hdr[kHdrSlotsUsed], hdr[kHdrChunkLen],
+                 hdr[kHdrFinTiles], hdr[kHdrError], hdr[kHdrErrorWhere]);
   if (hdr[kHdrError] != 0)
     return fail(BSA_ERR_INNER, "a kernel gave up a bounded wait (code %d)", hdr[kHdrErrorWhere]);
   return ok();

@@ -243,7 +243,12 @@ bsa_status bsa_mask_compact_noalloc(const bsa_tensor* block_sparse_mask, int64_t
 
 /* Synchronizes `stream`, then reads the error word a run call left at the start
  * of `workspace`: BSA_OK, or BSA_ERR_INNER if a kernel gave up a bounded wait
- * (the outputs are then not valid). 361001 if the CUDA calls fail. */
+ * (the outputs are then not valid). 361001 if the CUDA calls fail.
+ * Logging (the pages' call example logs through LOG_PRINT; here an environment
+ * switch): with BSA_LOG set to anything but "0", this call prints the backward
+ * work-list counts of the workspace (active tiles, work items, split columns),
+ * bsa_grad_workspace_size the plan and bsa_grad the kernels and dQ mode it
+ * launches, one line each on stderr. */
 bsa_status bsa_check_status(const void* workspace, void* stream);
 
 /* The same error words without a host synchronization: enqueues on `stream` a
