@@ -279,57 +279,77 @@ def e2e_pipelined(t, outs, size_of, launch, n_steps):
     device, runs both stages of the library call (`size_of(inputs, outputs)`
     gives the workspace size, `launch(inputs, outputs, ws, size, stream)` runs
     the first and second stage) and reads the outputs `outs` back into pinned
-    host memory. Two device buffer sets alternate, and the copies run on their
-    own streams, so the host-to-device copy of step i+1 and the read-back of
-    step i-1 overlap the compute of step i. Returns (ms per step, H2D bytes,
+    host memory. The inputs sit packed in one pinned host buffer and, per
+    buffer set, one device buffer (the outputs likewise), so each direction is
+    one copy per step; two device buffer sets alternate, and the copies run on
+    their own streams, so the host-to-device copy of step i+1 and the
+    read-back of step i-1 overlap the compute of step i. Returns (ms per step, H2D bytes,
     D2H bytes per step), timed with CUDA events from the first copy to the
     last read-back."""
     import torch
 
     import block_sparse_attention_attn_gb300 as bsa
     compute = torch.cuda.current_stream()
-    s_in = [torch.cuda.Stream() for _ in range(N_COPY_STREAMS)]
-    s_out = [torch.cuda.Stream() for _ in range(N_COPY_STREAMS)]
-    host = {k_: x.cpu().pin_memory() for k_, x in t.items() if x is not None}
+    dev = outs[0].device
+
+    def layout(tensors):
+        """Byte offsets of the tensors packed back to back (256-byte aligned)."""
+        offs, off = [], 0
+        for x in tensors:
+            offs.append(off)
+            off += (x.numel() * x.element_size() + 255) // 256 * 256
+        return offs, max(off, 256)
+
+    def carve(flat, like, off):
+        n = like.numel() * like.element_size()
+        return flat[off:off + n].view(like.dtype).view(like.shape)
+
+    # the inputs packed in one pinned host buffer and, per buffer set, one
+    # device buffer, so each step moves its inputs with one copy and its
+    # outputs with one read-back
+    names = [k_ for k_, x in t.items() if x is not None]
+    in_offs, in_bytes = layout([t[k_] for k_ in names])
+    out_offs, out_bytes = layout(outs)
+    h_in = torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True)
+    for k_, off in zip(names, in_offs):
+        carve(h_in, t[k_], off).copy_(t[k_].cpu())
     sets = []
     for k in range(2):
-        ti = dict(t) if k == 0 else {k_: (None if x is None else x.clone()) for k_, x in t.items()}
-        oi = tuple(outs) if k == 0 else tuple(torch.empty_like(x) for x in outs)
+        d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        d_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        ti = {k_: None for k_ in t}
+        for k_, off in zip(names, in_offs):
+            ti[k_] = carve(d_in, t[k_], off)
+        oi = tuple(carve(d_out, x, off) for x, off in zip(outs, out_offs))
+        d_in.copy_(h_in)
         size = size_of(ti, oi)
-        ws = torch.empty(max(size, 256), dtype=torch.uint8, device=outs[0].device)
-        h_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in oi]
-        sets.append((ti, oi, ws, size, h_out))
-    h2d = sum(x.numel() * x.element_size() for x in host.values())
-    d2h = sum(x.numel() * x.element_size() for x in sets[0][4])
-    ns = N_COPY_STREAMS
-    ev_in = [[torch.cuda.Event() for _ in range(ns)] for _ in range(2)]
+        ws = torch.empty(max(size, 256), dtype=torch.uint8, device=dev)
+        h_out = torch.empty(out_bytes, dtype=torch.uint8, pin_memory=True)
+        sets.append((ti, oi, ws, size, d_in, d_out, h_out))
+    h2d = sum(t[k_].numel() * t[k_].element_size() for k_ in names)
+    d2h = sum(x.numel() * x.element_size() for x in outs)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_c = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [[torch.cuda.Event() for _ in range(ns)] for _ in range(2)]
-    names = list(host)
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def run(i):
         k = i % 2
-        ti, oi, ws, size, h_out = sets[k]
-        for j, st in enumerate(s_in):
-            with torch.cuda.stream(st):
-                if i >= 2:
-                    st.wait_event(ev_c[k])    # step i-2 has read this set's inputs
-                for k_ in names[j::ns]:
-                    ti[k_].copy_(host[k_], non_blocking=True)
-                ev_in[k][j].record(st)
-        for e in ev_in[k]:
-            compute.wait_event(e)
+        ti, oi, ws, size, d_in, d_out, h_out = sets[k]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_c[k])      # step i-2 has read this set's inputs
+            d_in.copy_(h_in, non_blocking=True)
+            ev_in[k].record(s_in)
+        compute.wait_event(ev_in[k])
         if i >= 2:
-            for e in ev_out[k]:
-                compute.wait_event(e)         # step i-2's outputs have been read back
+            compute.wait_event(ev_out[k])     # step i-2's outputs have been read back
         launch(ti, oi, ws, size, compute)
         ev_c[k].record(compute)
-        for j, st in enumerate(s_out):
-            with torch.cuda.stream(st):
-                st.wait_event(ev_c[k])
-                for hd, dd in list(zip(h_out, oi))[j::ns]:
-                    hd.copy_(dd, non_blocking=True)
-                ev_out[k][j].record(st)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_c[k])
+            h_out.copy_(d_out, non_blocking=True)
+            ev_out[k].record(s_out)
 
     for i in range(2):                        # warm-up
         run(i)
@@ -337,23 +357,17 @@ def e2e_pipelined(t, outs, size_of, launch, n_steps):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(compute)
-    for st in s_in:
-        st.wait_event(start)
+    s_in.wait_event(start)
     for i in range(2, 2 + n_steps):
         run(i)
-    for st in s_out:                          # after the last read-backs
-        compute.wait_stream(st)
+    compute.wait_stream(s_out)                # after the last read-backs
     end.record(compute)
     torch.cuda.synchronize()
-    for ti, oi, ws, size, h_out in sets:
-        bsa.bsa_check_status(ws)
+    for st_ in sets:
+        bsa.bsa_check_status(st_[2])
     return start.elapsed_time(end) / n_steps, h2d, d2h
 
 
-# Copy streams per direction in the end-to-end measurement (2, 4 or 6 were
-# measured no faster: the host link, not the number of copy streams, sets the
-# copy time).
-N_COPY_STREAMS = 1
 
 
 # The other configurations of the workload table, timed in the same run
@@ -474,7 +488,8 @@ def bench_ours(args, rank, world, local):
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "schedule": "two device buffer sets; the H2D copy of step i+1 and the D2H "
+                "schedule": "inputs and outputs packed (one copy each way per step); two device "
+                            "buffer sets; the H2D copy of step i+1 and the D2H "
                             "read-back of step i-1 run on copy streams during step i"},
         # per step: info upload, mask compaction (count, fill), planner,
         # preprocess, backward, finalize
@@ -599,7 +614,8 @@ def bench_forward(args, rank, world, local):
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "schedule": "two device buffer sets; the H2D copy of step i+1 and the D2H "
+                "schedule": "inputs and outputs packed (one copy each way per step); two device "
+                            "buffer sets; the H2D copy of step i+1 and the D2H "
                             "read-back of step i-1 run on copy streams during step i"},
         "gpu_launches": (3 if w.atten_mask is not None else 2) * n,  # info upload, [mask packing,] forward
         "clocks": clk,
