@@ -806,9 +806,23 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
               !encode_map(&maps.v64, ex->v, g.dtype, g.layout, g.D, rows_k, heads_k, 64)))
     return fail(BSA_ERR_RUNTIME, "cuTensorMapEncodeTiled failed");
 
-  cudaError_t e = launch_upload(ex->info.data(), (int)ex->info.size(),
-                                reinterpret_cast<int*>(ws + ex->off_info), st);
-  if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "copy of sequence info: %s", cudaGetErrorString(e));
+  // The per-batch arrays go inline into the parameters of the two kernels that
+  // start the run (the column count stores the workspace copy); longer ones
+  // are uploaded first.
+  InfoInline info;
+  const bool inl = ex->info.size() <= (size_t)kInfoInline;
+  cudaError_t e = cudaSuccess;
+  if (inl) {
+    info.n = (int)ex->info.size();
+    for (int i = 0; i < 7; ++i) info.off[i] = ex->n_info_off[i];
+    info.dst = reinterpret_cast<int*>(ws + ex->off_info);
+    std::memcpy(info.v, ex->info.data(), ex->info.size() * sizeof(int));
+  } else {
+    e = launch_upload(ex->info.data(), (int)ex->info.size(), reinterpret_cast<int*>(ws + ex->off_info),
+                      st);
+    if (e != cudaSuccess) return fail(BSA_ERR_RUNTIME, "copy of sequence info: %s", cudaGetErrorString(e));
+  }
+  const InfoInline* ip = inl ? &info : nullptr;
   set_amask_ptrs(ex, p, ws);
   CompactArgs ca{};
   ca.mask = p.mask; ca.sb = p.mask_sb; ca.sh = p.mask_sh; ca.si = p.mask_si;
@@ -839,14 +853,14 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   what = "token mask packing";
   if ((e = launch_amask_for(ex, p, ws, cs)) != cudaSuccess) goto launch_fail;
   what = "column count";
-  if ((e = launch_columns(ca, 0, cs)) != cudaSuccess) goto launch_fail;
+  if ((e = launch_columns(ca, 0, cs, ip)) != cudaSuccess) goto launch_fail;
   what = "planner";
   if ((e = launch_plan(p, cs)) != cudaSuccess) goto launch_fail;
   what = "column fill";
   if ((e = launch_columns(ca, 1, cs)) != cudaSuccess) goto launch_fail;
   if (side && (e = cudaEventRecord(ex->ev_join, side)) != cudaSuccess) goto launch_fail;
   what = "preprocess";
-  if ((e = launch_preprocess(p, st)) != cudaSuccess) goto launch_fail;
+  if ((e = launch_preprocess(p, st, ip)) != cudaSuccess) goto launch_fail;
   what = "join";
   if (side && (e = cudaStreamWaitEvent(st, ex->ev_join, 0)) != cudaSuccess) goto launch_fail;
   what = "backward";

@@ -8,6 +8,7 @@
 //     and lse*log2(e), plus zeroing of the fp32 dQ accumulator;
 //   * the finalize kernels: fp32 dQ (and split-column dK/dV) -> output dtype,
 //     zeros for padding rows and for key tiles no query selects.
+#include <algorithm>
 #include <cstring>
 
 #include <cuda_bf16.h>
@@ -51,7 +52,7 @@ __device__ __forceinline__ int tile_bits(const CompactArgs& a, int b, int h, int
 
 // One warp per column (b, g, jt, hl) with index ((b*N2+g)*col_slots + jt)*G + hl.
 // fill == 0: counts[col] = active tiles; fill == 1: writes the entries.
-__global__ void k_columns(CompactArgs a, int fill) {
+__device__ __forceinline__ void columns_body(const CompactArgs& a, int fill) {
   if (fill && a.zero != nullptr) {  // e.g. the fp32 slots of split columns
     const int64_t n4 = (int64_t)(*a.zero_count) * a.zero_per / 4;
     float4* z = reinterpret_cast<float4*>(a.zero);
@@ -89,6 +90,20 @@ __global__ void k_columns(CompactArgs a, int fill) {
     }
   }
   if (!fill && lane == 0) a.counts[col] = count;
+}
+
+__global__ void k_columns(CompactArgs a, int fill) {
+  columns_body(a, fill);
+}
+
+// The column count of a backward run with the per-batch arrays inline: block 0
+// also stores them into the workspace for the kernels after this one.
+__global__ void k_columns_info(CompactArgs a, const __grid_constant__ InfoInline info) {
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < info.n; i += blockDim.x) info.dst[i] = info.v[i];
+  a.lq = info.v + info.off[0];
+  a.lk = info.v + info.off[1];
+  columns_body(a, 0);
 }
 
 // One warp per row (b, h, it) with index (b*N1+h)*row_slots + it.
@@ -347,7 +362,13 @@ __device__ __forceinline__ float2 to_f2<__half>(uint32_t u) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256) k_preprocess(Plan p) {
+__global__ void __launch_bounds__(256) k_preprocess(Plan p, const __grid_constant__ InfoInline info) {
+  if (info.n > 0) {  // the per-batch arrays from the parameter, not the workspace
+    p.lq = info.v + info.off[0];
+    p.cu_q = info.v + info.off[2];
+    p.qrow = info.v + info.off[4];
+    p.qtile_b = info.v + info.off[6];
+  }
   constexpr int TPR = D / 8;  // threads per row, 8 elements (16 B) each
   constexpr int RPB = 256 / TPR;
   const int sub = threadIdx.x % TPR;
@@ -587,8 +608,14 @@ cudaError_t launch_upload(const int* host, int n, int* dst, cudaStream_t st) {
 // --------------------------------------------------------------------------
 // launchers
 // --------------------------------------------------------------------------
-cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st) {
+cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st,
+                           const InfoInline* info) {
   const int ncols = a.B * a.N2 * a.col_slots * a.G;
+  if (info != nullptr && info->n > 0 && !fill) {
+    // block 0 stores the per-batch arrays, so the launch has one even with no column
+    k_columns_info<<<std::max((ncols + 7) / 8, 1), 256, 0, st>>>(a, *info);
+    return cudaGetLastError();
+  }
   if (ncols == 0) return cudaSuccess;
   k_columns<<<(ncols + 7) / 8, 256, 0, st>>>(a, fill);
   return cudaGetLastError();
@@ -614,25 +641,25 @@ cudaError_t launch_scan(const int* in, int* out, int n, cudaStream_t st) {
 
 cudaError_t launch_plan(const Plan& p, cudaStream_t st) {
   k_plan<<<1, 1024, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-static cudaError_t launch_pre_t(const Plan& p, cudaStream_t st) {
+static cudaError_t launch_pre_t(const Plan& p, cudaStream_t st, const InfoInline& info) {
   constexpr int RPB = 256 / (D / 8);
   const int64_t rows = (int64_t)p.N1 * p.Rq;
   if (rows == 0) return cudaSuccess;
-  k_preprocess<T, D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, st>>>(p);
+  k_preprocess<T, D><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, st>>>(p, info);
   return cudaGetLastError();
 }
 
-cudaError_t launch_preprocess(const Plan& p, cudaStream_t st) {
+cudaError_t launch_preprocess(const Plan& p, cudaStream_t st, const InfoInline* info) {
+  static const InfoInline none = {};  // n = 0: the workspace copy
+  const InfoInline& in = info != nullptr ? *info : none;
   if (p.dtype == kDtBF16)
-    return p.D == 128 ? launch_pre_t<__nv_bfloat16, 128>(p, st)
-                      : launch_pre_t<__nv_bfloat16, 64>(p, st);
-  return p.D == 128 ? launch_pre_t<__half, 128>(p, st) : launch_pre_t<__half, 64>(p, st);
+    return p.D == 128 ? launch_pre_t<__nv_bfloat16, 128>(p, st, in)
+                      : launch_pre_t<__nv_bfloat16, 64>(p, st, in);
+  return p.D == 128 ? launch_pre_t<__half, 128>(p, st, in) : launch_pre_t<__half, 64>(p, st, in);
 }
 
 template <typename T, int D>

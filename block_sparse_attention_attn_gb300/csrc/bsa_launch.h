@@ -43,7 +43,24 @@ void set_last_error(const char* msg);
 // 7680 ints): the host array may be reused as soon as the call returns, and
 // the upload can be captured in a CUDA graph.
 cudaError_t launch_upload(const int* host, int n, int* dst, cudaStream_t st);
-cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st);
+
+// The per-batch arrays of a run (Plan::lq .. Plan::qtile_b) inline in a kernel
+// parameter, for the two kernels that start a backward run side by side (the
+// column count and the preprocess): neither waits for an upload launch, and
+// the column count copies them to `dst` in the workspace for the kernels that
+// come after it.
+constexpr int kInfoInline = 1024;
+struct InfoInline {
+  int n;        // ints in v; 0: none (the kernels read the workspace copy)
+  int off[7];   // offsets of lq, lk, cu_q, cu_k, qrow, krow, qtile_b in v
+  int* dst;     // the workspace copy
+  int v[kInfoInline];
+};
+
+// Column count (fill = 0) or fill (fill = 1) over the mask. `info` (count
+// only): the per-batch arrays inline, copied to info->dst.
+cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st,
+                           const InfoInline* info = nullptr);
 
 // Packing of the token mask attenMask [rows, cols] (element strides st0, st1;
 // nonzero = masked) into the bit rows and sub-block classes of Plan::am_*.
@@ -61,7 +78,7 @@ cudaError_t launch_amask(const AmaskArgs& a, cudaStream_t st);
 cudaError_t launch_rows(const CompactArgs& a, int fill, cudaStream_t st);
 cudaError_t launch_scan(const int* in, int* out, int n, cudaStream_t st);
 cudaError_t launch_plan(const Plan& p, cudaStream_t st);
-cudaError_t launch_preprocess(const Plan& p, cudaStream_t st);
+cudaError_t launch_preprocess(const Plan& p, cudaStream_t st, const InfoInline* info = nullptr);
 cudaError_t launch_finalize(const Plan& p, cudaStream_t st);
 
 // Tensor maps of the backward / forward kernels (3-D views, 64-element x 128-row
