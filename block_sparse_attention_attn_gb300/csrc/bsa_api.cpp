@@ -397,9 +397,11 @@ struct bsa_executor {
   cudaEvent_t ev_before = nullptr, ev_after = nullptr;  // optional timing of the main kernel
   int k64 = 0;  // 64-key-block backward requested (bsa_executor_set_key_block64)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;      // owned: side-stream compaction
+  cudaEvent_t ev_am = nullptr;                            // owned: token mask packed
   ~bsa_executor() {
     if (ev_fork) cudaEventDestroy(ev_fork);
     if (ev_join) cudaEventDestroy(ev_join);
+    if (ev_am) cudaEventDestroy(ev_am);
   }
   CUtensorMap map_dk{}, map_dv{};  // dK / dV store views (valid when plan.dkv_tma)
 };
@@ -489,13 +491,17 @@ void set_amask_ptrs(const bsa_executor* ex, Plan& p, uint8_t* ws) {
   p.am_sub = ws + ex->off_am_sub;
 }
 
-cudaError_t launch_amask_for(const bsa_executor* ex, const Plan& p, uint8_t* ws, cudaStream_t st) {
+// The bit rows per query (`rows`: the forward and the deterministic dQ pass
+// read them) and per key (`cols`: the backward kernel) are written only where
+// a pass of the run reads them.
+cudaError_t launch_amask_for(const bsa_executor* ex, const Plan& p, uint8_t* ws, cudaStream_t st,
+                             bool rows, bool cols) {
   if (!p.am) return cudaSuccess;
   AmaskArgs a{};
   a.m = ex->am_ptr; a.st0 = ex->am_st0; a.st1 = ex->am_st1;
   a.rows = ex->am_rows; a.cols = ex->am_cols;
-  a.row_bits = reinterpret_cast<uint32_t*>(ws + ex->off_am_row);
-  a.col_bits = reinterpret_cast<uint32_t*>(ws + ex->off_am_col);
+  a.row_bits = rows ? reinterpret_cast<uint32_t*>(ws + ex->off_am_row) : nullptr;
+  a.col_bits = cols ? reinterpret_cast<uint32_t*>(ws + ex->off_am_col) : nullptr;
   a.sub = ws + ex->off_am_sub;
   a.nsub_q = p.Mq_t * 2; a.nsub_k = p.Mk_t * 2;
   a.wk = p.am_wk; a.wq = p.am_wq;
@@ -743,6 +749,10 @@ bsa_status bsa_grad_workspace_size(
     if (ex->ev_fork) cudaEventDestroy(ex->ev_fork);
     ex->ev_fork = ex->ev_join = nullptr;
   }
+  if (ex->ev_fork && p.am && cudaEventCreateWithFlags(&ex->ev_am, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    ex->ev_am = nullptr;  // the preprocess then runs beside the packing
+  }
   *workspace_size = off;
   *executor = ex;
   if (log_enabled())
@@ -851,7 +861,14 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
                (e = cudaStreamWaitEvent(side, ex->ev_fork, 0)) != cudaSuccess))
     goto launch_fail;
   what = "token mask packing";
-  if ((e = launch_amask_for(ex, p, ws, cs)) != cudaSuccess) goto launch_fail;
+  if ((e = launch_amask_for(ex, p, ws, cs, p.det != 0, true)) != cudaSuccess) goto launch_fail;
+  // With a token mask the preprocess starts after its packing: alone the
+  // packing is short, beside the preprocess it waits on memory behind it and
+  // holds up the compaction chain
+  if (side && p.am && ex->ev_am &&
+      ((e = cudaEventRecord(ex->ev_am, side)) != cudaSuccess ||
+       (e = cudaStreamWaitEvent(st, ex->ev_am, 0)) != cudaSuccess))
+    goto launch_fail;
   what = "column count";
   if ((e = launch_columns(ca, 0, cs, ip)) != cudaSuccess) goto launch_fail;
   what = "planner";
@@ -1103,7 +1120,7 @@ bsa_status bsa_fwd(void* workspace, uint64_t workspace_size, bsa_executor* execu
                                 reinterpret_cast<int*>(ws + ex->off_info), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, kHdrWords * 4, st);
   set_amask_ptrs(ex, f.p, ws);
-  if (e == cudaSuccess) e = launch_amask_for(ex, f.p, ws, st);
+  if (e == cudaSuccess) e = launch_amask_for(ex, f.p, ws, st, true, false);
   if (e == cudaSuccess && ex->ev_before) e = cudaEventRecord(ex->ev_before, st);
   if (e == cudaSuccess) e = launch_fwd(f, maps, st);
   if (e == cudaSuccess && ex->ev_after) e = cudaEventRecord(ex->ev_after, st);

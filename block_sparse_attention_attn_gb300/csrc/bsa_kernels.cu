@@ -140,56 +140,104 @@ __global__ void k_rows(CompactArgs a, int fill) {
 // --------------------------------------------------------------------------
 // token mask packing (attenMaskOptional; 1 = the pair is masked out)
 // --------------------------------------------------------------------------
-// One 256-thread block per 64x64 sub-block (i, j): the bytes go through shared
-// memory once and come out as two 32-bit words per query row (keys
-// 64j .. 64j+63), two per key row (queries 64i .. 64i+63) and the sub-block's
-// class. Positions outside the matrix count as masked. A whole sub-block of a
-// row-contiguous, 16-byte aligned matrix is read 16 bytes per thread.
+// One 256-thread block per strip of kAmStrip 64x64 sub-blocks (i, j0 ..
+// j0 + kAmStrip - 1), out as two 32-bit words per query row and sub-block
+// (keys 64j .. 64j+63), two per key row (queries 64i .. 64i+63) and each
+// sub-block's class. Positions outside the matrix count as masked. Thread
+// (r, q) reads 16 bytes of row r (16-byte loads from a row-contiguous, 16-byte
+// aligned matrix, all of its loads in flight at once; else byte by byte
+// through shared memory) and packs them to 16 bits in registers; the key-row
+// words come from 32x32 bit transposes by warp shuffles.
+constexpr int kAmStrip = 4;
+
+// Four 0/1 bytes of a word -> four bits (byte k -> bit k): the multiplier puts
+// byte k's bit at bit 21 + k and no two partial products share a bit.
+__device__ __forceinline__ uint32_t flag_nibble(uint32_t w) { return ((w * 0x00204081u) >> 21) & 0xFu; }
+
 __global__ void __launch_bounds__(256) k_amask(AmaskArgs a) {
-  __shared__ __align__(16) uint8_t tile[64][80];  // 80-byte rows: 16-byte aligned, fewer conflicts
-  const int i = blockIdx.y, j = blockIdx.x, tid = threadIdx.x;
-  const bool whole = (i + 1) * 64 <= a.rows && (j + 1) * 64 <= a.cols;
-  const bool vec = whole && a.st1 == 1 && (a.st0 & 15) == 0 &&
-                   (reinterpret_cast<uintptr_t>(a.m) & 15) == 0;
-  if (vec) {
-    const int r = tid >> 2, c0 = 16 * (tid & 3);
-    const uint4 u = *reinterpret_cast<const uint4*>(a.m + (int64_t)(i * 64 + r) * a.st0 + j * 64 + c0);
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  __shared__ __align__(16) uint8_t tile[64][80];  // the byte-by-byte path, one sub-block at a time
+  __shared__ uint32_t rw[kAmStrip][64][2];        // [sub-block][row][32-key half] row words
+  const int i = blockIdx.y, j0 = blockIdx.x * kAmStrip, tid = threadIdx.x;
+  const int r = tid >> 2, q = tid & 3, lane = tid & 31, warp = tid >> 5;
+  const bool aligned = a.st1 == 1 && (a.st0 & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.m) & 15) == 0 && (i + 1) * 64 <= a.rows;
+  uint4 u[kAmStrip];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {  // each byte -> 0 or 1 (bit 0 ORs the byte's bits)
-      uint32_t x = w[k];
-      x |= x >> 4;
-      x |= x >> 2;
-      x |= x >> 1;
-      w[k] = x & 0x01010101u;
+  for (int jj = 0; jj < kAmStrip; ++jj) {
+    const int j = j0 + jj;
+    if (aligned && j < a.nsub_k && (j + 1) * 64 <= a.cols)
+      u[jj] = *reinterpret_cast<const uint4*>(a.m + (int64_t)(i * 64 + r) * a.st0 + j * 64 + 16 * q);
+  }
+  uint32_t rb[kAmStrip];  // bits 16q .. 16q+15 of row r of each sub-block
+#pragma unroll
+  for (int jj = 0; jj < kAmStrip; ++jj) {
+    const int j = j0 + jj;
+    rb[jj] = 0xFFFFu;
+    if (j >= a.nsub_k) continue;  // the same for the whole block
+    if (aligned && (j + 1) * 64 <= a.cols) {
+      uint32_t w[4] = {u[jj].x, u[jj].y, u[jj].z, u[jj].w};
+      uint32_t bits = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // each byte -> 0 or 1 (bit 0 ORs the byte's bits)
+        uint32_t x = w[k];
+        x |= x >> 4;
+        x |= x >> 2;
+        x |= x >> 1;
+        bits |= flag_nibble(x & 0x01010101u) << (4 * k);
+      }
+      rb[jj] = bits;
+    } else {
+      __syncthreads();  // the previous sub-block's reads of `tile` are done
+      for (int e = tid; e < 64 * 64; e += 256) {
+        const int rr = e >> 6, c = e & 63;
+        const int s = i * 64 + rr, t = j * 64 + c;
+        uint8_t v = 1;
+        if (s < a.rows && t < a.cols) v = a.m[(int64_t)s * a.st0 + (int64_t)t * a.st1] != 0;
+        tile[rr][c] = v;
+      }
+      __syncthreads();
+      uint32_t bits = 0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) bits |= (uint32_t)tile[r][16 * q + k] << k;
+      rb[jj] = bits;
     }
-    *reinterpret_cast<uint4*>(&tile[r][c0]) = make_uint4(w[0], w[1], w[2], w[3]);
-  } else {
-    for (int e = tid; e < 64 * 64; e += 256) {
-      const int r = e >> 6, c = e & 63;
-      const int s = i * 64 + r, t = j * 64 + c;
-      uint8_t v = 1;
-      if (s < a.rows && t < a.cols) v = a.m[(int64_t)s * a.st0 + (int64_t)t * a.st1] != 0;
-      tile[r][c] = v;
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, rb[jj], 1);
+    if ((q & 1) == 0) {
+      const uint32_t word = rb[jj] | (hi << 16);  // keys 32 (q/2) .. 32 (q/2) + 31 of row r
+      rw[jj][r][q >> 1] = word;
+      if (a.row_bits != nullptr) a.row_bits[(int64_t)(i * 64 + r) * a.wk + 2 * j + (q >> 1)] = word;
     }
   }
   __syncthreads();
-  const int r = tid >> 2, q = tid & 3;  // row / column r, 16-wide quarter q
-  uint32_t rb = 0, cb = 0;
+  if (a.col_bits != nullptr) {
+    // warp w: the 32x32 block of rows 32 rh .. and keys 32 ch .. of sub-blocks
+    // w/4, w/4 + 2; lane L starts with row 32 rh + L and ends with key 32 ch + L
+    const int rh = warp & 1, ch = (warp >> 1) & 1;
+    for (int jj = warp >> 2; jj < kAmStrip; jj += 2) {
+      const int j = j0 + jj;
+      if (j >= a.nsub_k) break;
+      uint32_t x = rw[jj][32 * rh + lane][ch];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    rb |= (uint32_t)tile[r][16 * q + k] << k;
-    cb |= (uint32_t)tile[16 * q + k][r] << k;
+      for (int sh = 16; sh >= 1; sh >>= 1) {
+        const uint32_t m = sh == 16 ? 0x0000FFFFu
+                         : sh == 8  ? 0x00FF00FFu
+                         : sh == 4  ? 0x0F0F0F0Fu
+                         : sh == 2  ? 0x33333333u
+                                    : 0x55555555u;  // keys whose bit `sh` is clear
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, sh);
+        x = (lane & sh) ? ((x & ~m) | ((y & ~m) >> sh)) : ((x & m) | ((y & m) << sh));
+      }
+      a.col_bits[(int64_t)(j * 64 + 32 * ch + lane) * a.wq + 2 * i + rh] = x;
+    }
   }
-  const uint32_t rb_hi = __shfl_down_sync(0xffffffffu, rb, 1);
-  const uint32_t cb_hi = __shfl_down_sync(0xffffffffu, cb, 1);
-  if ((q & 1) == 0) {
-    a.row_bits[(int64_t)(i * 64 + r) * a.wk + 2 * j + (q >> 1)] = rb | (rb_hi << 16);
-    a.col_bits[(int64_t)(j * 64 + r) * a.wq + 2 * i + (q >> 1)] = cb | (cb_hi << 16);
+#pragma unroll
+  for (int jj = 0; jj < kAmStrip; ++jj) {
+    const int j = j0 + jj;
+    if (j >= a.nsub_k) break;
+    const int all = __syncthreads_and(rb[jj] == 0xFFFFu);
+    const int any = __syncthreads_or(rb[jj] != 0u);
+    if (tid == 0) a.sub[(int64_t)i * a.nsub_k + j] = all ? kAmAll : (any ? kAmSome : kAmNone);
   }
-  const int all = __syncthreads_and(rb == 0xFFFFu);
-  const int any = __syncthreads_or(rb != 0u);
-  if (tid == 0) a.sub[(int64_t)i * a.nsub_k + j] = all ? kAmAll : (any ? kAmSome : kAmNone);
 }
 
 // Block-wide exclusive scan of one value per thread (1024 threads).
@@ -623,7 +671,7 @@ cudaError_t launch_columns(const CompactArgs& a, int fill, cudaStream_t st,
 
 cudaError_t launch_amask(const AmaskArgs& a, cudaStream_t st) {
   if (a.nsub_q == 0 || a.nsub_k == 0) return cudaSuccess;
-  k_amask<<<dim3(a.nsub_k, a.nsub_q), 256, 0, st>>>(a);
+  k_amask<<<dim3((a.nsub_k + kAmStrip - 1) / kAmStrip, a.nsub_q), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

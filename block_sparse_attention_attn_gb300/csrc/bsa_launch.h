@@ -68,8 +68,8 @@ struct AmaskArgs {
   const uint8_t* m;
   int64_t st0, st1;
   int rows, cols;
-  uint32_t* row_bits;  // [nsub_q*64][wk]
-  uint32_t* col_bits;  // [nsub_k*64][wq]
+  uint32_t* row_bits;  // [nsub_q*64][wk] (null: not written)
+  uint32_t* col_bits;  // [nsub_k*64][wq] (null: not written)
   uint8_t* sub;        // [nsub_q][nsub_k]
   int nsub_q, nsub_k;  // 64x64 sub-blocks (2 * tiles each way)
   int wk, wq;          // words per bit row (2*nsub_k, 2*nsub_q)
