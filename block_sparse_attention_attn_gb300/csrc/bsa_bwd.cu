@@ -685,8 +685,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ii.e0 >= ii.e1) { ++itc; continue; }
       const int Lk = p.lk[ii.b];
       const bool t_ok = (ii.jt * 128 + t) < Lk;
+      // the next tile's entry, and (token mask) its sub-block classes and this
+      // thread's mask words, are loaded one tile ahead: each depends on the
+      // one before, and they would otherwise stall the start of every tile
+      int32_t ent_n = p.entries[ii.e0];
+      uint32_t cls01_n = 0, cls23_n = 0;  // class bytes of the tile's 2x2 sub-blocks
+      uint2 amw_n = make_uint2(0u, 0u);
+      auto am_prefetch = [&](int32_t en) {
+        const int itn = entry_it(en);
+        const uint8_t* sc = p.am_sub + (int64_t)(2 * itn) * p.am_sk + 2 * ii.jt;
+        cls01_n = *reinterpret_cast<const uint16_t*>(sc);
+        cls23_n = *reinterpret_cast<const uint16_t*>(sc + p.am_sk);
+        amw_n = *reinterpret_cast<const uint2*>(p.am_col + ((int64_t)ii.jt * 128 + t) * p.am_wq +
+                                                4 * itn + 2 * wg);
+      };
+      if (EM && p.am) am_prefetch(ent_n);
       for (int e = ii.e0; e < ii.e1; ++e) {
-        const int32_t ent = p.entries[e];
+        const int32_t ent = ent_n;
+        const uint32_t cls01 = cls01_n, cls23 = cls23_n;
+        const uint2 amw = amw_n;
+        if (e + 1 < ii.e1) ent_n = p.entries[e + 1];
         const int sub = entry_sub(ent);
         const int s_sub = (p.rb == 2) ? wg : 0;
         const int t_sub = (p.cb == 2) ? (t >> 6) : 0;
@@ -709,13 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             wm1 = bit_range(w.x - 32, w.y - 32);
           }
           if (p.am) {
-            const uint8_t* sc = p.am_sub + (int64_t)(2 * it) * p.am_sk + 2 * ii.jt;
-            if ((sc[0] & sc[1] & sc[p.am_sk] & sc[p.am_sk + 1]) != kAmNone) {
+            const uint32_t c = cls01 & cls23;
+            if (((c & 0xFFu) & (c >> 8)) != (uint32_t)kAmNone) {  // some sub-block has a masked pair
               wcut = true;
-              const uint2 a = *reinterpret_cast<const uint2*>(
-                  p.am_col + (int64_t)(t0 + t) * p.am_wq + 4 * it + 2 * wg);
-              wm0 &= ~a.x;
-              wm1 &= ~a.y;
+              wm0 &= ~amw.x;
+              wm1 &= ~amw.y;
             }
           }
         }
@@ -763,6 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kPReady]);
+        if (EM && p.am && e + 1 < ii.e1) am_prefetch(ent_n);  // ent_n has arrived by now
         if (!mbar_wait<kTagSoftmax>(&bars[kDpFull], n & 1, abort_flag)) { where = kErrWaitDP; break; }
         if (!mbar_wait<kTagSoftmax>(&bars[kDsFree], (n & 1) ^ 1, abort_flag)) { where = kErrWaitMisc; break; }
         tc_fence_after();
