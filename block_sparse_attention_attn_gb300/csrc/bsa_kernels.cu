@@ -527,39 +527,55 @@ template <typename T, int D>
 __device__ __forceinline__ void finalize_dq_rows(const Plan& p) {
   constexpr int TPR = D / 8;
   constexpr int RPB = 256 / TPR;
+  constexpr int kRows = 4;  // rows per thread and pass: their loads are in flight together
   const int sub = threadIdx.x % TPR;
   const int64_t nrows = (p.layout == kLayoutBNSD) ? (int64_t)p.B * p.N1 * p.Sq
                                                   : (int64_t)p.Tq * p.N1;
-  for (int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; row < nrows;
-       row += (int64_t)gridDim.x * RPB) {
-    int b, h, s;
-    int64_t off;
-    if (p.layout == kLayoutBNSD) {
-      s = (int)(row % p.Sq);
-      const int64_t bh = row / p.Sq;
-      h = (int)(bh % p.N1);
-      b = (int)(bh / p.N1);
-      off = b * p.dq_st[0] + h * p.dq_st[1] + s * p.dq_st[2];
-    } else {
-      h = (int)(row % p.N1);
-      const int tok = (int)(row / p.N1);
-      b = batch_of_token(p.cu_q, p.B, tok);
-      s = tok - p.cu_q[b];
-      off = tok * p.dq_st[0] + h * p.dq_st[1];
-    }
-    float x[8];
-    if (s < p.lq[b]) {
-      const float4* src = reinterpret_cast<const float4*>(
-          p.dqacc + ((int64_t)h * p.Rq + p.qrow[b] + s) * D + sub * 8);
-      const float4 a = src[0], c = src[1];
-      x[0] = a.x * p.scale; x[1] = a.y * p.scale; x[2] = a.z * p.scale; x[3] = a.w * p.scale;
-      x[4] = c.x * p.scale; x[5] = c.y * p.scale; x[6] = c.z * p.scale; x[7] = c.w * p.scale;
-    } else {
+  const int64_t stride = (int64_t)gridDim.x * RPB;
+  const int64_t sd = p.dq_st[p.layout == kLayoutBNSD ? 3 : 2];
+  for (int64_t row0 = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; row0 < nrows;
+       row0 += kRows * stride) {
+    int64_t off[kRows];
+    const float* acc[kRows];  // null: a padding row (zeros)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = 0.f;
+    for (int u = 0; u < kRows; ++u) {
+      const int64_t row = row0 + u * stride;
+      acc[u] = nullptr;
+      off[u] = -1;
+      if (row >= nrows) continue;
+      int b, h, s;
+      if (p.layout == kLayoutBNSD) {
+        s = (int)(row % p.Sq);
+        const int64_t bh = row / p.Sq;
+        h = (int)(bh % p.N1);
+        b = (int)(bh / p.N1);
+        off[u] = b * p.dq_st[0] + h * p.dq_st[1] + s * p.dq_st[2];
+      } else {
+        h = (int)(row % p.N1);
+        const int tok = (int)(row / p.N1);
+        b = batch_of_token(p.cu_q, p.B, tok);
+        s = tok - p.cu_q[b];
+        off[u] = tok * p.dq_st[0] + h * p.dq_st[1];
+      }
+      if (s < p.lq[b]) acc[u] = p.dqacc + ((int64_t)h * p.Rq + p.qrow[b] + s) * D + sub * 8;
     }
-    const int64_t sd = p.dq_st[p.layout == kLayoutBNSD ? 3 : 2];
-    store8<T>(p.dq, off + sub * 8 * sd, sd, p.dq_vec != 0, x);
+    float4 a[kRows], c[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      c[u] = a[u];
+      if (acc[u] != nullptr) {
+        a[u] = reinterpret_cast<const float4*>(acc[u])[0];
+        c[u] = reinterpret_cast<const float4*>(acc[u])[1];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      if (off[u] < 0) continue;
+      const float x[8] = {a[u].x * p.scale, a[u].y * p.scale, a[u].z * p.scale, a[u].w * p.scale,
+                          c[u].x * p.scale, c[u].y * p.scale, c[u].z * p.scale, c[u].w * p.scale};
+      store8<T>(p.dq, off[u] + sub * 8 * sd, sd, p.dq_vec != 0, x);
+    }
   }
 }
 
