@@ -15,7 +15,10 @@ from typing import Optional, Sequence
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "lib", "libbsa.so")
+# BSA_LIBRARY=checks selects the bounds-check build (libbsa_checks.so, built by
+# `python -m block_sparse_attention_attn_gb300.build --checks`)
+_LIB_PATH = os.path.join(_HERE, "lib", "libbsa_checks.so" if os.environ.get("BSA_LIBRARY") == "checks"
+                         else "libbsa.so")
 _lib = None
 
 BSA_OK = 0
@@ -50,7 +53,8 @@ def load_library():
         return _lib
     if not os.path.exists(_LIB_PATH):
         raise BsaError(BSA_ERR_RUNTIME, f"{_LIB_PATH} not built; run "
-                       "`python -m block_sparse_attention_attn_gb300.build`")
+                       "`python -m block_sparse_attention_attn_gb300.build`"
+                       + (" --checks" if _LIB_PATH.endswith("_checks.so") else ""))
     lib = ctypes.CDLL(_LIB_PATH)
     P = ctypes.POINTER
     T = P(BsaTensor)

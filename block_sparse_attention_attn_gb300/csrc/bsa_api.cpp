@@ -846,6 +846,13 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.win = p.win; ca.win_pre = p.win_pre; ca.win_next = p.win_next;
   ca.am_sub = p.am ? p.am_sub : nullptr; ca.am_sk = p.am_sk;
   ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
+  ca.check_hdr = p.header; ca.out_cap = p.max_entries;
+#if defined(BSA_CHECKS) && BSA_CHECKS
+  {  // the test of the bounds checks (this build only): one out-of-range entry
+    const char* t = std::getenv("BSA_CHECK_TEST");
+    ca.check_test = (t != nullptr && t[0] == '1') ? 1 : 0;
+  }
+#endif
   // The token-mask packing, the mask compaction and the planner (small or
   // latency-bound launches) run on a high-priority side stream while the
   // preprocess (bandwidth-bound) runs on `st`.
@@ -914,6 +921,13 @@ bsa_status bsa_check_status(const void* workspace, void* stream) {
                  "finalize tiles=%d error=%d where=%d\n",
                  hdr[kHdrTotalTiles], hdr[kHdrNumItems], hdr[kHdrSlotsUsed], hdr[kHdrChunkLen],
                  hdr[kHdrFinTiles], hdr[kHdrError], hdr[kHdrErrorWhere]);
+  if (hdr[kHdrError] != 0 && hdr[kHdrErrorWhere] == kErrBounds) {
+    int check = 0;
+    if (cudaMemcpy(&check, static_cast<const int*>(workspace) + kHdrCheckWhere, sizeof(int),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+      cudaGetLastError();
+    return fail(BSA_ERR_INNER, "a bounds check failed (check %d)", check);
+  }
   if (hdr[kHdrError] != 0)
     return fail(BSA_ERR_INNER, "a kernel gave up a bounded wait (code %d)", hdr[kHdrErrorWhere]);
   return ok();

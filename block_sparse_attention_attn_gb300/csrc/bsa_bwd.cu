@@ -172,7 +172,7 @@ __device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
   int4 it = make_int4(-1, 0, 0, -1);
   if (lane == 0) {
     const int idx = atomicAdd(&p.header[kHdrWorkCounter], 1);
-    if (idx < p.header[kHdrNumItems]) it = p.items[idx];
+    if (idx < p.header[kHdrNumItems]) it = checked_item(p, p.items[idx]);
   }
   it.x = __shfl_sync(0xffffffffu, it.x, 0);
   it.y = __shfl_sync(0xffffffffu, it.y, 0);
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        const int32_t ent = p.entries[e];
+        const int32_t ent = load_entry(p, e);
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
         const int st = n & 1;
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16k + 15 for step k)
         int kq0 = 0, kq1 = 8;
         if (p.cb == 2) {
-          const int sub = entry_sub(p.entries[e]);
+          const int sub = entry_sub(load_entry(p, e));
           const bool h0 = ((sub | (sub >> 2)) & 1) != 0, h1 = ((sub | (sub >> 2)) & 2) != 0;
           if (h0 != h1) {
             kq0 = h0 ? 0 : 4;
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next tile's entry, and (token mask) its sub-block classes and this
       // thread's mask words, are loaded one tile ahead: each depends on the
       // one before, and they would otherwise stall the start of every tile
-      int32_t ent_n = p.entries[ii.e0];
+      int32_t ent_n = load_entry(p, ii.e0);
       uint32_t cls01_n = 0, cls23_n = 0;  // class bytes of the tile's 2x2 sub-blocks
       uint2 amw_n = make_uint2(0u, 0u);
       auto am_prefetch = [&](int32_t en) {
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t ent = ent_n;
         const uint32_t cls01 = cls01_n, cls23 = cls23_n;
         const uint2 amw = amw_n;
-        if (e + 1 < ii.e1) ent_n = p.entries[e + 1];
+        if (e + 1 < ii.e1) ent_n = load_entry(p, e + 1);
         const int sub = entry_sub(ent);
         const int s_sub = (p.rb == 2) ? wg : 0;
         const int t_sub = (p.cb == 2) ? (t >> 6) : 0;
@@ -847,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ii.e0 >= ii.e1) { ++itc; continue; }
       const int Lk = p.lk[ii.b];
       for (int e = ii.e0; e < ii.e1; ++e) {
-        const int32_t ent = p.entries[e];
+        const int32_t ent = load_entry(p, e);
         const int it = entry_it(ent);
         const int h = ii.g * p.G + entry_hl(ent);
         if (!mbar_wait<kTagDrain>(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }

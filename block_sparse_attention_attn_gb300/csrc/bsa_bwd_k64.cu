@@ -138,7 +138,7 @@ __device__ __forceinline__ int4 claim_item(const Plan& p, int lane) {
   int4 it = make_int4(-1, 0, 0, -1);
   if (lane == 0) {
     const int idx = atomicAdd(&p.header[kHdrWorkCounter], 1);
-    if (idx < p.header[kHdrNumItems]) it = p.items[idx];
+    if (idx < p.header[kHdrNumItems]) it = checked_item(p, p.items[idx]);
   }
   it.x = __shfl_sync(0xffffffffu, it.x, 0);
   it.y = __shfl_sync(0xffffffffu, it.y, 0);
@@ -161,7 +161,7 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // block h of the tile in either query block.
 __device__ __forceinline__ int next_visit(const Plan& p, int e, int e1, int h) {
   while (e < e1) {
-    const int sub = entry_sub(p.entries[e]);
+    const int sub = entry_sub(load_entry(p, e));
     if ((((sub | (sub >> 2)) >> h) & 1) != 0) break;
     ++e;
   }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t_live = Lk - (ii.jt * 128 + 64 * hb);
         bool first = true;
         for (int e = next_visit(p, ii.e0, ii.e1, hb); e < ii.e1; e = next_visit(p, e + 1, ii.e1, hb)) {
-          const int32_t ent = p.entries[e];
+          const int32_t ent = load_entry(p, e);
           const int h = ii.g * p.G + entry_hl(ent);
           const int st = n & 1;
           const uint32_t ph = (n >> 1) & 1;
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // a selected sub-block (with two query blocks per tile, the row's own
           // block decides); rows past the query length need no test, their
           // lse rows hold +inf, so P is exactly 0 there
-          const int sub = entry_sub(p.entries[e]);
+          const int sub = entry_sub(load_entry(p, e));
           const bool row_sel = p.rb == 2 ? (((sub >> ((q >> 6) * 2 + hb)) & 1) != 0) : true;
           const uint32_t cm = row_sel ? kmask : 0u;
           const int st = n & 1, bf = n & 1;
@@ -710,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++n;
             continue;
           }
-          const int32_t ent = p.entries[e];
+          const int32_t ent = load_entry(p, e);
           const int h = ii.g * p.G + entry_hl(ent);
           if (!mbar_wait<kTagDrain>(&bars[kDqFull], n & 1, abort_flag)) { where = kErrWaitDQ; break; }
           tc_fence_after();

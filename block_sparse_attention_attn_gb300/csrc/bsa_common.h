@@ -31,6 +31,7 @@ enum HeaderWord {
   kHdrErrorWhere = 6,  // code of the first wait that gave up
   kHdrFinTiles = 7,    // key tiles the finalize kernel writes (unselected or split)
   kHdrDqCounter = 8,   // work-queue head of the deterministic dQ pass
+  kHdrCheckWhere = 9,  // bounds-check build: id of the first check that failed
   kHdrErrorCounts = 16, // [16, 32): number of failed waits per code
   kHdrWords = 64
 };
@@ -50,6 +51,16 @@ enum ErrWhere {
   kErrWaitAcc = 10,
   kErrWaitMisc = 11,
   kErrWaitTest = 12,     // the deliberate wait of the wait_test switch
+  kErrBounds = 13,       // bounds-check build: an index outside its array (see kHdrCheckWhere)
+};
+
+// Checks of the bounds-check build (kHdrCheckWhere).
+enum CheckId {
+  kCheckItem = 1,        // a work item: key tile, entry range or slot out of range
+  kCheckEntry = 2,       // a list entry: query tile or local head out of range
+  kCheckItemPos = 3,     // the planner placing an item past the item list
+  kCheckEntryPos = 4,    // the fill placing an entry past the entry list
+  kCheckFinTile = 5,     // the finalize list naming a key tile or slot out of range
 };
 
 // Entry of a backward work list: query tile `it` of local head `hl`, with the

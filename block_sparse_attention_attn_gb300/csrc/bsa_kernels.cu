@@ -15,6 +15,7 @@
 #include <cuda_fp16.h>
 
 #include "bsa_common.h"
+#include "bsa_device.cuh"
 #include "bsa_launch.h"
 
 namespace bsa {
@@ -84,12 +85,16 @@ __device__ __forceinline__ void columns_body(const CompactArgs& a, int fill) {
       const unsigned ball = __ballot_sync(0xffffffffu, bits != 0);
       if (fill && bits) {
         const int pos = base + count + __popc(ball & ((1u << lane) - 1u));
-        a.out[pos] = a.plain ? it : pack_entry(it, hl, bits);
+        if (kChecks && a.out_cap > 0 && pos >= a.out_cap) check_failed(a.check_hdr, kCheckEntryPos);
+        else a.out[pos] = a.plain ? it : pack_entry(it, hl, bits);
       }
       count += __popc(ball);
     }
   }
   if (!fill && lane == 0) a.counts[col] = count;
+  // the test of the checks: column 0's first entry names a query tile past the last one
+  if (kChecks && fill && a.check_test && col == 0 && lane == 0 && count > 0)
+    a.out[base] = pack_entry(a.row_slots, 0, 1);
 }
 
 __global__ void k_columns(CompactArgs a, int fill) {
@@ -297,6 +302,12 @@ __device__ __forceinline__ int chunk_begin(int n, int chunks, int c) {
 }
 
 __global__ void __launch_bounds__(1024) k_plan(Plan p) {
+  if (threadIdx.x == 0) {  // the error words of the run (before any check of this kernel)
+    p.header[kHdrError] = 0;
+    p.header[kHdrErrorWhere] = 0;
+    p.header[kHdrCheckWhere] = 0;
+    for (int i = 0; i < 16; ++i) p.header[kHdrErrorCounts + i] = 0;
+  }
   // Items are ordered by (wave, length descending): a wave is a run of
   // consecutive (b, kv head) groups (p.n_waves of them, equal counts), and
   // within a wave the longest items go first. Lengths >= kLenB - 1 share a
@@ -376,7 +387,8 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     for (int c = 0; c < chunks; ++c) {
       const int b0 = chunk_begin(n, chunks, c), b1 = chunk_begin(n, chunks, c + 1);
       const int pos = atomicAdd(&hist[key_of(gc, b1 - b0)], 1);
-      p.items[pos] = make_int4(gc, e0 + b0, e0 + b1, info >= 0 ? info : -1);
+      if (kChecks && pos >= p.max_items) check_failed(p.header, kCheckItemPos);
+      else p.items[pos] = make_int4(gc, e0 + b0, e0 + b1, info >= 0 ? info : -1);
     }
   }
   if (threadIdx.x == 0) {
@@ -387,9 +399,6 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     p.header[kHdrChunkLen] = L;
     p.header[kHdrWorkCounter] = 0;
     p.header[kHdrDqCounter] = 0;
-    p.header[kHdrError] = 0;
-    p.header[kHdrErrorWhere] = 0;
-    for (int i = 0; i < 16; ++i) p.header[kHdrErrorCounts + i] = 0;
   }
 }
 
@@ -591,6 +600,10 @@ __device__ __forceinline__ void finalize_dkdv_tiles(const Plan& p) {
   for (int64_t row = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR; row < nrows;
        row += (int64_t)gridDim.x * RPB) {
     const int gc = p.fin_tiles[row / kTile];
+    if (kChecks && !(gc >= 0 && gc < p.NGC && p.colinfo[gc] < p.max_slots)) {
+      check_failed(p.header, kCheckFinTile);
+      continue;
+    }
     const int jt = gc % p.Mk_t;
     const int bg = gc / p.Mk_t;
     const int g = bg % p.N2, b = bg / p.N2;

@@ -244,6 +244,13 @@ bsa_status bsa_mask_compact_noalloc(const bsa_tensor* block_sparse_mask, int64_t
 /* Synchronizes `stream`, then reads the error word a run call left at the start
  * of `workspace`: BSA_OK, or BSA_ERR_INNER if a kernel gave up a bounded wait
  * (the outputs are then not valid). 361001 if the CUDA calls fail.
+ * Bounds-check build (the same ABI, libbsa_checks.so, kernels compiled with
+ * BSA_CHECKS=1): the kernels also validate the work items and list entries they
+ * read; an index outside its array is dropped and reported here as
+ * BSA_ERR_INNER with code 13 in word 6 and the id of the failed check in word 9
+ * (1 work item, 2 list entry, 3 item position, 4 entry position, 5 finalize
+ * tile). In that build only, the environment switch BSA_CHECK_TEST=1 makes the
+ * next bsa_grad plant one out-of-range entry (the test of these checks).
  * Logging (the pages' call example logs through LOG_PRINT; here an environment
  * switch): with BSA_LOG set to anything but "0", this call prints the backward
  * work-list counts of the workspace (active tiles, work items, split columns),

@@ -218,8 +218,10 @@ def test_token_mask_drops_fully_masked_blocks():
     g = [t.to(DEV) for t in (dout, q, k, v)]
     out, lse = run_fwd(w, q, k, v, am)
     dq, dk, dv = (torch.empty_like(g[i]) for i in (1, 2, 3))
-    size, ex = bsa.bsa_grad_workspace_size(*g, out, lse, torch.from_numpy(w.mask).to(DEV),
-                                           torch.from_numpy(am).to(DEV), [128, 128],
+    # the masks stay allocated until the run has read them (the executor keeps
+    # their addresses, as it keeps every tensor's)
+    mask_d, am_d = torch.from_numpy(w.mask).to(DEV), torch.from_numpy(am).to(DEV)
+    size, ex = bsa.bsa_grad_workspace_size(*g, out, lse, mask_d, am_d, [128, 128],
                                            list(w.seq_q), list(w.seq_kv), "BNSD", "BNSD", 2, 1,
                                            w.scale, dq=dq, dk=dk, dv=dv)
     ws = torch.empty(size, dtype=torch.uint8, device=DEV)

@@ -31,6 +31,21 @@ def test_exports_every_declared_symbol(lib):
     assert lib.bsa_version() >= 100
 
 
+def test_checks_build_exports_every_declared_symbol():
+    """The bounds-check variant (kernels compiled with BSA_CHECKS=1) builds and
+    exports the same C ABI."""
+    import ctypes
+    from block_sparse_attention_attn_gb300 import build
+    path = build.build(checks=True)
+    assert path.endswith("libbsa_checks.so")
+    chk = ctypes.CDLL(path)
+    with open(os.path.join(ROOT, "include", "bsa.h")) as f:
+        names = set(re.findall(r"^\s*(?:bsa_status|const char\*|int32_t)\s+(bsa_\w+)\s*\(", f.read(), re.M))
+    for n in sorted(names):
+        assert hasattr(chk, n), n
+    assert chk.bsa_version() >= 100
+
+
 def _t(*shape, dtype=torch.bfloat16):
     return torch.zeros(*shape, dtype=dtype)
 
