@@ -894,11 +894,22 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
                      : (p.win || p.am ? "k_bwd (element masks)" : "k_bwd"),
                  p.det ? "deterministic query-tile pass (k_bwd_dq)" : "fp32 reduce-add + k_finalize");
   if (ex->ev_before && (e = cudaEventRecord(ex->ev_before, st)) != cudaSuccess) goto launch_fail;
+  // The deterministic dQ pass needs only the preprocess and the planner, not
+  // the backward kernel (whose dK / dV it does not touch): on the side stream
+  // beside it, its CTAs take the SMs the other kernel's tail leaves idle.
+  // (The fork / join events are recorded again: the waits above have taken
+  // their earlier states.)
+  if (p.det && side && ((e = cudaEventRecord(ex->ev_fork, st)) != cudaSuccess ||
+                        (e = cudaStreamWaitEvent(side, ex->ev_fork, 0)) != cudaSuccess))
+    goto launch_fail;
   if ((e = k64 ? launch_bwd_k64(p, maps, st) : launch_bwd(p, maps, st)) != cudaSuccess)
     goto launch_fail;
   if (p.det) {
     what = "deterministic dQ";
-    if ((e = launch_bwd_dq(p, maps, st)) != cudaSuccess) goto launch_fail;
+    if ((e = launch_bwd_dq(p, maps, cs)) != cudaSuccess) goto launch_fail;
+    if (side && ((e = cudaEventRecord(ex->ev_join, side)) != cudaSuccess ||
+                 (e = cudaStreamWaitEvent(st, ex->ev_join, 0)) != cudaSuccess))
+      goto launch_fail;
   }
   if (ex->ev_after && (e = cudaEventRecord(ex->ev_after, st)) != cudaSuccess) goto launch_fail;
   what = "finalize";
