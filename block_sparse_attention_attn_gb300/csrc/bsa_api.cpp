@@ -706,7 +706,6 @@ bsa_status bsa_grad_workspace_size(
   }
   p.max_entries = (int)std::max<int64_t>(max_entries, 1);
   p.max_slots = std::min(p.NGC, 2 * num_sms + 1);
-  p.max_items = p.NGC + 2 * num_sms + p.max_slots + 1;
   p.min_chunk = 16;
   {
     // Waves of consecutive (batch, kv head) groups whose dQ accumulator, Q and
@@ -726,6 +725,10 @@ bsa_status bsa_grad_workspace_size(
     nw = std::min<int64_t>(std::max<int64_t>(nw, 1), std::min(32, g.B * g.N2));
     p.n_waves = (int)nw;
   }
+  // work items: one per key tile, or ceil(n / Lw) chunks of a split one; with
+  // chunk lengths Lw >= T / (n_waves * 2 * num_sms) (the planner's shortest, in
+  // the last wave) they number at most NGC + n_waves * 2 * num_sms
+  p.max_items = p.NGC + p.n_waves * 2 * num_sms + p.max_slots + 1;
   // workspace layout
   uint64_t off = align256(kHdrWords * 4);
   ex->off_info = off; off = align256(off + ex->info.size() * 4);

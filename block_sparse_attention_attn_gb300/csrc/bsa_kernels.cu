@@ -293,10 +293,11 @@ __global__ void k_scan(const int* in, int* out, int n) {
 // Backward planner (single block of 1024 threads):
 //  1. colptr = exclusive scan of the grouped column counts;
 //  2. per key tile gc (all G heads of the group): n = its active tiles; a
-//     column longer than the chunk length L (and while partial slots remain)
-//     is split into ceil(n/L) balanced chunks that add into an fp32 slot;
-//  3. items are ordered longest first (counting sort on the item length), so
-//     the persistent CTAs pick the long work before the short work.
+//     column longer than the chunk length of its wave (and while partial
+//     slots remain) is split into balanced chunks that add into an fp32 slot;
+//  3. items are ordered by wave, longest first within a wave (counting sort
+//     on the item length), so the persistent CTAs pick the long work of a
+//     wave before its short work.
 __device__ __forceinline__ int chunk_begin(int n, int chunks, int c) {
   return (int)(((int64_t)c * n) / chunks);
 }
@@ -317,9 +318,9 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
   __shared__ int s_L;
   __shared__ int hist[kKeys];
   const int nbg = p.NGC / p.Mk_t;
+  auto wave_of = [&](int gc) { return (int)((int64_t)(gc / p.Mk_t) * p.n_waves / nbg); };
   auto key_of = [&](int gc, int len) {
-    const int w = (int)((int64_t)(gc / p.Mk_t) * p.n_waves / nbg);
-    return w * kLenB + (kLenB - 1 - min(len, kLenB - 1));
+    return wave_of(gc) * kLenB + (kLenB - 1 - min(len, kLenB - 1));
   };
   int carry = 0;
   for (int base = 0; base < p.NC; base += blockDim.x) {
@@ -340,25 +341,41 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
   for (int i = threadIdx.x; i < kKeys; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int L = s_L;
+  // Chunk length of key tile gc: an item claimed when its wave starts must end
+  // before the work left from there on is done, so the chunks shrink wave by
+  // wave, to half an SM's share of one wave in the last (a long item claimed
+  // late would otherwise run on alone while the other SMs idle).
+  auto chunk_len = [&](int gc) {
+    const int64_t den = (int64_t)p.n_waves * 2 * p.num_sms;
+    const int64_t left = (int64_t)(p.n_waves - wave_of(gc)) * T;
+    return max((int)((left + den - 1) / den), p.min_chunk);
+  };
   // pass 1: split decision, slots, length histogram (descending buckets), and
-  // the list of key tiles the finalize kernel writes (no entries, or split)
+  // the list of key tiles the finalize kernel writes (no entries, or split).
+  // Key tiles are taken from the last one back, so that when slots run short
+  // the late waves, whose long items would end the kernel, still split.
   int slot_carry = 0, fin_carry = 0;
   for (int base = 0; base < p.NGC; base += blockDim.x) {
-    const int gc = base + threadIdx.x;
-    int n = 0;
-    if (gc < p.NGC) n = p.colptr[(gc + 1) * p.G] - p.colptr[gc * p.G];
-    const int want = (n > L) ? 1 : 0;
+    const int r = base + threadIdx.x;
+    const bool valid = r < p.NGC;
+    const int gc = p.NGC - 1 - r;
+    int n = 0, Lw = L;
+    if (valid) {
+      n = p.colptr[(gc + 1) * p.G] - p.colptr[gc * p.G];
+      Lw = chunk_len(gc);
+    }
+    const int want = (valid && n > Lw) ? 1 : 0;
     int tot;
     const int sidx = block_exclusive_scan(want, ws, &tot) + slot_carry;
     slot_carry += tot;
     const int split = want && (sidx < p.max_slots);
-    const int fin = (gc < p.NGC) && (n == 0 || split);
+    const int fin = valid && (n == 0 || split);
     const int fidx = block_exclusive_scan(fin, ws, &tot) + fin_carry;
     fin_carry += tot;
     if (fin) p.fin_tiles[fidx] = gc;
-    if (gc < p.NGC) {
+    if (valid) {
       p.colinfo[gc] = (n == 0) ? -1 : (split ? sidx : -2);
-      const int chunks = split ? (n + L - 1) / L : (n > 0 ? 1 : 0);
+      const int chunks = split ? (n + Lw - 1) / Lw : (n > 0 ? 1 : 0);
       for (int c = 0; c < chunks; ++c) {
         const int len = chunk_begin(n, chunks, c + 1) - chunk_begin(n, chunks, c);
         atomicAdd(&hist[key_of(gc, len)], 1);
@@ -383,7 +400,8 @@ __global__ void __launch_bounds__(1024) k_plan(Plan p) {
     if (info == -1) continue;
     const int e0 = p.colptr[gc * p.G];
     const int n = p.colptr[(gc + 1) * p.G] - e0;
-    const int chunks = info >= 0 ? (n + L - 1) / L : 1;
+    const int Lw = chunk_len(gc);
+    const int chunks = info >= 0 ? (n + Lw - 1) / Lw : 1;
     for (int c = 0; c < chunks; ++c) {
       const int b0 = chunk_begin(n, chunks, c), b1 = chunk_begin(n, chunks, c + 1);
       const int pos = atomicAdd(&hist[key_of(gc, b1 - b0)], 1);
