@@ -148,8 +148,10 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """The backward kernel's sources and those of its work plan (planner
+    kernel, host planning), which set the kernel's memory traffic too."""
     h = hashlib.sha256()
-    for f in ("bsa_bwd.cu", "sm103_ptx.cuh"):
+    for f in ("bsa_bwd.cu", "sm103_ptx.cuh", "bsa_kernels.cu", "bsa_api.cpp"):
         with open(os.path.join(ROOT, "block_sparse_attention_attn_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -706,7 +706,7 @@ bsa_status bsa_grad_workspace_size(
   }
   p.max_entries = (int)std::max<int64_t>(max_entries, 1);
   p.max_slots = std::min(p.NGC, 2 * num_sms + 1);
-  p.min_chunk = 16;
+  p.min_chunk = 20;  // shorter chunks cost more in their slot epilogue than they balance
   {
     // Waves of consecutive (batch, kv head) groups whose dQ accumulator, Q and
     // dO rows (8 bytes per element) fit in about half of L2: items run wave by
