@@ -380,7 +380,7 @@ def e2e_pipelined(t, outs, size_of, launch, n_steps):
 
 
 # The other configurations of the workload table, timed in the same run
-# after the headline one (w1dense: configs[1] with mask = nullptr).
+# after the headline one (w1dense: the w1 shape with mask = nullptr).
 # (record name, workload, mode): mode "grad" is the default backward, "det"
 # the deterministic dQ mode, "k64" the 64-key-block kernel, "fwd" the forward
 OTHER_CONFIGS = [("w1dense", "w1dense", "grad"), ("w2", "w2", "grad"), ("w3", "w3", "grad"),
