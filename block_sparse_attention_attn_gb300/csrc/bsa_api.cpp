@@ -851,7 +851,7 @@ bsa_status bsa_grad(void* workspace, uint64_t workspace_size, bsa_executor* exec
   ca.zero = p.slots; ca.zero_count = p.header + kHdrSlotsUsed; ca.zero_per = 2 * kTile * g.D;
   ca.check_hdr = p.header; ca.out_cap = p.max_entries;
 #if defined(BSA_CHECKS) && BSA_CHECKS
-  {  // the test of the bounds checks (this build only): one out-of-range entry
+  {  // the test of the bounds checks (the bounds-check variant only): one out-of-range entry
     const char* t = std::getenv("BSA_CHECK_TEST");
     ca.check_test = (t != nullptr && t[0] == '1') ? 1 : 0;
   }

@@ -34,7 +34,7 @@ struct CompactArgs {
   float* zero;            // fill pass: optional fp32 region cleared first (or null)
   const int* zero_count;  // device: number of zero_per-float units to clear
   int zero_per;           // floats per unit, a multiple of 4
-  // bounds-check build only: entries past out_cap (0: unchecked) are dropped
+  // bounds-check variant only: entries past out_cap (0: unchecked) are dropped
   // and recorded in check_hdr; check_test plants one out-of-range entry in
   // column 0 (the test of the checks)
   int* check_hdr;

@@ -88,7 +88,7 @@ typedef struct bsa_executor bsa_executor; /* opaque, host side */
  *                                key positions counted from each sequence's start.
  *   block_shape, block_shape_len : host int64 [bx, by, ...]; NULL or len 0 =
  *                                {128, 128}; at least 2 entries, extra entries are
- *                                ignored. This build supports bx, by in {64, 128}.
+ *                                ignored. The library supports bx, by in {64, 128}.
  *   actual_seq_lengths(_kv), n_seq(_kv) : host int64 per-batch valid token counts.
  *                                Required for TND (sum must equal Tq/Tkv);
  *                                optional for BNSD (NULL = Sq/Skv; rows past the
@@ -249,7 +249,7 @@ bsa_status bsa_mask_compact_noalloc(const bsa_tensor* block_sparse_mask, int64_t
  * read; an index outside its array is dropped and reported here as
  * BSA_ERR_INNER with code 13 in word 6 and the id of the failed check in word 9
  * (1 work item, 2 list entry, 3 item position, 4 entry position, 5 finalize
- * tile). In that build only, the environment switch BSA_CHECK_TEST=1 makes the
+ * tile). In that variant only, the environment switch BSA_CHECK_TEST=1 makes the
  * next bsa_grad plant one out-of-range entry (the test of these checks).
  * Logging (the pages' call example logs through LOG_PRINT; here an environment
  * switch): with BSA_LOG set to anything but "0", this call prints the backward

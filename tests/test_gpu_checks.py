@@ -4,7 +4,7 @@ processes so the library choice is read fresh:
 * on small shapes (GQA, two 64-key blocks per tile with the 64-key-block
   kernel, TND, split columns) the whole outputs match the fp64 oracle and no
   check fails;
-* a planted out-of-range list entry (BSA_CHECK_TEST=1, honoured by this build
+* a planted out-of-range list entry (BSA_CHECK_TEST=1, honoured by the bounds-check variant
   only: the fill names a query tile past the last one in column 0) is caught
   by the backward kernel's entry check: the run reports 561002 with check id 2
   (kCheckEntry) in header word 9, nothing faults, and the next run in the same
